@@ -1,0 +1,205 @@
+"""ctypes binding of libdflash.so: the C ABI of include/dflash.h, same names.
+
+Argument marshalling only: torch tensors are passed as raw device pointers
+and the caller's current CUDA stream is passed as the stream handle.  Every
+step of the computation runs in the library's CUDA kernels.  If the shared
+library is missing, loading raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libdflash.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "dflash.h")
+
+DFLASH_F32, DFLASH_BF16, DFLASH_I32 = 0, 1, 2
+DFLASH_ACCEPT_GREEDY, DFLASH_ACCEPT_ALL = 0, 1
+DFLASH_VERIFY_LAST_ONLY = 1
+
+STATUS = {0: "OK", 1: "INVALID_ARG", 2: "CAPACITY", 3: "OOM", 4: "CUDA", 5: "DEVICE_CHECK",
+          6: "TIMEOUT", 7: "UNSUPPORTED", 8: "STATE"}
+
+
+class DFlashError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"dflash status {status} ({STATUS.get(status, '?')}): {msg}")
+        self.status = status
+
+
+class Config(ctypes.Structure):
+    _fields_ = [
+        ("d_model", ctypes.c_int32), ("n_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32), ("ffn_dim", ctypes.c_int32), ("vocab", ctypes.c_int32),
+        ("n_target_layers", ctypes.c_int32), ("n_draft_layers", ctypes.c_int32),
+        ("n_inject", ctypes.c_int32), ("inject_layers", ctypes.c_int32 * 16),
+        ("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float),
+        ("block_size", ctypes.c_int32), ("max_batch", ctypes.c_int32),
+        ("max_ctx", ctypes.c_int32), ("max_rows", ctypes.c_int32),
+        ("max_tree_nodes", ctypes.c_int32), ("dtype", ctypes.c_int32),
+    ]
+
+
+class DTree(ctypes.Structure):
+    _fields_ = [
+        ("tok", ctypes.c_void_p), ("parent", ctypes.c_void_p), ("depth", ctypes.c_void_p),
+        ("anc", ctypes.c_void_p), ("n_nodes", ctypes.c_void_p),
+        ("max_nodes", ctypes.c_int32), ("anc_words", ctypes.c_int32),
+    ]
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int32
+_SIGS = {
+    "dflash_create": ([ctypes.POINTER(Config), ctypes.POINTER(_P)], _I),
+    "dflash_set_weight": ([_P, ctypes.c_char_p, _P, _I, ctypes.POINTER(ctypes.c_int64), _I], _I),
+    "dflash_reset_seq": ([_P, _I, _P], _I),
+    "dflash_verify": ([_P, _I, _P, _P, _I, _P, _I, _P, _P, _P, _P], _I),
+    "dflash_draft_block": ([_P, _I, _P, _P, _P, _I, _P, _P, _P, _P], _I),
+    "dflash_accept_commit": ([_P, _I, _P, _P, _P, ctypes.POINTER(DTree), _I, _P, _P, _P, _P], _I),
+    "dflash_inject_kv": ([_P, _I, _P, _P, _P, _P], _I),
+    "dtree_build": ([_P, _I, _P, _P, _P, _I, _I, ctypes.POINTER(DTree), _P], _I),
+    "dtree_verify": ([_P, _I, _P, ctypes.POINTER(DTree), _P, _P, _P, _P], _I),
+    "dflash_check": ([_P], _I),
+    "dflash_last_error": ([_P], ctypes.c_char_p),
+    "dflash_seq_lengths": ([_P], _P),
+    "dflash_launch_count": ([_P], ctypes.c_int64),
+    "dflash_debug_view": ([_P, ctypes.c_char_p, _I, ctypes.POINTER(_P), ctypes.POINTER(ctypes.c_int64)], _I),
+    "dflash_destroy": ([_P], None),
+}
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def header_functions():
+    """Names of the functions declared in include/dflash.h."""
+    with open(HEADER) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b((?:dflash|dtree)_[a-z_]+)\s*\(", src)))
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads libdflash.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise FileNotFoundError(f"{path} is missing: build it with __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    for name, (args, ret) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ret
+    _lib = lib
+    return lib
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is not None:
+        return stream if isinstance(stream, int) else stream.cuda_stream
+    import torch
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _check(ctx, status: int) -> None:
+    if status != 0:
+        msg = load().dflash_last_error(ctx).decode() if ctx else ""
+        raise DFlashError(status, msg)
+
+
+# ---------------------------------------------------------------------------
+# the C ABI, one wrapper per function (raises DFlashError on a non-OK status)
+# ---------------------------------------------------------------------------
+
+def dflash_create(cfg: Config) -> int:
+    h = _P()
+    st = load().dflash_create(ctypes.byref(cfg), ctypes.byref(h))
+    if st != 0:
+        raise DFlashError(st, "dflash_create rejected the configuration")
+    return h.value
+
+
+def dflash_destroy(ctx: int) -> None:
+    load().dflash_destroy(ctx)
+
+
+def dflash_set_weight(ctx: int, name: str, tensor, dtype: int) -> None:
+    shape = (ctypes.c_int64 * tensor.dim())(*tensor.shape)
+    _check(ctx, load().dflash_set_weight(ctx, name.encode(), _ptr(tensor), dtype, shape, tensor.dim()))
+
+
+def dflash_reset_seq(ctx: int, seq_id: int, stream=None) -> None:
+    _check(ctx, load().dflash_reset_seq(ctx, seq_id, _stream(stream)))
+
+
+def dflash_verify(ctx, batch, seq_ids, tokens, q, q_lens, flags, argmax, margin=None, logits=None,
+                  stream=None) -> None:
+    _check(ctx, load().dflash_verify(ctx, batch, _ptr(seq_ids), _ptr(tokens), q, _ptr(q_lens), flags,
+                                     _ptr(argmax), _ptr(margin), _ptr(logits), _stream(stream)))
+
+
+def dflash_draft_block(ctx, batch, seq_ids, anchor, block, topk=0, topk_ids=None, topk_logp=None,
+                       logits=None, stream=None) -> None:
+    _check(ctx, load().dflash_draft_block(ctx, batch, _ptr(seq_ids), _ptr(anchor), _ptr(block), topk,
+                                          _ptr(topk_ids), _ptr(topk_logp), _ptr(logits),
+                                          _stream(stream)))
+
+
+def dflash_accept_commit(ctx, batch, seq_ids, block, argmax, tree, mode, accept_len, next_anchor,
+                         emitted, stream=None) -> None:
+    tp = ctypes.byref(tree) if tree is not None else None
+    _check(ctx, load().dflash_accept_commit(ctx, batch, _ptr(seq_ids), _ptr(block), _ptr(argmax), tp,
+                                            mode, _ptr(accept_len), _ptr(next_anchor), _ptr(emitted),
+                                            _stream(stream)))
+
+
+def dflash_inject_kv(ctx, n_rows=0, row_seq=None, row_pos=None, hidden=None, stream=None) -> None:
+    _check(ctx, load().dflash_inject_kv(ctx, n_rows, _ptr(row_seq), _ptr(row_pos), _ptr(hidden),
+                                        _stream(stream)))
+
+
+def dtree_build(ctx, batch, anchor, topk_ids, topk_logp, topk, budget, tree: DTree,
+                stream=None) -> None:
+    _check(ctx, load().dtree_build(ctx, batch, _ptr(anchor), _ptr(topk_ids), _ptr(topk_logp), topk,
+                                   budget, ctypes.byref(tree), _stream(stream)))
+
+
+def dtree_verify(ctx, batch, seq_ids, tree: DTree, node_argmax, margin=None, logits=None,
+                 stream=None) -> None:
+    _check(ctx, load().dtree_verify(ctx, batch, _ptr(seq_ids), ctypes.byref(tree), _ptr(node_argmax),
+                                    _ptr(margin), _ptr(logits), _stream(stream)))
+
+
+def dflash_check(ctx) -> None:
+    _check(ctx, load().dflash_check(ctx))
+
+
+def dflash_last_error(ctx) -> str:
+    return load().dflash_last_error(ctx).decode()
+
+
+def dflash_seq_lengths(ctx) -> int:
+    return load().dflash_seq_lengths(ctx)
+
+
+def dflash_launch_count(ctx) -> int:
+    return int(load().dflash_launch_count(ctx))
+
+
+def dflash_debug_view(ctx, name: str, layer: int = 0):
+    p = _P()
+    n = ctypes.c_int64()
+    _check(ctx, load().dflash_debug_view(ctx, name.encode(), layer, ctypes.byref(p), ctypes.byref(n)))
+    return p.value, n.value

@@ -1,0 +1,354 @@
+// Dense projections of the target and of the drafter: out = X . W^T.
+//
+// bf16 storage: tcgen05 tensor-core kernel.  The weight matrix is always the
+// 128-row MMA operand (A) and the token rows are the N operand (B, 16..256
+// wide), so one kernel covers the weight-streaming regime of a 16-row block
+// and the compute-bound regime of a 512-row batch.  Operands are staged in
+// shared memory by TMA (128-byte swizzle) through an mbarrier ring; one
+// thread issues the MMAs, accumulators live in tensor memory and are read
+// back by all four warps.  K may be split across CTAs; every split writes
+// its own fp32 slab and the consumer kernels sum the slabs in a fixed order.
+//
+// f32 storage: a tiled SIMT kernel (fp32 FMA), used by the small fp32 model.
+#include <cstdio>
+#include <cstring>
+
+#include "internal.cuh"
+
+namespace dflash {
+
+constexpr int kMaxSeg = 12;
+
+struct TmapSet {
+  CUtensorMap m[kMaxSeg];
+};
+
+struct TcParams {
+  int M, N, K;
+  int n_seg;
+  int seg_begin[kMaxSeg + 1];
+  int BN, stages, kb_per_split, n_kb;
+  float* out;
+  long long split_stride;
+  int32_t* status;
+};
+
+__global__ void __launch_bounds__(128, 1)
+    gemm_tc_kernel(const __grid_constant__ TmapSet wmaps, const __grid_constant__ CUtensorMap xmap,
+                   const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int BN = p.BN, S = p.stages;
+  const uint32_t a_bytes = 128 * 64 * 2;
+  const uint32_t b_bytes = (uint32_t)BN * 64 * 2;
+  uint8_t* a_s = smem;
+  uint8_t* b_s = smem + S * a_bytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(b_s + S * b_bytes);
+  uint64_t* empty = full + S;
+  uint64_t* accum = empty + S;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * 128, m0 = blockIdx.y * BN;
+  const int kb0 = blockIdx.z * p.kb_per_split;
+  const int kb1 = min(p.n_kb, kb0 + p.kb_per_split);
+  const int nkb = kb1 - kb0;
+  int seg = 0;
+  while (seg + 1 < p.n_seg && p.seg_begin[seg + 1] <= n0) ++seg;
+  const int wrow0 = n0 - p.seg_begin[seg];
+  const uint32_t tmem_cols = BN <= 32 ? 32u : (BN <= 64 ? 64u : (BN <= 128 ? 128u : 256u));
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accum, 1);
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // TMA producer
+    tma_prefetch_desc(&wmaps.m[seg]);
+    tma_prefetch_desc(&xmap);
+    int issued = 0;
+    for (int i = 0; i < nkb; ++i) {
+      const int s = i % S;
+      const uint32_t ph = (uint32_t)(i / S) & 1u;
+      if (!mbar_wait(&empty[s], ph ^ 1u, p.status)) break;
+      mbar_arrive_expect_tx(&full[s], a_bytes + b_bytes);
+      const int kx = (kb0 + i) * 64;
+      tma_load_2d(a_s + s * a_bytes, &wmaps.m[seg], kx, wrow0, &full[s]);
+      tma_load_2d(b_s + s * b_bytes, &xmap, kx, m0, &full[s]);
+      ++issued;
+    }
+    // drain: every issued copy has landed before this thread leaves
+    for (int i = max(0, issued - S); i < issued; ++i)
+      mbar_wait(&full[i % S], (uint32_t)(i / S) & 1u, p.status);
+  } else if (warp == 1 && lane == 0) {
+    // MMA issuer
+    const uint32_t idesc = idesc_bf16_f32(128, BN);
+    for (int i = 0; i < nkb; ++i) {
+      const int s = i % S;
+      const uint32_t ph = (uint32_t)(i / S) & 1u;
+      if (!mbar_wait(&full[s], ph, p.status)) break;
+      tc_fence_after();
+      const uint64_t ad = sw128_desc(smem_u32(a_s + s * a_bytes));
+      const uint64_t bd = sw128_desc(smem_u32(b_s + s * b_bytes));
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        tc_mma_bf16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+      tc_commit(&empty[s]);
+    }
+    tc_commit(accum);
+  }
+
+  // epilogue: TMEM lane = weight row (output feature), column = token row
+  mbar_wait(accum, 0, p.status);
+  __syncwarp();
+  tc_fence_after();
+  const int feat = n0 + warp * 32 + lane;
+  float* outp = p.out + (size_t)blockIdx.z * (size_t)p.split_stride;
+  for (int c = 0; c < BN; c += 16) {
+    float v[16];
+    tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, v);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int t = m0 + c + i;
+      if (t < p.M && feat < p.N) outp[(size_t)t * p.N + feat] = v[i];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, tmem_cols);
+}
+
+// ---------------------------------------------------------------------------
+// fp32 SIMT GEMM (small fp32 models)
+// ---------------------------------------------------------------------------
+struct SegPtrs {
+  const float* w[kMaxSeg];
+  int begin[kMaxSeg + 1];
+  int n;
+};
+
+__global__ void __launch_bounds__(256) gemm_f32_kernel(const float* __restrict__ x, int M, int K,
+                                                       const SegPtrs segs, int N,
+                                                       float* __restrict__ out) {
+  __shared__ float xs[16][64 + 1];
+  __shared__ float wsm[16][64 + 1];
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    for (int i = threadIdx.x; i < 64 * 16; i += 256) {
+      const int r = i / 16, kk = i % 16;
+      const int m = m0 + r, n = n0 + r, k = k0 + kk;
+      xs[kk][r] = (m < M && k < K) ? x[(size_t)m * K + k] : 0.f;
+      float wv = 0.f;
+      if (n < N && k < K) {
+        int s = 0;
+        while (s + 1 < segs.n && segs.begin[s + 1] <= n) ++s;
+        wv = segs.w[s][(size_t)(n - segs.begin[s]) * K + k];
+      }
+      wsm[kk][r] = wv;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = xs[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = wsm[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int m = m0 + ty * 4 + i, n = n0 + tx * 4 + j;
+      if (m < M && n < N) out[(size_t)m * N + n] = acc[i][j];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor [rows][cols] (row-major), box [box_rows][64], 128-byte swizzle.
+static dflash_status get_tmap(dflash_ctx* ctx, const void* ptr, int64_t rows, int64_t cols,
+                              int box_rows, const CUtensorMap** out) {
+  auto key = std::make_tuple(ptr, rows, cols, box_rows);
+  auto it = ctx->tmaps.find(key);
+  if (it != ctx->tmaps.end()) {
+    *out = &it->second;
+    return DFLASH_OK;
+  }
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) {
+    set_error(ctx, "cuTensorMapEncodeTiled entry point unavailable");
+    return DFLASH_E_CUDA;
+  }
+  CUtensorMap m;
+  memset(&m, 0, sizeof(m));
+  cuuint64_t gdim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t gstride[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+  cuuint32_t estride[2] = {1u, 1u};
+  CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), gdim, gstride,
+                  box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error(ctx, "cuTensorMapEncodeTiled failed (%d) rows=%lld cols=%lld box=%d", (int)r,
+              (long long)rows, (long long)cols, box_rows);
+    return DFLASH_E_CUDA;
+  }
+  auto res = ctx->tmaps.emplace(key, m);
+  *out = &res.first->second;
+  return DFLASH_OK;
+}
+
+static int tc_stages(int BN) {
+  const int per = 128 * 64 * 2 + BN * 64 * 2;
+  int budget = (BN <= 32) ? 110 * 1024 : 200 * 1024;  // small tiles: 2 CTAs per SM
+  int s = budget / per;
+  if (s > 8) s = 8;
+  if (s < 2) s = 2;
+  return s;
+}
+
+static size_t tc_smem_bytes(int BN, int stages) {
+  return 1024 + (size_t)stages * (128 * 64 * 2 + BN * 64 * 2) + (2 * stages + 1) * 8 + 16;
+}
+
+dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs& segs,
+                   float* out, int max_splits, int* splits_used, cudaStream_t st) {
+  if (M <= 0) {
+    *splits_used = 1;
+    return DFLASH_OK;
+  }
+  int N = 0;
+  for (int i = 0; i < segs.n; ++i) N += segs.rows[i];
+  if (segs.n < 1 || segs.n > kMaxSeg) return DFLASH_E_INVALID_ARG;
+
+  if (ctx->cfg.dtype == DFLASH_F32) {
+    SegPtrs sp;
+    memset(&sp, 0, sizeof(sp));
+    sp.n = segs.n;
+    sp.begin[0] = 0;
+    for (int i = 0; i < segs.n; ++i) {
+      sp.w[i] = static_cast<const float*>(segs.w[i]);
+      sp.begin[i + 1] = sp.begin[i] + segs.rows[i];
+    }
+    if ((size_t)M * N > ctx->ws_elems) {
+      set_error(ctx, "GEMM output %dx%d exceeds workspace", M, N);
+      return DFLASH_E_CAPACITY;
+    }
+    dim3 grid((N + 63) / 64, (M + 63) / 64);
+    gemm_f32_kernel<<<grid, 256, 0, st>>>(static_cast<const float*>(x), M, K, sp, N, out);
+    DF_LAUNCHED(ctx);
+    *splits_used = 1;
+    return DFLASH_OK;
+  }
+
+  if (K % 64 != 0) {
+    set_error(ctx, "GEMM K=%d is not a multiple of 64", K);
+    return DFLASH_E_UNSUPPORTED;
+  }
+  for (int i = 0; i + 1 < segs.n; ++i)
+    if (segs.rows[i] % 128 != 0) {
+      set_error(ctx, "GEMM segment %d has %d rows (not a multiple of 128)", i, segs.rows[i]);
+      return DFLASH_E_UNSUPPORTED;
+    }
+  const int m_tiles = (M + 255) / 256;
+  int BN = (M + m_tiles - 1) / m_tiles;
+  BN = ((BN + 15) / 16) * 16;
+  if (BN < 16) BN = 16;
+  const int stages = tc_stages(BN);
+  const int n_tiles = (N + 127) / 128;
+  const int n_kb = K / 64;
+  const int ctas = n_tiles * m_tiles;
+  const int per_sm = (BN <= 32) ? 2 : 1;
+  int splits = (per_sm * ctx->sm_count + ctas - 1) / ctas;
+  if (splits > max_splits) splits = max_splits;
+  if (splits > n_kb / 4) splits = n_kb / 4;
+  if (splits < 1) splits = 1;
+  while (splits > 1 && (size_t)splits * M * N > ctx->ws_elems) --splits;
+  if ((size_t)M * N > ctx->ws_elems) {
+    set_error(ctx, "GEMM output %dx%d exceeds workspace", M, N);
+    return DFLASH_E_CAPACITY;
+  }
+  const int kb_per = (n_kb + splits - 1) / splits;
+  splits = (n_kb + kb_per - 1) / kb_per;
+
+  TmapSet maps;
+  memset(&maps, 0, sizeof(maps));
+  TcParams p;
+  memset(&p, 0, sizeof(p));
+  p.seg_begin[0] = 0;
+  for (int i = 0; i < segs.n; ++i) {
+    const CUtensorMap* m = nullptr;
+    DF_TRY(get_tmap(ctx, segs.w[i], segs.rows[i], K, 128, &m));
+    maps.m[i] = *m;
+    p.seg_begin[i + 1] = p.seg_begin[i] + segs.rows[i];
+  }
+  const CUtensorMap* xm = nullptr;
+  DF_TRY(get_tmap(ctx, x, M, K, BN, &xm));
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.n_seg = segs.n;
+  p.BN = BN;
+  p.stages = stages;
+  p.kb_per_split = kb_per;
+  p.n_kb = n_kb;
+  p.out = out;
+  p.split_stride = (long long)M * N;
+  p.status = ctx->dev_status;
+
+  static bool attr_set = false;
+  if (!attr_set) {
+    DF_CUDA_TRY(ctx, cudaFuncSetAttribute(gemm_tc_kernel,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024));
+    attr_set = true;
+  }
+  dim3 grid(n_tiles, m_tiles, splits);
+  gemm_tc_kernel<<<grid, 128, tc_smem_bytes(BN, stages), st>>>(maps, *xm, p);
+  DF_LAUNCHED(ctx);
+  *splits_used = splits;
+  return DFLASH_OK;
+}
+
+}  // namespace dflash

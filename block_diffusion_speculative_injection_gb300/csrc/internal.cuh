@@ -1,0 +1,362 @@
+// Internal declarations of the DFlash GB300 library: context layout,
+// kernel launchers and small PTX wrappers (mbarrier, TMA, tcgen05, mma.sync).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+#include <map>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "../../include/dflash.h"
+
+namespace dflash {
+
+typedef __nv_bfloat16 bf16;
+
+// ---------------------------------------------------------------------------
+// device status word (sticky; read by dflash_check)
+// ---------------------------------------------------------------------------
+enum DevStatus { kDevOk = 0, kDevCapacity = 1, kDevTimeout = 2, kDevCheck = 3 };
+
+__device__ __forceinline__ void set_dev_status(int32_t* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// Iteration bound of every spin-wait on an mbarrier.  try_wait suspends the
+// thread for a hardware-defined interval per call, so this is seconds at most.
+constexpr uint32_t kSpinLimit = 1u << 26;
+
+// ---------------------------------------------------------------------------
+// weights and context
+// ---------------------------------------------------------------------------
+struct WeightRef {
+  const void* ptr = nullptr;
+  int64_t shape[2] = {0, 0};
+  int ndim = 0;
+};
+
+enum PassKind { kPassNone = 0, kPassLinear = 1, kPassTree = 2, kPassDraft = 3 };
+
+struct LayerW {
+  const void *attn_norm, *wq, *wk, *wv, *wo, *ffn_norm, *w_gate, *w_up, *w_down;
+};
+
+}  // namespace dflash
+
+struct dflash_ctx {
+  dflash_config cfg;
+  int device = 0;
+  int sm_count = 0;
+  int esize = 2;  // bytes per stored element (2 bf16, 4 f32)
+
+  std::map<std::string, dflash::WeightRef> weights;
+  std::vector<dflash::LayerW> tl, dl;  // resolved target / draft layer pointers
+  const void *tok_emb = nullptr, *lm_head = nullptr, *final_norm = nullptr;
+  const void *fuse = nullptr, *mask_emb = nullptr, *draft_final_norm = nullptr;
+  bool resolved = false;
+
+  // per-sequence state
+  int32_t* seq_len = nullptr;        // [max_batch] committed length
+  std::vector<int64_t> host_len_ub;  // host upper bound of each slot's length
+  int32_t* dev_status = nullptr;     // [1]
+
+  // caches: [layers][max_batch][n_kv][max_ctx][hd]
+  void *kc = nullptr, *vc = nullptr, *dkc = nullptr, *dvc = nullptr;
+  size_t layer_cache_elems = 0;
+
+  // activations (rows = max_rows)
+  void* capture = nullptr;  // [max_rows][n_inject][d]
+  float* resid = nullptr;   // [max_rows][d]
+  void* xn = nullptr;       // [max_rows][d]  normalised GEMM input
+  void* qb = nullptr;       // [max_rows][H*hd]
+  void* ao = nullptr;       // [max_rows][H*hd] attention output
+  void* act = nullptr;      // [max_rows][F] SwiGLU product
+  void* fb = nullptr;       // [max_rows][d] fused injection feature F
+  void* lm_in = nullptr;    // [max_rows][d] gathered lm_head input
+  float* ws = nullptr;      // GEMM fp32 output / split-K partials
+  size_t ws_elems = 0;
+  float* part_o = nullptr;  // split-KV partial outputs
+  float* part_ml = nullptr;
+  size_t part_rows_cap = 0;  // capacity in (split*row*head) units
+  int32_t* vk_part = nullptr;  // vocab reduction partial ids
+  float* vv_part = nullptr;    // vocab reduction partial values / lse
+  size_t vpart_cap = 0;
+
+  // pass metadata
+  int32_t* pass_seq = nullptr;   // [max_batch]
+  int32_t* pass_ctx = nullptr;   // [max_batch] committed length at pass start
+  int32_t* pass_blk = nullptr;   // [max_batch] block rows of the sequence
+  int32_t* row_pos = nullptr;    // [max_rows] rope position (-1 inactive)
+  int32_t* row_slot = nullptr;   // [max_rows] cache slot
+  int32_t* row_seq = nullptr;    // [max_rows] sequence slot (-1 inactive)
+  int32_t* lm_rows = nullptr;    // [max_rows] rows fed to the lm_head
+  int32_t* inj_seq = nullptr;    // [max_rows] pending injection: slot (-1 none)
+  int32_t* inj_pos = nullptr;    // [max_rows] pending injection: position
+  int32_t* path = nullptr;       // [max_batch][32] accepted tree path (+ old length)
+  float* rope_cos = nullptr;     // [rope_len][hd/2]
+  float* rope_sin = nullptr;
+  int rope_len = 0;
+
+  int last_kind = dflash::kPassNone;
+  int last_batch = 0, last_q = 0;
+  int pending_rows = 0;  // rows of the injection queue (capture rows)
+
+  int64_t launches = 0;
+  std::string last_error;
+  std::map<std::tuple<const void*, int64_t, int64_t, int>, CUtensorMap> tmaps;
+};
+
+namespace dflash {
+
+// ---------------------------------------------------------------------------
+// launchers (each increments ctx->launches per kernel launched)
+// ---------------------------------------------------------------------------
+struct GemmSegs {
+  const void* w[12];
+  int rows[12];
+  int n;
+};
+
+// out[split][M][N] (fp32) = X[M][K] . W^T, W = vertical stack of the segments.
+// Returns the number of K splits used (the caller reduces them).
+dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs& segs,
+                   float* out, int max_splits, int* splits_used, cudaStream_t st);
+
+enum MaskKind { kMaskNone = 0, kMaskCausal = 1, kMaskTree = 2 };
+
+struct AttnArgs {
+  const void* q;      // [rows][H][hd]
+  void* out;          // [rows][H*hd]
+  const void* kc;     // layer cache base [max_batch][Hkv][max_ctx][hd]
+  const void* vc;
+  int batch, q_stride;  // rows of sequence b: b*q_stride + j, j < pass_blk[b]
+  int mask;
+  const uint64_t* anc;  // tree: [batch][q_stride][anc_words]
+  int anc_words;
+  int64_t max_keys_ub;  // host upper bound on ctx+blk keys of any sequence
+};
+dflash_status attention(dflash_ctx* ctx, const AttnArgs& a, cudaStream_t st);
+
+// row operations
+dflash_status launch_pass_setup_full(dflash_ctx* ctx, int batch, const int32_t* seq_ids, int q,
+                                     const int32_t* q_lens, const int32_t* depth,
+                                     const int32_t* n_nodes, int kind, int last_only,
+                                     const int32_t* anchor, int32_t* block_out, int32_t* pseq,
+                                     int32_t* pctx, int32_t* pblk, cudaStream_t st);
+dflash_status launch_embed(dflash_ctx* ctx, const int32_t* tokens, int rows, int draft_block,
+                           int block, cudaStream_t st);
+dflash_status launch_resid_norm(dflash_ctx* ctx, int rows, int splits, const void* gain,
+                                void* out, const int32_t* out_rows, int n_out, void* capture,
+                                int cap_slot, bool add, cudaStream_t st);
+dflash_status launch_qkv_epilogue(dflash_ctx* ctx, int rows, int splits, void* kc, void* vc,
+                                  cudaStream_t st);
+dflash_status launch_swiglu(dflash_ctx* ctx, int rows, int splits, cudaStream_t st);
+dflash_status launch_store_act(dflash_ctx* ctx, int rows, int n, int splits, void* out,
+                               cudaStream_t st);
+dflash_status launch_inject_epilogue(dflash_ctx* ctx, int rows, int splits, int layer0,
+                                     int n_layers, const int32_t* inj_seq,
+                                     const int32_t* inj_pos, cudaStream_t st);
+dflash_status launch_vocab_reduce(dflash_ctx* ctx, int rows, int vocab, const int32_t* row_out,
+                                  int n_out, int topk, int32_t* argmax, float* margin,
+                                  int32_t* topk_ids, float* topk_logp, float* logits_copy,
+                                  cudaStream_t st);
+
+// speculation control
+dflash_status launch_accept_linear(dflash_ctx* ctx, int batch, const int32_t* seq_ids,
+                                   const int32_t* block, const int32_t* argmax, int q, int mode,
+                                   int32_t* accept_len, int32_t* next_anchor, int32_t* emitted,
+                                   cudaStream_t st);
+dflash_status launch_tree_build(dflash_ctx* ctx, int batch, const int32_t* anchor,
+                                const int32_t* ids, const float* logp, int topk, int depth,
+                                int budget, const dtree_buffers* t, cudaStream_t st);
+dflash_status launch_tree_accept(dflash_ctx* ctx, int batch, const int32_t* seq_ids,
+                                 const dtree_buffers* t, const int32_t* argmax,
+                                 int32_t* accept_len, int32_t* next_anchor, int32_t* emitted,
+                                 cudaStream_t st);
+
+void set_error(dflash_ctx* ctx, const char* fmt, ...);
+
+#define DF_CUDA_TRY(ctx, expr)                                                    \
+  do {                                                                            \
+    cudaError_t e__ = (expr);                                                     \
+    if (e__ != cudaSuccess) {                                                     \
+      ::dflash::set_error((ctx), "%s: %s", #expr, cudaGetErrorString(e__));       \
+      return DFLASH_E_CUDA;                                                       \
+    }                                                                             \
+  } while (0)
+
+#define DF_LAUNCHED(ctx)                                                          \
+  do {                                                                            \
+    (ctx)->launches++;                                                            \
+    cudaError_t e__ = cudaGetLastError();                                         \
+    if (e__ != cudaSuccess) {                                                     \
+      ::dflash::set_error((ctx), "launch at %s:%d: %s", __FILE__, __LINE__,       \
+                          cudaGetErrorString(e__));                               \
+      return DFLASH_E_CUDA;                                                       \
+    }                                                                             \
+  } while (0)
+
+#define DF_TRY(expr)                  \
+  do {                                \
+    dflash_status s__ = (expr);       \
+    if (s__ != DFLASH_OK) return s__; \
+  } while (0)
+
+// ---------------------------------------------------------------------------
+// element load/store helpers for the two storage types
+// ---------------------------------------------------------------------------
+template <typename T>
+__device__ __forceinline__ float ld_f(const T* p);
+template <>
+__device__ __forceinline__ float ld_f<float>(const float* p) { return *p; }
+template <>
+__device__ __forceinline__ float ld_f<bf16>(const bf16* p) { return __bfloat162float(*p); }
+
+template <typename T>
+__device__ __forceinline__ void st_f(T* p, float v);
+template <>
+__device__ __forceinline__ void st_f<float>(float* p, float v) { *p = v; }
+template <>
+__device__ __forceinline__ void st_f<bf16>(bf16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait: gives up after ~2 s of wall time (or kSpinLimit polls),
+// records a timeout in the status word and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1; i < kSpinLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 1023u) == 0 && global_ns() - t0 > 2000000000ull) break;
+  }
+  set_dev_status(status, kDevTimeout);
+  return false;
+}
+
+// ---------------------------------------------------------------------------
+// TMA (tiled tensor copies global -> shared)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05 (5th-generation tensor cores, accumulators in tensor memory)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D(tmem) (+)= A(smem desc) * B(smem desc)^T, kind::f16 (bf16 in, fp32 accumulate).
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on an mbarrier once all previously issued tcgen05.mma of this thread complete.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+// 32 lanes x 16 consecutive 32-bit columns per warp.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor of a K-major bf16 tile written by TMA with
+// 128-byte swizzling: rows of 64 elements (128 B), 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr >> 4) & 0x3FFF);  // start address
+  d |= (uint64_t)1 << 16;                      // leading byte offset (unused with swizzle)
+  d |= (uint64_t)(1024 >> 4) << 32;            // stride byte offset: 8 rows x 128 B
+  d |= (uint64_t)1 << 46;                      // descriptor version (sm_100 family)
+  d |= (uint64_t)2 << 61;                      // swizzle mode: 128 B
+  return d;
+}
+
+// Instruction descriptor: kind::f16, D f32, A/B bf16, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(m >> 4) << 24);
+}
+
+}  // namespace dflash

@@ -1,0 +1,496 @@
+// Row-wise kernels of the target / draft passes.  Each consumes the fp32
+// GEMM slabs (summing K splits in a fixed order) and applies what follows
+// the projection: RoPE + KV-cache scatter, SwiGLU, residual add + RMSNorm
+// (+ capture of the injected layers), and the KV-injection scatter.
+#include "internal.cuh"
+
+namespace dflash {
+
+// ---------------------------------------------------------------------------
+// pass setup: per-sequence and per-row metadata of one pass
+// ---------------------------------------------------------------------------
+struct PassSetupArgs {
+  const int32_t* seq_ids;
+  const int32_t* q_lens;
+  const int32_t* depth;    // tree: [batch][q]
+  const int32_t* n_nodes;  // tree: [batch]
+  const int32_t* anchor;   // draft: [batch] (slot 0 of the block)
+  int32_t* block_out;      // draft: [batch][q]
+  const int32_t* seq_len;
+  int32_t *pass_seq, *pass_ctx, *pass_blk;
+  int32_t *row_pos, *row_slot, *row_seq;
+  int32_t *lm_in, *lm_arg, *lm_vec;
+  int batch, q, kind, last_only, max_batch, max_ctx;
+  int32_t* status;
+};
+
+__global__ void pass_setup_kernel(PassSetupArgs a) {
+  __shared__ int s_blk[1024];
+  __shared__ int s_ctx[1024];
+  for (int b = threadIdx.x; b < a.batch; b += blockDim.x) {
+    const int seq = a.seq_ids[b];
+    int blk = 0, ctx = 0;
+    if (seq < 0 || seq >= a.max_batch) {
+      set_dev_status(a.status, kDevCheck);
+    } else {
+      ctx = a.seq_len[seq];
+      if (a.kind == kPassTree) blk = a.n_nodes[b];
+      else if (a.kind == kPassDraft) blk = a.q;
+      else blk = a.q_lens ? a.q_lens[b] : a.q;
+      if (blk < 0 || blk > a.q) {
+        set_dev_status(a.status, kDevCheck);
+        blk = 0;
+      }
+      if (ctx + blk > a.max_ctx) {
+        set_dev_status(a.status, kDevCapacity);
+        blk = 0;
+      }
+    }
+    a.pass_seq[b] = seq < 0 || seq >= a.max_batch ? 0 : seq;
+    a.pass_ctx[b] = ctx;
+    a.pass_blk[b] = blk;
+    s_blk[b] = blk;
+    s_ctx[b] = ctx;
+    if (a.kind == kPassDraft && a.block_out) a.block_out[(size_t)b * a.q] = a.anchor[b];
+  }
+  __syncthreads();
+  const int rows = a.batch * a.q;
+  for (int r = threadIdx.x; r < rows; r += blockDim.x) {
+    const int b = r / a.q, j = r % a.q;
+    const int blk = s_blk[b], ctx = s_ctx[b];
+    const bool live = j < blk;
+    int pos = ctx + j;
+    if (a.kind == kPassTree && live) {
+      const int d = a.depth[r];
+      if (d < 0 || d > j) set_dev_status(a.status, kDevCheck);
+      pos = ctx + (d < 0 ? 0 : (d > j ? j : d));
+    }
+    a.row_pos[r] = live ? pos : -1;
+    a.row_slot[r] = live ? ctx + j : -1;
+    a.row_seq[r] = live ? a.seq_ids[b] : -1;
+  }
+  // lm_head row maps
+  if (a.kind == kPassDraft) {
+    const int per = a.q - 1;
+    for (int i = threadIdx.x; i < a.batch * per; i += blockDim.x) {
+      const int b = i / per, j = i % per;
+      const int r = b * a.q + 1 + j;
+      a.lm_in[i] = r;
+      a.lm_arg[i] = s_blk[b] > 0 ? r : -1;
+      a.lm_vec[i] = s_blk[b] > 0 ? i : -1;
+    }
+  } else if (a.last_only) {
+    for (int b = threadIdx.x; b < a.batch; b += blockDim.x) {
+      const int r = b * a.q + (s_blk[b] > 0 ? s_blk[b] - 1 : 0);
+      a.lm_in[b] = r;
+      a.lm_arg[b] = s_blk[b] > 0 ? r : -1;
+      a.lm_vec[b] = s_blk[b] > 0 ? r : -1;
+    }
+  } else {
+    for (int r = threadIdx.x; r < rows; r += blockDim.x) {
+      const bool live = (r % a.q) < s_blk[r / a.q];
+      a.lm_in[r] = r;
+      a.lm_arg[r] = live ? r : -1;
+      a.lm_vec[r] = live ? r : -1;
+    }
+  }
+}
+
+dflash_status launch_pass_setup_full(dflash_ctx* ctx, int batch, const int32_t* seq_ids, int q,
+                                     const int32_t* q_lens, const int32_t* depth,
+                                     const int32_t* n_nodes, int kind, int last_only,
+                                     const int32_t* anchor, int32_t* block_out, int32_t* pseq,
+                                     int32_t* pctx, int32_t* pblk, cudaStream_t st) {
+  PassSetupArgs a;
+  a.seq_ids = seq_ids;
+  a.q_lens = q_lens;
+  a.depth = depth;
+  a.n_nodes = n_nodes;
+  a.anchor = anchor;
+  a.block_out = block_out;
+  a.seq_len = ctx->seq_len;
+  a.pass_seq = pseq;
+  a.pass_ctx = pctx;
+  a.pass_blk = pblk;
+  a.row_pos = ctx->row_pos;
+  a.row_slot = ctx->row_slot;
+  a.row_seq = ctx->row_seq;
+  a.lm_in = ctx->lm_rows;
+  a.lm_arg = ctx->lm_rows + ctx->cfg.max_rows;
+  a.lm_vec = ctx->lm_rows + 2 * (size_t)ctx->cfg.max_rows;
+  a.batch = batch;
+  a.q = q;
+  a.kind = kind;
+  a.last_only = last_only;
+  a.max_batch = ctx->cfg.max_batch;
+  a.max_ctx = ctx->cfg.max_ctx;
+  a.status = ctx->dev_status;
+  pass_setup_kernel<<<1, 1024, 0, st>>>(a);
+  DF_LAUNCHED(ctx);
+  return DFLASH_OK;
+}
+
+// ---------------------------------------------------------------------------
+// embedding: resid[r] = tok_emb[token] (target rows) or, for a draft block,
+// slot 0 = tok_emb[anchor], slots 1..B-1 = mask embedding.  Dead rows = 0.
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void embed_kernel(const int32_t* __restrict__ tokens, const T* __restrict__ emb,
+                             const T* __restrict__ mask_emb, const int32_t* __restrict__ row_pos,
+                             float* __restrict__ resid, int d, int vocab, int draft_block,
+                             int block, int32_t* status) {
+  const int r = blockIdx.x;
+  float* out = resid + (size_t)r * d;
+  const T* src = nullptr;
+  if (row_pos[r] >= 0) {
+    int tok;
+    if (draft_block) {
+      const int b = r / block, j = r % block;
+      if (j == 0) tok = tokens[b];
+      else tok = -2;
+    } else {
+      tok = tokens[r];
+    }
+    if (tok == -2) src = mask_emb;
+    else if (tok >= 0 && tok < vocab) src = emb + (size_t)tok * d;
+    else set_dev_status(status, kDevCheck);
+  }
+  for (int i = threadIdx.x; i < d; i += blockDim.x) out[i] = src ? ld_f(src + i) : 0.f;
+}
+
+dflash_status launch_embed(dflash_ctx* ctx, const int32_t* tokens, int rows, int draft_block,
+                           int block, cudaStream_t st) {
+  const int d = ctx->cfg.d_model;
+  if (ctx->cfg.dtype == DFLASH_BF16)
+    embed_kernel<bf16><<<rows, 256, 0, st>>>(tokens, static_cast<const bf16*>(ctx->tok_emb),
+                                             static_cast<const bf16*>(ctx->mask_emb), ctx->row_pos,
+                                             ctx->resid, d, ctx->cfg.vocab, draft_block, block,
+                                             ctx->dev_status);
+  else
+    embed_kernel<float><<<rows, 256, 0, st>>>(tokens, static_cast<const float*>(ctx->tok_emb),
+                                              static_cast<const float*>(ctx->mask_emb),
+                                              ctx->row_pos, ctx->resid, d, ctx->cfg.vocab,
+                                              draft_block, block, ctx->dev_status);
+  DF_LAUNCHED(ctx);
+  return DFLASH_OK;
+}
+
+// ---------------------------------------------------------------------------
+// residual add + RMSNorm (+ capture), and the gathered final norm
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float block_sum(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  float t = 0.f;
+  const int nw = blockDim.x >> 5;
+  for (int i = 0; i < nw; ++i) t += red[i];
+  return t;
+}
+
+constexpr int kNormThreads = 256;
+constexpr int kNormMaxPer = 32;  // d_model <= 8192
+
+template <typename T>
+__global__ void __launch_bounds__(kNormThreads)
+    resid_norm_kernel(float* __restrict__ resid, const float* __restrict__ ws, int splits,
+                      long long split_stride, int d, const T* __restrict__ gain,
+                      T* __restrict__ out, T* __restrict__ capture, int cap_slot, int n_inject,
+                      float eps, int add) {
+  __shared__ float red[32];
+  const int r = blockIdx.x;
+  float x[kNormMaxPer];
+  float ss = 0.f;
+  const int per = (d + kNormThreads - 1) / kNormThreads;
+#pragma unroll
+  for (int k = 0; k < kNormMaxPer; ++k) {
+    if (k >= per) break;
+    const int i = threadIdx.x + k * kNormThreads;
+    float v = 0.f;
+    if (i < d) {
+      v = resid[(size_t)r * d + i];
+      if (add) {
+        for (int s = 0; s < splits; ++s) v += ws[(size_t)s * split_stride + (size_t)r * d + i];
+        resid[(size_t)r * d + i] = v;
+      }
+      if (capture) st_f(capture + ((size_t)r * n_inject + cap_slot) * d + i, v);
+    }
+    x[k] = v;
+    ss += v * v;
+  }
+  if (!out) return;
+  const float tot = block_sum(ss, red);
+  const float inv = rsqrtf(tot / (float)d + eps);
+#pragma unroll
+  for (int k = 0; k < kNormMaxPer; ++k) {
+    if (k >= per) break;
+    const int i = threadIdx.x + k * kNormThreads;
+    if (i < d) st_f(out + (size_t)r * d + i, x[k] * inv * ld_f(gain + i));
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kNormThreads)
+    gather_norm_kernel(const float* __restrict__ resid, const int32_t* __restrict__ rows_in,
+                       int d, const T* __restrict__ gain, T* __restrict__ out, float eps) {
+  __shared__ float red[32];
+  const int i_out = blockIdx.x;
+  const int r = rows_in[i_out];
+  float x[kNormMaxPer];
+  float ss = 0.f;
+  const int per = (d + kNormThreads - 1) / kNormThreads;
+#pragma unroll
+  for (int k = 0; k < kNormMaxPer; ++k) {
+    if (k >= per) break;
+    const int i = threadIdx.x + k * kNormThreads;
+    const float v = (i < d && r >= 0) ? resid[(size_t)r * d + i] : 0.f;
+    x[k] = v;
+    ss += v * v;
+  }
+  const float tot = block_sum(ss, red);
+  const float inv = rsqrtf(tot / (float)d + eps);
+#pragma unroll
+  for (int k = 0; k < kNormMaxPer; ++k) {
+    if (k >= per) break;
+    const int i = threadIdx.x + k * kNormThreads;
+    if (i < d) st_f(out + (size_t)i_out * d + i, x[k] * inv * ld_f(gain + i));
+  }
+}
+
+dflash_status launch_resid_norm(dflash_ctx* ctx, int rows, int splits, const void* gain,
+                                void* out, const int32_t* out_rows, int n_out, void* capture,
+                                int cap_slot, bool add, cudaStream_t st) {
+  const int d = ctx->cfg.d_model;
+  const float eps = ctx->cfg.rms_eps;
+  if (out_rows) {
+    if (ctx->cfg.dtype == DFLASH_BF16)
+      gather_norm_kernel<bf16><<<n_out, kNormThreads, 0, st>>>(
+          ctx->resid, out_rows, d, static_cast<const bf16*>(gain), static_cast<bf16*>(out), eps);
+    else
+      gather_norm_kernel<float><<<n_out, kNormThreads, 0, st>>>(
+          ctx->resid, out_rows, d, static_cast<const float*>(gain), static_cast<float*>(out),
+          eps);
+    DF_LAUNCHED(ctx);
+    return DFLASH_OK;
+  }
+  const long long stride = (long long)rows * d;
+  if (ctx->cfg.dtype == DFLASH_BF16)
+    resid_norm_kernel<bf16><<<rows, kNormThreads, 0, st>>>(
+        ctx->resid, ctx->ws, splits, stride, d, static_cast<const bf16*>(gain),
+        static_cast<bf16*>(out), static_cast<bf16*>(capture), cap_slot, ctx->cfg.n_inject, eps,
+        add ? 1 : 0);
+  else
+    resid_norm_kernel<float><<<rows, kNormThreads, 0, st>>>(
+        ctx->resid, ctx->ws, splits, stride, d, static_cast<const float*>(gain),
+        static_cast<float*>(out), static_cast<float*>(capture), cap_slot, ctx->cfg.n_inject, eps,
+        add ? 1 : 0);
+  DF_LAUNCHED(ctx);
+  return DFLASH_OK;
+}
+
+// ---------------------------------------------------------------------------
+// QKV epilogue: RoPE on Q and K at the row's position; Q -> qb, K/V -> cache
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void qkv_epilogue_kernel(const float* __restrict__ ws, int splits, long long sstride,
+                                    const int32_t* __restrict__ row_pos,
+                                    const int32_t* __restrict__ row_slot,
+                                    const int32_t* __restrict__ row_seq,
+                                    const float* __restrict__ rcos, const float* __restrict__ rsin,
+                                    T* __restrict__ qb, T* __restrict__ kc, T* __restrict__ vc,
+                                    int H, int Hkv, int hd, int max_ctx) {
+  const int r = blockIdx.x;
+  const int pos = row_pos[r];
+  if (pos < 0) return;
+  const int slot = row_slot[r], seq = row_seq[r];
+  const int half = hd / 2;
+  const int N = (H + 2 * Hkv) * hd;
+  const float* src = ws + (size_t)r * N;
+  const int n_pairs = (H + Hkv) * half;  // rotated pairs (Q and K heads)
+  for (int i = threadIdx.x; i < n_pairs + Hkv * hd; i += blockDim.x) {
+    if (i < n_pairs) {
+      const int head = i / half, p = i % half;  // head < H: query, else key
+      const int col = head * hd + p;
+      float lo = 0.f, hi = 0.f;
+      for (int s = 0; s < splits; ++s) {
+        lo += src[(size_t)s * sstride + col];
+        hi += src[(size_t)s * sstride + col + half];
+      }
+      const float c = rcos[(size_t)pos * half + p], sn = rsin[(size_t)pos * half + p];
+      const float olo = lo * c - hi * sn, ohi = hi * c + lo * sn;
+      if (head < H) {
+        T* dst = qb + ((size_t)r * H + head) * hd;
+        st_f(dst + p, olo);
+        st_f(dst + p + half, ohi);
+      } else {
+        const int kh = head - H;
+        T* dst = kc + (((size_t)seq * Hkv + kh) * max_ctx + slot) * hd;
+        st_f(dst + p, olo);
+        st_f(dst + p + half, ohi);
+      }
+    } else {
+      const int v = i - n_pairs;
+      const int kh = v / hd, e = v % hd;
+      const int col = (H + Hkv) * hd + v;
+      float acc = 0.f;
+      for (int s = 0; s < splits; ++s) acc += src[(size_t)s * sstride + col];
+      st_f(vc + (((size_t)seq * Hkv + kh) * max_ctx + slot) * hd + e, acc);
+    }
+  }
+}
+
+dflash_status launch_qkv_epilogue(dflash_ctx* ctx, int rows, int splits, void* kc, void* vc,
+                                  cudaStream_t st) {
+  const dflash_config& c = ctx->cfg;
+  const long long sstride = (long long)rows * (c.n_heads + 2 * c.n_kv_heads) * c.head_dim;
+  if (c.dtype == DFLASH_BF16)
+    qkv_epilogue_kernel<bf16><<<rows, 256, 0, st>>>(
+        ctx->ws, splits, sstride, ctx->row_pos, ctx->row_slot, ctx->row_seq, ctx->rope_cos,
+        ctx->rope_sin, static_cast<bf16*>(ctx->qb), static_cast<bf16*>(kc),
+        static_cast<bf16*>(vc), c.n_heads, c.n_kv_heads, c.head_dim, c.max_ctx);
+  else
+    qkv_epilogue_kernel<float><<<rows, 256, 0, st>>>(
+        ctx->ws, splits, sstride, ctx->row_pos, ctx->row_slot, ctx->row_seq, ctx->rope_cos,
+        ctx->rope_sin, static_cast<float*>(ctx->qb), static_cast<float*>(kc),
+        static_cast<float*>(vc), c.n_heads, c.n_kv_heads, c.head_dim, c.max_ctx);
+  DF_LAUNCHED(ctx);
+  return DFLASH_OK;
+}
+
+// ---------------------------------------------------------------------------
+// SwiGLU: act = SiLU(gate) * up  (GEMM columns: [gate | up])
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void swiglu_kernel(const float* __restrict__ ws, int splits, long long sstride,
+                              int rows, int F, T* __restrict__ act) {
+  const size_t n = (size_t)rows * F;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const size_t r = i / F, f = i % F;
+    float g = 0.f, u = 0.f;
+    for (int s = 0; s < splits; ++s) {
+      g += ws[(size_t)s * sstride + r * 2 * F + f];
+      u += ws[(size_t)s * sstride + r * 2 * F + F + f];
+    }
+    const float silu = g / (1.f + __expf(-g));
+    st_f(act + i, silu * u);
+  }
+}
+
+dflash_status launch_swiglu(dflash_ctx* ctx, int rows, int splits, cudaStream_t st) {
+  const int F = ctx->cfg.ffn_dim;
+  const long long sstride = (long long)rows * 2 * F;
+  const size_t n = (size_t)rows * F;
+  int blocks = (int)((n + 255) / 256);
+  if (blocks > 8 * ctx->sm_count) blocks = 8 * ctx->sm_count;
+  if (ctx->cfg.dtype == DFLASH_BF16)
+    swiglu_kernel<bf16><<<blocks, 256, 0, st>>>(ctx->ws, splits, sstride, rows, F,
+                                                static_cast<bf16*>(ctx->act));
+  else
+    swiglu_kernel<float><<<blocks, 256, 0, st>>>(ctx->ws, splits, sstride, rows, F,
+                                                 static_cast<float*>(ctx->act));
+  DF_LAUNCHED(ctx);
+  return DFLASH_OK;
+}
+
+// out[r][n] = sum of splits, in the storage type
+template <typename T>
+__global__ void store_act_kernel(const float* __restrict__ ws, int splits, long long sstride,
+                                 size_t n, T* __restrict__ out) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    float v = 0.f;
+    for (int s = 0; s < splits; ++s) v += ws[(size_t)s * sstride + i];
+    st_f(out + i, v);
+  }
+}
+
+dflash_status launch_store_act(dflash_ctx* ctx, int rows, int n, int splits, void* out,
+                               cudaStream_t st) {
+  const size_t tot = (size_t)rows * n;
+  int blocks = (int)((tot + 255) / 256);
+  if (blocks > 8 * ctx->sm_count) blocks = 8 * ctx->sm_count;
+  if (ctx->cfg.dtype == DFLASH_BF16)
+    store_act_kernel<bf16><<<blocks, 256, 0, st>>>(ctx->ws, splits, (long long)tot, tot,
+                                                   static_cast<bf16*>(out));
+  else
+    store_act_kernel<float><<<blocks, 256, 0, st>>>(ctx->ws, splits, (long long)tot, tot,
+                                                    static_cast<float*>(out));
+  DF_LAUNCHED(ctx);
+  return DFLASH_OK;
+}
+
+// ---------------------------------------------------------------------------
+// KV injection epilogue: GEMM columns per draft layer l: [K_l (kv) | V_l (kv)]
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void inject_epilogue_kernel(const float* __restrict__ ws, int splits,
+                                       long long sstride, const int32_t* __restrict__ inj_seq,
+                                       const int32_t* __restrict__ inj_pos,
+                                       const float* __restrict__ rcos,
+                                       const float* __restrict__ rsin, T* __restrict__ dkc,
+                                       T* __restrict__ dvc, size_t layer_elems, int layer0,
+                                       int n_layers, int Hkv, int hd, int max_ctx, int max_batch,
+                                       int32_t* status) {
+  const int r = blockIdx.x;
+  const int seq = inj_seq[r], pos = inj_pos[r];
+  if (seq < 0) return;
+  if (seq >= max_batch || pos < 0 || pos >= max_ctx) {
+    set_dev_status(status, kDevCheck);
+    return;
+  }
+  const int half = hd / 2;
+  const int kv = Hkv * hd;
+  const int N = n_layers * 2 * kv;
+  const float* src = ws + (size_t)r * N;
+  const int per_layer = Hkv * half + kv;  // rotated K pairs + V elements
+  for (int i = threadIdx.x; i < n_layers * per_layer; i += blockDim.x) {
+    const int l = i / per_layer, w = i % per_layer;
+    const size_t lbase = (size_t)(layer0 + l) * layer_elems;
+    const int cbase = l * 2 * kv;
+    if (w < Hkv * half) {
+      const int kh = w / half, p = w % half;
+      const int col = cbase + kh * hd + p;
+      float lo = 0.f, hi = 0.f;
+      for (int s = 0; s < splits; ++s) {
+        lo += src[(size_t)s * sstride + col];
+        hi += src[(size_t)s * sstride + col + half];
+      }
+      const float c = rcos[(size_t)pos * half + p], sn = rsin[(size_t)pos * half + p];
+      T* dst = dkc + lbase + (((size_t)seq * Hkv + kh) * max_ctx + pos) * hd;
+      st_f(dst + p, lo * c - hi * sn);
+      st_f(dst + p + half, hi * c + lo * sn);
+    } else {
+      const int v = w - Hkv * half;
+      const int kh = v / hd, e = v % hd;
+      const int col = cbase + kv + v;
+      float acc = 0.f;
+      for (int s = 0; s < splits; ++s) acc += src[(size_t)s * sstride + col];
+      st_f(dvc + lbase + (((size_t)seq * Hkv + kh) * max_ctx + pos) * hd + e, acc);
+    }
+  }
+}
+
+dflash_status launch_inject_epilogue(dflash_ctx* ctx, int rows, int splits, int layer0,
+                                     int n_layers, const int32_t* inj_seq,
+                                     const int32_t* inj_pos, cudaStream_t st) {
+  const dflash_config& c = ctx->cfg;
+  const long long sstride = (long long)rows * n_layers * 2 * c.n_kv_heads * c.head_dim;
+  if (c.dtype == DFLASH_BF16)
+    inject_epilogue_kernel<bf16><<<rows, 256, 0, st>>>(
+        ctx->ws, splits, sstride, inj_seq, inj_pos, ctx->rope_cos, ctx->rope_sin,
+        static_cast<bf16*>(ctx->dkc), static_cast<bf16*>(ctx->dvc), ctx->layer_cache_elems,
+        layer0, n_layers, c.n_kv_heads, c.head_dim, c.max_ctx, c.max_batch, ctx->dev_status);
+  else
+    inject_epilogue_kernel<float><<<rows, 256, 0, st>>>(
+        ctx->ws, splits, sstride, inj_seq, inj_pos, ctx->rope_cos, ctx->rope_sin,
+        static_cast<float*>(ctx->dkc), static_cast<float*>(ctx->dvc), ctx->layer_cache_elems,
+        layer0, n_layers, c.n_kv_heads, c.head_dim, c.max_ctx, c.max_batch, ctx->dev_status);
+  DF_LAUNCHED(ctx);
+  return DFLASH_OK;
+}
+
+}  // namespace dflash

@@ -1,0 +1,288 @@
+"""Host harness over the C ABI: seeded weights on the device, the step loops.
+
+The harness only moves arguments: it uploads the seeded synthetic weights
+(the generator's value pool, gathered on the device into each named tensor),
+allocates the caller-side buffers, and calls the C functions in the order
+the pages give for one step (anchor -> block draft -> one-pass verify ->
+longest-prefix accept -> KV injection), or the DDTree order (draft top-k ->
+heap tree -> tree verify -> accept walk -> injection).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import List, Optional, Sequence
+
+import numpy as np
+import torch
+
+import workloads as wl
+
+from . import capi
+
+
+def config_for(shape: wl.ModelShape, block_size: int, max_batch: int, max_ctx: int,
+               max_rows: int, max_tree_nodes: int = 0) -> capi.Config:
+    c = capi.Config()
+    c.d_model = shape.d_model
+    c.n_heads = shape.n_heads
+    c.n_kv_heads = shape.n_kv_heads
+    c.head_dim = shape.head_dim
+    c.ffn_dim = shape.ffn_dim
+    c.vocab = shape.vocab
+    c.n_target_layers = shape.n_layers
+    c.n_draft_layers = shape.n_draft_layers
+    c.n_inject = shape.n_inject
+    for i, l in enumerate(shape.inject_layers):
+        c.inject_layers[i] = l
+    c.rope_theta = shape.rope_theta
+    c.rms_eps = shape.rms_eps
+    c.block_size = block_size
+    c.max_batch = max_batch
+    c.max_ctx = max_ctx
+    c.max_rows = max_rows
+    c.max_tree_nodes = max_tree_nodes
+    c.dtype = capi.DFLASH_BF16 if shape.dtype == "bf16" else capi.DFLASH_F32
+    return c
+
+
+def device_weights(shape: wl.ModelShape, seed: int = 0, device: str = "cuda"):
+    """Named weight tensors on the device, bytes identical to the generator's."""
+    sw = wl.SyntheticWeights(shape, seed)
+    tdt = torch.bfloat16 if shape.dtype == "bf16" else torch.float32
+    pool = torch.from_numpy(sw.pool()).to(device).to(tdt)
+    widest = max(s[-1] for _, s in sw.specs.items())
+    ext = torch.cat([pool, pool[:widest]])
+    out = {}
+    for name, shp in sw.specs.items():
+        if wl.is_norm(name):
+            out[name] = torch.ones(shp, dtype=tdt, device=device)
+            continue
+        width = shp[-1]
+        off = torch.from_numpy(sw.offsets(name)).to(device)
+        t = ext.unfold(0, width, 1)[off]
+        out[name] = t.reshape(shp).contiguous()
+    return out
+
+
+@dataclass
+class StepOut:
+    block: torch.Tensor        # [b][B] (linear) or tree tokens
+    argmax: torch.Tensor       # [b][q]
+    accept_len: torch.Tensor   # [b]
+    next_anchor: torch.Tensor  # [b]
+    emitted: torch.Tensor      # [b][q]
+
+
+class DFlashEngine:
+    """One library context plus its weights and step buffers."""
+
+    def __init__(self, shape: wl.ModelShape, block_size: int, max_batch: int, max_ctx: int,
+                 max_rows: Optional[int] = None, max_tree_nodes: int = 0, seed: int = 0,
+                 weights=None, device: str = "cuda"):
+        capi.load()
+        self.shape = shape
+        self.B = block_size
+        self.max_batch = max_batch
+        self.max_tree_nodes = max_tree_nodes
+        self.device = device
+        self.max_rows = max_rows or max(max_batch * max(block_size, max_tree_nodes), 1)
+        self.cfg = config_for(shape, block_size, max_batch, max_ctx, self.max_rows, max_tree_nodes)
+        self.dtype_code = self.cfg.dtype
+        self.ctx = capi.dflash_create(self.cfg)
+        self.weights = weights if weights is not None else device_weights(shape, seed, device)
+        for name, t in self.weights.items():
+            capi.dflash_set_weight(self.ctx, name, t, self.dtype_code)
+        i32 = dict(dtype=torch.int32, device=device)
+        mb = max_batch
+        q = max(block_size, max_tree_nodes, 1)
+        self.argmax = torch.empty(self.max_rows, **i32)
+        self.block = torch.empty(mb * block_size, **i32)
+        self.accept_len = torch.empty(mb, **i32)
+        self.next_anchor = torch.empty(mb, **i32)
+        self.emitted = torch.empty(max(self.max_rows, mb * q), **i32)
+        self.margin = torch.empty(self.max_rows, dtype=torch.float32, device=device)
+        if max_tree_nodes:
+            self.tree_mem = dict(
+                tok=torch.empty(mb * max_tree_nodes, **i32),
+                parent=torch.empty(mb * max_tree_nodes, **i32),
+                depth=torch.empty(mb * max_tree_nodes, **i32),
+                anc=torch.empty(mb * max_tree_nodes * ((max_tree_nodes + 63) // 64),
+                                dtype=torch.int64, device=device),
+                n_nodes=torch.empty(mb, **i32),
+                topk_ids=torch.empty(mb * (block_size - 1) * 16, **i32),
+                topk_logp=torch.empty(mb * (block_size - 1) * 16, dtype=torch.float32, device=device),
+            )
+            self.tree = self.make_tree(max_tree_nodes)
+
+    def make_tree(self, max_nodes: int) -> capi.DTree:
+        m = self.tree_mem
+        t = capi.DTree()
+        t.tok, t.parent, t.depth = m["tok"].data_ptr(), m["parent"].data_ptr(), m["depth"].data_ptr()
+        t.anc, t.n_nodes = m["anc"].data_ptr(), m["n_nodes"].data_ptr()
+        t.max_nodes = max_nodes
+        t.anc_words = (max_nodes + 63) // 64
+        return t
+
+    def close(self) -> None:
+        if getattr(self, "ctx", None):
+            capi.dflash_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # -- sequence setup ----------------------------------------------------
+    def seq_ids(self, batch: int) -> torch.Tensor:
+        return torch.arange(batch, dtype=torch.int32, device=self.device)
+
+    def lengths(self, batch: int) -> List[int]:
+        """Committed length of the first ``batch`` sequence slots (syncs)."""
+        v = device_view(capi.dflash_seq_lengths(self.ctx), (self.max_batch,), torch.int32)
+        torch.cuda.synchronize()
+        return v[:batch].tolist()
+
+    def debug_view(self, name: str, layer: int = 0) -> torch.Tensor:
+        """Zero-copy view of an internal buffer (see dflash_debug_view)."""
+        ptr, nbytes = capi.dflash_debug_view(self.ctx, name, layer)
+        es = 2 if self.shape.dtype == "bf16" else 4
+        t = device_view(ptr, (nbytes // es,), torch.bfloat16 if es == 2 else torch.float32)
+        s = self.shape
+        if name == "capture":
+            return t.view(self.max_rows, s.n_inject, s.d_model)
+        return t.view(self.max_batch, s.n_kv_heads, self.cfg.max_ctx, s.head_dim)
+
+    def prefill(self, prompts: Sequence[np.ndarray], chunk: Optional[int] = None) -> torch.Tensor:
+        """Target prefill of each sequence (slot = its index); returns the
+        first generated token of every sequence (the first anchors)."""
+        b = len(prompts)
+        anchors = torch.empty(b, dtype=torch.int32, device=self.device)
+        chunk = chunk or self.max_rows
+        for s, p in enumerate(prompts):
+            capi.dflash_reset_seq(self.ctx, s)
+            sid = torch.tensor([s], dtype=torch.int32, device=self.device)
+            toks = torch.from_numpy(np.asarray(p, dtype=np.int32)).to(self.device)
+            for c0 in range(0, len(p), chunk):
+                part = toks[c0:c0 + chunk].contiguous()
+                q = part.numel()
+                capi.dflash_verify(self.ctx, 1, sid, part, q, None, capi.DFLASH_VERIFY_LAST_ONLY,
+                                   self.argmax)
+                capi.dflash_accept_commit(self.ctx, 1, sid, None, self.argmax, None,
+                                          capi.DFLASH_ACCEPT_ALL, self.accept_len, self.next_anchor,
+                                          self.emitted)
+                capi.dflash_inject_kv(self.ctx)
+            anchors[s:s + 1].copy_(self.next_anchor[:1])
+        return anchors
+
+    # -- one DFlash step -----------------------------------------------------
+    def step(self, seq_ids: torch.Tensor, anchors: torch.Tensor, want_logits: bool = False,
+             draft_override: Optional[torch.Tensor] = None):
+        b = seq_ids.numel()
+        B = self.B
+        block = self.block[: b * B]
+        dlog = vlog = None
+        if want_logits:
+            dlog = torch.empty(b * max(B - 1, 1) * self.shape.vocab, dtype=torch.float32,
+                               device=self.device)
+            vlog = torch.empty(b * B * self.shape.vocab, dtype=torch.float32, device=self.device)
+        capi.dflash_draft_block(self.ctx, b, seq_ids, anchors, block, 0, None, None, dlog)
+        if draft_override is not None:
+            block.view(b, B)[:, 1:].copy_(draft_override)
+        argmax = self.argmax[: b * B]
+        margin = self.margin[: b * B]
+        capi.dflash_verify(self.ctx, b, seq_ids, block, B, None, 0, argmax, margin, vlog)
+        emitted = self.emitted[: b * B]
+        capi.dflash_accept_commit(self.ctx, b, seq_ids, block, argmax, None,
+                                  capi.DFLASH_ACCEPT_GREEDY, self.accept_len[:b],
+                                  self.next_anchor[:b], emitted)
+        capi.dflash_inject_kv(self.ctx)
+        out = StepOut(block.view(b, B), argmax.view(b, B), self.accept_len[:b],
+                      self.next_anchor[:b], emitted.view(b, B))
+        if want_logits:
+            return out, dlog.view(b, max(B - 1, 1), -1), vlog.view(b, B, -1), margin.view(b, B)
+        return out
+
+    def ar_step(self, seq_ids: torch.Tensor, anchors: torch.Tensor):
+        """Plain greedy decoding step: verify the anchor alone, commit it."""
+        b = seq_ids.numel()
+        toks = anchors.contiguous()
+        argmax = self.argmax[:b]
+        capi.dflash_verify(self.ctx, b, seq_ids, toks, 1, None, 0, argmax)
+        capi.dflash_accept_commit(self.ctx, b, seq_ids, toks, argmax, None,
+                                  capi.DFLASH_ACCEPT_GREEDY, self.accept_len[:b],
+                                  self.next_anchor[:b], self.emitted[:b])
+        capi.dflash_inject_kv(self.ctx)
+        return self.next_anchor[:b]
+
+    # -- one DDTree step -----------------------------------------------------
+    def tree_step(self, seq_ids: torch.Tensor, anchors: torch.Tensor, topk: int, budget: int,
+                  want_logits: bool = False):
+        b = seq_ids.numel()
+        B = self.B
+        m = self.tree_mem
+        n = self.max_tree_nodes
+        ids = m["topk_ids"][: b * (B - 1) * topk]
+        lps = m["topk_logp"][: b * (B - 1) * topk]
+        block = self.block[: b * B]
+        capi.dflash_draft_block(self.ctx, b, seq_ids, anchors, block, topk, ids, lps, None)
+        capi.dtree_build(self.ctx, b, anchors, ids, lps, topk, budget, self.tree)
+        argmax = self.argmax[: b * n]
+        margin = self.margin[: b * n]
+        vlog = None
+        if want_logits:
+            vlog = torch.empty(b * n * self.shape.vocab, dtype=torch.float32, device=self.device)
+        capi.dtree_verify(self.ctx, b, seq_ids, self.tree, argmax, margin, vlog)
+        emitted = self.emitted[: b * n]
+        capi.dflash_accept_commit(self.ctx, b, seq_ids, None, argmax, self.tree,
+                                  capi.DFLASH_ACCEPT_GREEDY, self.accept_len[:b],
+                                  self.next_anchor[:b], emitted)
+        capi.dflash_inject_kv(self.ctx)
+        res = dict(ids=ids.view(b, B - 1, topk), logp=lps.view(b, B - 1, topk),
+                   tok=m["tok"][: b * n].view(b, n), parent=m["parent"][: b * n].view(b, n),
+                   depth=m["depth"][: b * n].view(b, n), n_nodes=m["n_nodes"][:b],
+                   anc=m["anc"][: b * n * self.tree.anc_words].view(b, n, -1),
+                   argmax=argmax.view(b, n), margin=margin.view(b, n),
+                   accept_len=self.accept_len[:b], next_anchor=self.next_anchor[:b],
+                   emitted=emitted.view(b, n))
+        if want_logits:
+            res["logits"] = vlog.view(b, n, -1)
+        return res
+
+    # -- whole generations ---------------------------------------------------
+    def generate(self, prompts: Sequence[np.ndarray], n_new: int, mode: str = "dflash",
+                 topk: int = 8, budget: int = 64) -> List[List[int]]:
+        b = len(prompts)
+        sid = self.seq_ids(b)
+        anchors = self.prefill(prompts)
+        outs = [[int(t)] for t in anchors.tolist()]
+        while min(len(o) for o in outs) < n_new:
+            if mode == "ar":
+                anchors = self.ar_step(sid, anchors).clone()
+                for s, t in enumerate(anchors.tolist()):
+                    outs[s].append(int(t))
+                continue
+            if mode == "ddtree":
+                r = self.tree_step(sid, anchors, topk, budget)
+                em = r["emitted"]
+            else:
+                em = self.step(sid, anchors).emitted
+            anchors = self.next_anchor[:b].clone()
+            for s, row in enumerate(em.tolist()):
+                outs[s].extend(int(t) for t in row if t >= 0)
+        return [o[:n_new] for o in outs]
+
+
+class _CudaArray:
+    def __init__(self, ptr: int, shape, typestr: str):
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr,
+                                         "data": (ptr, False), "version": 2, "strides": None}
+
+
+def device_view(ptr: int, shape, dtype: torch.dtype) -> torch.Tensor:
+    """Zero-copy torch view of device memory owned by the library."""
+    if dtype == torch.bfloat16:
+        return torch.as_tensor(_CudaArray(ptr, shape, "<i2"), device="cuda").view(torch.bfloat16)
+    code = {torch.int32: "<i4", torch.float32: "<f4", torch.int64: "<i8"}[dtype]
+    return torch.as_tensor(_CudaArray(ptr, shape, code), device="cuda")

@@ -1,0 +1,251 @@
+/*
+ * dflash.h -- C ABI of the DFlash speculate-and-verify step on one GB300
+ * (sm_103a), plus its DDTree draft-tree variant.
+ *
+ * The step follows the four stages described in the "DFlash speculative
+ * decoding" glossary entry (globaladvisors.biz), section "DFlash:
+ * architecture and workflow":
+ *   1. the anchor is the token at the decoding frontier;
+ *   2. the block-diffusion drafter fills B-1 masked positions in ONE forward
+ *      pass, conditioned on target hidden states injected into the K/V of
+ *      every draft layer ("DFlash, Diffusion LLMs, dLLM, MTP and Speculative
+ *      Decoding: A Deep Research Report", section "Key points");
+ *   3. the target verifies the whole block in one forward pass, comparing
+ *      each draft token with its own argmax;
+ *   4. the longest matching prefix is emitted, followed by the target's own
+ *      token at the first mismatch, and the cycle restarts at the new
+ *      frontier.
+ * DDTree ("LLMs hit ludicrous speed ..." (joindrip.ai), DDTree paragraph)
+ * replaces the single draft by a best-first tree of continuations built from
+ * the drafter's per-position distributions, verified in one target pass with
+ * an ancestor-only attention mask.
+ *
+ * Conventions shared by every call:
+ *  - Pointers named *_dev are device pointers; the library never frees them.
+ *    Weights are BORROWED: they must stay valid until dflash_destroy.
+ *    KV caches, the hidden-state capture buffer and all scratch belong to the
+ *    context and are allocated once, in dflash_create.
+ *  - Every call only enqueues work on `stream` and returns without waiting
+ *    for the GPU.  A context keeps scratch between calls, so all calls on one
+ *    context must be issued on one stream (or otherwise ordered); one
+ *    context per host thread.
+ *  - Host-side argument checks run before any launch; on failure the call
+ *    returns an error status and launches nothing.  Violations found on the
+ *    device (a sequence that would overflow its cache, a tree deeper than the
+ *    block) set a sticky status word instead of trapping; dflash_check reads
+ *    it.  No kernel of this library traps or waits without a bound.
+ *  - Token ids are int32.  Sequences are addressed by slot id in
+ *    [0, max_batch); each slot keeps its committed length on the device.
+ */
+#ifndef DFLASH_H_
+#define DFLASH_H_
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DFLASH_API __attribute__((visibility("default")))
+#else
+#define DFLASH_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t (a CUDA runtime stream handle); 0 = legacy stream. */
+typedef struct CUstream_st *dflash_stream_t;
+
+typedef enum {
+  DFLASH_OK = 0,
+  DFLASH_E_INVALID_ARG = 1,   /* bad pointer, size, id or name */
+  DFLASH_E_CAPACITY = 2,      /* request exceeds a capacity fixed at create */
+  DFLASH_E_OOM = 3,           /* device allocation failed in dflash_create */
+  DFLASH_E_CUDA = 4,          /* a CUDA runtime/driver call failed */
+  DFLASH_E_DEVICE_CHECK = 5,  /* a device-side check failed (sticky) */
+  DFLASH_E_TIMEOUT = 6,       /* a bounded device wait gave up (sticky) */
+  DFLASH_E_UNSUPPORTED = 7,   /* shape/dtype combination not built */
+  DFLASH_E_STATE = 8          /* call order violated (e.g. weights missing) */
+} dflash_status;
+
+enum { DFLASH_F32 = 0, DFLASH_BF16 = 1, DFLASH_I32 = 2 };
+
+typedef struct {
+  /* target (and drafter: same width, heads, FFN, vocabulary) */
+  int32_t d_model, n_heads, n_kv_heads, head_dim, ffn_dim, vocab;
+  int32_t n_target_layers;
+  int32_t n_draft_layers;
+  int32_t n_inject;            /* number of target layers whose output is injected */
+  int32_t inject_layers[16];   /* ascending 0-based target layer ids */
+  float rope_theta, rms_eps;
+  int32_t block_size;          /* B, 1..16 */
+  /* capacities */
+  int32_t max_batch;           /* sequence slots */
+  int32_t max_ctx;             /* cache slots per sequence (prompt + generated + B or tree) */
+  int32_t max_rows;            /* rows of one target pass (batch*q), >= max_batch*block */
+  int32_t max_tree_nodes;      /* 0 or >= 2 (root + drafted nodes), <= 128 */
+  int32_t dtype;               /* storage type of weights, caches, capture: DFLASH_F32 | DFLASH_BF16 */
+} dflash_config;
+
+typedef struct dflash_ctx dflash_ctx;
+
+/* Draft tree of one batch, all arrays device memory owned by the caller.
+ * Node 0 is the root (the anchor); nodes are numbered in heap pop order, so
+ * a parent always has a smaller id than its children. */
+typedef struct {
+  int32_t *tok;        /* [batch][max_nodes]  token id, -1 past n_nodes */
+  int32_t *parent;     /* [batch][max_nodes]  parent id, -1 for the root */
+  int32_t *depth;      /* [batch][max_nodes]  0 for the root, 1..B-1 */
+  uint64_t *anc;       /* [batch][max_nodes][anc_words] bit m set = node m is an ancestor or self */
+  int32_t *n_nodes;    /* [batch] */
+  int32_t max_nodes;   /* row stride of the arrays above */
+  int32_t anc_words;   /* ceil(max_nodes / 64) */
+} dtree_buffers;
+
+/* Accept modes of dflash_accept_commit. */
+enum {
+  DFLASH_ACCEPT_GREEDY = 0,  /* longest matching prefix + bonus (block) or tree walk */
+  DFLASH_ACCEPT_ALL = 1      /* commit every row of the pass (prompt prefill) */
+};
+
+/* Flags of dflash_verify. */
+enum {
+  DFLASH_VERIFY_LAST_ONLY = 1  /* run the lm_head on each sequence's last row only */
+};
+
+/* Creates a context: validates the configuration, allocates KV caches of
+ * the target (n_target_layers) and of the drafter (n_draft_layers), the
+ * capture buffer of injected hidden states and all scratch, and uploads the
+ * RoPE tables.  Uses the current CUDA device.  On success *out owns them. */
+DFLASH_API dflash_status dflash_create(const dflash_config *cfg, dflash_ctx **out);
+
+/* Registers a borrowed weight tensor (row-major, device memory, dtype must be
+ * the context's storage type).  Names and shapes, with d = d_model,
+ * q = n_heads*head_dim, kv = n_kv_heads*head_dim, F = ffn_dim:
+ *   tok_emb [vocab][d]  lm_head [vocab][d]  final_norm [d]
+ *   layers.<l>.{attn_norm [d], wq [q][d], wk [kv][d], wv [kv][d], wo [d][q],
+ *               ffn_norm [d], w_gate [F][d], w_up [F][d], w_down [d][F]}
+ *   draft.fuse [d][n_inject*d]  draft.mask_emb [d]  draft.final_norm [d]
+ *   draft.layers.<l>.{same names as a target layer}
+ * The drafter shares tok_emb and lm_head with the target. */
+DFLASH_API dflash_status dflash_set_weight(dflash_ctx *ctx, const char *name, const void *dev_ptr,
+                                int32_t dtype, const int64_t *shape, int32_t ndim);
+
+/* Marks sequence slot `seq_id` empty (committed length 0). */
+DFLASH_API dflash_status dflash_reset_seq(dflash_ctx *ctx, int32_t seq_id, dflash_stream_t stream);
+
+/* Target pass ("verify", also used for prompt prefill and plain AR steps).
+ * For every b < batch, rows j < q_len[b] hold tokens[b][j] at position
+ * P_b + j, where P_b is the committed length of slot seq_ids[b].  The K/V of
+ * row j are written TENTATIVELY to cache slot P_b + j of every target layer
+ * (the committed length does not change); attention is causal over the
+ * cache and inside the block.  The residual stream after each injected
+ * layer is kept in the context's capture buffer for dflash_inject_kv.
+ *   tokens_dev  [batch][q] int32
+ *   q_lens_dev  [batch] int32 or NULL (= q for all)
+ *   argmax_dev  [batch][q] int32: target argmax of each row (ties: lowest id);
+ *               -1 for rows past q_len (and, with LAST_ONLY, all but the last)
+ *   margin_dev  [batch][q] float or NULL: top-1 minus top-2 logit
+ *   logits_dev  [batch][q][vocab] float or NULL: debug copy of the logits
+ * Requires batch*q <= max_rows and P_b + q <= max_ctx (device-checked). */
+DFLASH_API dflash_status dflash_verify(dflash_ctx *ctx, int32_t batch, const int32_t *seq_ids_dev,
+                            const int32_t *tokens_dev, int32_t q, const int32_t *q_lens_dev,
+                            int32_t flags, int32_t *argmax_dev, float *margin_dev,
+                            float *logits_dev, dflash_stream_t stream);
+
+/* One block-diffusion draft pass (stage 2).  Slot j of the block of slot
+ * seq_ids[b] sits at position P_b + j; slot 0 embeds anchor_dev[b], slots
+ * 1..B-1 the mask embedding.  Every block position attends to the injected
+ * draft context 0..P_b-1 and to all B block positions (no mask).
+ *   block_dev   [batch][B] int32 out: [anchor, d_1 .. d_{B-1}] where d_j is
+ *               the argmax of the shared lm_head at slot j (ties: lowest id)
+ *   topk        0, or k in 1..16: also return the top-k of every slot
+ *   topk_ids_dev  [batch][B-1][topk] int32 (logit descending, ties lowest id)
+ *   topk_logp_dev [batch][B-1][topk] float: log-softmax values (temperature 1)
+ *   logits_dev  [batch][B-1][vocab] float or NULL: debug copy */
+DFLASH_API dflash_status dflash_draft_block(dflash_ctx *ctx, int32_t batch, const int32_t *seq_ids_dev,
+                                 const int32_t *anchor_dev, int32_t *block_dev, int32_t topk,
+                                 int32_t *topk_ids_dev, float *topk_logp_dev, float *logits_dev,
+                                 dflash_stream_t stream);
+
+/* Acceptance and commit (stage 4) of the LAST target pass on this context
+ * (dflash_verify or dtree_verify, same batch and seq_ids).
+ * GREEDY, linear block (tree == NULL): with d_i = block[b][i] and
+ *   y_j = argmax[b][j], a = max{ j <= q_len-1 : d_i == y_{i-1} for all i <= j };
+ *   emitted[b] = d_1..d_a, y_a (then -1); next_anchor[b] = y_a;
+ *   accept_len[b] = a; the committed length grows by a + 1 (rows P..P+a are
+ *   kept; the rest is rolled back by length).
+ * GREEDY, tree: walk from the root to the child whose token equals the
+ *   current node's argmax until none matches; a = path length; the accepted
+ *   nodes' K/V (every target layer) are moved to slots P+1..P+a; bonus =
+ *   argmax at the last node.
+ * ALL (prefill): every row j < q_len is committed; accept_len[b] = q_len;
+ *   next_anchor[b] = emitted[b][0] = argmax of the last row.
+ * In every mode the committed rows are queued for dflash_inject_kv.
+ *   block_dev  [batch][q] (linear) -- the verified tokens; ignored for trees
+ *   argmax_dev [batch][q] from the verify call
+ *   emitted_dev [batch][q] int32, accept_len_dev / next_anchor_dev [batch] */
+DFLASH_API dflash_status dflash_accept_commit(dflash_ctx *ctx, int32_t batch, const int32_t *seq_ids_dev,
+                                   const int32_t *block_dev, const int32_t *argmax_dev,
+                                   const dtree_buffers *tree, int32_t mode,
+                                   int32_t *accept_len_dev, int32_t *next_anchor_dev,
+                                   int32_t *emitted_dev, dflash_stream_t stream);
+
+/* KV injection (Deep Research Report, "Key points"): for every queued row,
+ * h_cat = concat of the captured target residual streams (layer order),
+ * F = W_fuse h_cat, and for every draft layer l: K = RoPE(Wk_l F) and
+ * V = Wv_l F are written to the draft cache at the row's position.
+ * With hidden_dev == NULL the rows queued by the last dflash_accept_commit
+ * are injected (the other pointer arguments are ignored).  Otherwise rows
+ * r < n_rows use hidden_dev[r] ([n_inject][d_model], storage dtype), slot
+ * row_seq_dev[r] and position row_pos_dev[r] (< 0 skips the row); n_rows
+ * <= max_rows. */
+DFLASH_API dflash_status dflash_inject_kv(dflash_ctx *ctx, int32_t n_rows, const int32_t *row_seq_dev,
+                               const int32_t *row_pos_dev, const void *hidden_dev,
+                               dflash_stream_t stream);
+
+/* DDTree build: per sequence, a best-first heap over prefixes of the per-slot
+ * top-k lists (score = fp32 sum of log-probs in depth order; ties: shallower
+ * first, then lexicographically smaller rank vector) pops `budget` nodes;
+ * popping pushes the first child and the next sibling.  Node 0 = anchor.
+ *   topk_ids_dev / topk_logp_dev [batch][B-1][topk] from dflash_draft_block
+ *   budget + 1 <= tree->max_nodes <= max_tree_nodes */
+DFLASH_API dflash_status dtree_build(dflash_ctx *ctx, int32_t batch, const int32_t *anchor_dev,
+                          const int32_t *topk_ids_dev, const float *topk_logp_dev, int32_t topk,
+                          int32_t budget, const dtree_buffers *tree, dflash_stream_t stream);
+
+/* DDTree verify: one target pass over every node; node n sits at position
+ * P + depth[n] and tentative cache slot P + n, and attends to the context
+ * 0..P-1 plus its ancestors and itself.
+ *   node_argmax_dev [batch][max_nodes] (-1 past n_nodes); margin/logits as
+ *   in dflash_verify (row stride max_nodes) or NULL. */
+DFLASH_API dflash_status dtree_verify(dflash_ctx *ctx, int32_t batch, const int32_t *seq_ids_dev,
+                           const dtree_buffers *tree, int32_t *node_argmax_dev, float *margin_dev,
+                           float *logits_dev, dflash_stream_t stream);
+
+/* Waits for all work on the device, then returns (and clears) the sticky
+ * device status word. */
+DFLASH_API dflash_status dflash_check(dflash_ctx *ctx);
+
+/* Text of the last host-side error of this context ("" if none). */
+DFLASH_API const char *dflash_last_error(const dflash_ctx *ctx);
+
+/* Device pointer to the committed length of every sequence slot [max_batch]. */
+DFLASH_API const int32_t *dflash_seq_lengths(const dflash_ctx *ctx);
+
+/* Number of kernels this context has launched so far. */
+DFLASH_API int64_t dflash_launch_count(const dflash_ctx *ctx);
+
+/* Read-only views of internal buffers for tests and tooling.
+ *   "k_cache"/"v_cache"   target layer `layer`: [max_batch][n_kv_heads][max_ctx][head_dim]
+ *   "dk_cache"/"dv_cache" draft layer `layer`: same layout
+ *   "capture"             [max_rows][n_inject][d_model] (row = b*q + j of the last pass)
+ * Element type = the storage dtype.  *bytes receives the view's size. */
+DFLASH_API dflash_status dflash_debug_view(const dflash_ctx *ctx, const char *name, int32_t layer,
+                                const void **dev_ptr, int64_t *bytes);
+
+DFLASH_API void dflash_destroy(dflash_ctx *ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DFLASH_H_ */
