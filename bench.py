@@ -1,0 +1,415 @@
+#!/usr/bin/env python
+"""Benchmark of the DFlash speculate-and-verify step on GB300.
+
+Metric: verified (emitted) tokens/s per GB300 and draft+verify step time, on
+a Qwen3-8B-shaped random-init bf16 target with a 5-layer block-diffusion
+drafter (B = 16, batch 1, 2048-token random prompt).  One step = one block
+draft pass + one target verify pass + accept/commit + KV injection.
+
+Timing: W untimed warm-up steps, then K steps between CUDA events on the
+launching stream, bracketed by a barrier and a device synchronize; max over
+ranks.  Every step streams ~19 GB of weights, far above the 129 MB L2, so no
+explicit L2 flush is needed between steps.  SM clocks are sampled with
+nvidia-smi during the timed region.
+
+Also reported: the end-to-end rate through the C ABI with host buffers
+(H2D of each step's anchors from pinned memory, D2H of its emitted tokens),
+the GEMM kernel class against the measured HBM peak (live CUDA-event timing
+from the library's profiler over a second pass of the same steps), the AR
+step cost and the projected speedup S = C_AR * E[L] / C_DF with E[L] from
+the pages, and the CPU oracle timed on a bounded sample on the host cores.
+
+--impl reference times that oracle alone (the reference arm: the pages ship
+no code, so the plain CPU restatement is the baseline program).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+PAGES_ACCEPT_LEN = 7.84  # mean acceptance length on MATH-500 (Deep Research Report)
+METRIC = "verified tokens/s per GB300 and draft+verify step µs (Qwen3-8B shape, B=16)"
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle sample (the reported CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------
+class OracleSample:
+    """Times the oracle on a bounded sample of one step and extrapolates.
+
+    Sample: one target layer and one draft layer over 2 block rows (with the
+    real P-row context in attention), 1/16 of the lm_head rows for 1 token
+    row, and the fused injection projection for 1 row -- all with the
+    oracle's own fp64 functions.  Extrapolated to one step of the workload:
+    B rows x L target layers, B rows x L_d draft layers, 2B-1 lm_head rows,
+    B injected rows at most (a+1 with random weights: 1).
+    """
+
+    def __init__(self, w: wl.Workload):
+        from oracle import numerics as nm
+        from oracle.models import Weights
+        s = w.shape
+        self.w, self.s, self.nm = w, s, nm
+        self.W = Weights(wl.SyntheticWeights(s, w.seed))
+        P = w.prompt_len[0]
+        rng = np.random.default_rng(5)
+        self.P = P
+        self.ck = nm.round_bf16(rng.standard_normal((P, s.n_kv_heads, s.head_dim)))
+        self.cv = nm.round_bf16(rng.standard_normal((P, s.n_kv_heads, s.head_dim)))
+        self.x = rng.standard_normal((2, s.d_model)) * 0.1
+        self.hcat = rng.standard_normal((1, s.n_inject * s.d_model)) * 0.1
+        keys = ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down")
+        for pre in ("layers.0", "draft.layers.0"):
+            for k in keys:
+                self.W[f"{pre}.{k}"]
+        sw = self.W.source
+        rows = sw.offsets("lm_head")[: s.vocab // 16]
+        self.lm_part = wl.pool_rows(sw.pool(), rows, s.d_model).astype(np.float64)
+        self.W["final_norm"], self.W["draft.fuse"]
+
+    def step_seconds(self):
+        from oracle.models import _layer
+        nm, s, W, P = self.nm, self.s, self.W, self.P
+        B = self.w.block_size
+        prec = nm.Precision("bf16emu")
+        pos = P + np.arange(2)
+
+        def causal(q, k, v):
+            kk, vv = np.concatenate([self.ck, k]), np.concatenate([self.cv, v])
+            return np.stack([nm.attend(q[i], kk[: P + i + 1], vv[: P + i + 1]) for i in range(2)])
+
+        def full(q, k, v):
+            kk, vv = np.concatenate([self.ck, k]), np.concatenate([self.cv, v])
+            return np.stack([nm.attend(q[i], kk, vv) for i in range(2)])
+
+        t = time.perf_counter()
+        _layer(W, s, prec, "layers.0", self.x, pos, causal)
+        t_tl = (time.perf_counter() - t) / 2
+        t = time.perf_counter()
+        _layer(W, s, prec, "draft.layers.0", self.x, pos, full)
+        t_dl = (time.perf_counter() - t) / 2
+        t = time.perf_counter()
+        nm.linear(nm.rmsnorm(self.x[:1], W["final_norm"], s.rms_eps), self.lm_part)
+        t_lm = (time.perf_counter() - t) * 16
+        t = time.perf_counter()
+        nm.linear(self.hcat, W["draft.fuse"])
+        t_inj = time.perf_counter() - t
+        per_step = B * (s.n_layers * t_tl + s.n_draft_layers * t_dl) + (2 * B - 1) * t_lm + t_inj
+        sampled = 2 * t_tl + 2 * t_dl + t_lm / 16 + t_inj
+        return per_step, sampled
+
+    def describe(self, sampled):
+        s, B = self.s, self.w.block_size
+        return (f"oracle (fp64 numpy) on 2 rows of 1 target layer and 1 draft layer at context "
+                f"{self.P}, 1/16 of the lm_head for 1 row, the fuse projection for 1 row; "
+                f"extrapolated to {B} rows x ({s.n_layers}+{s.n_draft_layers}) layers and "
+                f"{2 * B - 1} lm_head rows per step; {sampled:.2f}s of CPU work per sample")
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, w: wl.Workload) -> None:
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    smp = OracleSample(w)
+    for _ in range(args.warmup):
+        smp.step_seconds()
+    times, sampled = [], []
+    for _ in range(args.steps):
+        sec, cpu_s = smp.step_seconds()
+        times.append(sec)
+        sampled.append(cpu_s)
+    per_step = statistics.median(times)
+    info = smp.describe(statistics.median(sampled)) + f"; {args.steps} samples, median"
+    value = w.batch * 1.0 / per_step  # random-init weights: one verified token per step
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "prompt_len": w.prompt_len[0],
+                   "block": w.block_size},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": info},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_ours(args, w: wl.Workload) -> None:
+    import torch
+    import torch.distributed as dist
+
+    from block_diffusion_speculative_injection_gb300 import capi
+    from block_diffusion_speculative_injection_gb300.engine import DFlashEngine
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("gloo")
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+
+    B = w.block_size
+    b = w.batch
+    lens = wl.prompt_lengths(w)
+    prompts = wl.prompts(w)
+    total_steps = args.warmup + args.steps + args.prof_steps + args.e2e_steps + 4
+    max_ctx = max(lens) + B * (total_steps + 2) + args.ar_steps + 64
+    eng = DFlashEngine(w.shape, B, b, max_ctx, max_rows=max(max(lens), b * B), seed=w.seed)
+    ctx = eng.ctx
+    sid = eng.seq_ids(b)
+    stream = torch.cuda.current_stream()
+
+    anchors = eng.prefill(prompts)
+    for _ in range(args.warmup):
+        eng.step(sid, anchors)
+        anchors = eng.next_anchor[:b].clone()
+    acc_log = torch.zeros(args.steps, b, dtype=torch.int32, device="cuda")
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier()
+    l0 = capi.dflash_launch_count(ctx)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        out = eng.step(sid, anchors)
+        acc_log[i].copy_(out.accept_len)
+        anchors = out.next_anchor  # consumed by the next call on the same stream
+    ev1.record(stream)
+    barrier()
+    clocks = sampler.stop()
+    launches = capi.dflash_launch_count(ctx) - l0
+    ms = ev0.elapsed_time(ev1)
+    anchors = eng.next_anchor[:b].clone()
+    emitted = int((acc_log + 1).sum().item())
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        n = torch.tensor([emitted], dtype=torch.float64)
+        dist.all_reduce(n, op=dist.ReduceOp.SUM)
+        emitted_all = int(n.item())
+    else:
+        emitted_all = emitted
+    value = emitted_all / (ms / 1e3)
+    step_ms = ms / args.steps
+    tau = emitted / (args.steps * b)
+
+    # live per-kernel timing over a second pass of the same steps
+    capi.dflash_profile(ctx, True)
+    for _ in range(args.prof_steps):
+        eng.step(sid, anchors)
+        anchors = eng.next_anchor[:b].clone()
+    capi.dflash_profile(ctx, False)
+    prof = {}
+    names = {capi.PROF_GEMM: "gemm_tc_kernel", capi.PROF_ATTN: "attention", capi.PROF_ROW: "row_ops",
+             capi.PROF_VOCAB: "vocab_reduce", capi.PROF_SPEC: "accept_tree"}
+    for k, name in names.items():
+        n, kms, kbytes, kflops = capi.dflash_profile_read(ctx, k)
+        prof[name] = {"launches_per_step": n / max(args.prof_steps, 1),
+                      "ms_per_step": kms / max(args.prof_steps, 1),
+                      "bytes": kbytes, "flops": kflops, "ms": kms, "n": n}
+    hbm, tflops, src = peaks()
+    g = prof["gemm_tc_kernel"]
+    achieved = (g["bytes"] / g["n"]) / ((g["ms"] / g["n"]) / 1e3) / 1e9 if g["n"] else 0.0
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "gemm_traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            tj = json.load(f)
+        if tj.get("workload") == w.name and tj.get("kernel_rev") == KERNEL_REV:
+            traffic = tj.get("dram_bytes_per_launch")
+
+    # AR step cost (the B = 1 path: verify the anchor alone, commit it)
+    for _ in range(3):
+        eng.ar_step(sid, anchors)
+        anchors = eng.next_anchor[:b].clone()
+    barrier()
+    ev0.record(stream)
+    for _ in range(args.ar_steps):
+        anchors = eng.ar_step(sid, anchors)
+    ev1.record(stream)
+    barrier()
+    ar_ms = ev0.elapsed_time(ev1) / args.ar_steps
+    anchors = eng.next_anchor[:b].clone()
+
+    # end to end through the C ABI with host buffers
+    h_anchor = torch.empty(b, dtype=torch.int32, pin_memory=True)
+    h_anchor.copy_(anchors.cpu())
+    h_emit = torch.empty(b, B, dtype=torch.int32, pin_memory=True)
+    h_acc = torch.empty(b, dtype=torch.int32, pin_memory=True)
+    d_anchor = torch.empty(b, dtype=torch.int32, device="cuda")
+    barrier()
+    t0 = time.perf_counter()
+    e2e_tokens = 0
+    for _ in range(args.e2e_steps):
+        d_anchor.copy_(h_anchor, non_blocking=True)
+        out = eng.step(sid, d_anchor)
+        h_emit.copy_(out.emitted, non_blocking=True)
+        h_acc.copy_(out.accept_len, non_blocking=True)
+        h_anchor.copy_(out.next_anchor, non_blocking=True)
+        stream.synchronize()
+        e2e_tokens += int(h_acc.sum().item()) + b
+    e2e_s = time.perf_counter() - t0
+    barrier()
+    e2e_value = e2e_tokens * world / e2e_s
+
+    if rank != 0:
+        eng.close()
+        return
+    cpu = None
+    if not args.no_cpu_baseline:
+        smp = OracleSample(w)
+        smp.step_seconds()
+        secs, cpu_s, t_end = [], [], time.perf_counter() + 10.0
+        while time.perf_counter() < t_end or len(secs) < 3:
+            a, c = smp.step_seconds()
+            secs.append(a)
+            cpu_s.append(c)
+        sec = statistics.median(secs)
+        cpu = {"value": b / sec, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": smp.describe(statistics.median(cpu_s)) + f"; {len(secs)} samples, median"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded random-init weights, uniform random prompt tokens)",
+        "config": {"workload": w.name, "target": w.shape.name, "batch": b, "prompt_len": lens[0],
+                   "block": B, "draft_layers": w.shape.n_draft_layers,
+                   "inject_layers": list(w.shape.inject_layers), "parallelism": "replicas",
+                   "l2": "no flush: every step streams ~19 GB of weights (> 129 MB L2)"},
+        "step_us": step_ms * 1e3,
+        "tau": tau,
+        "ar_step_us": ar_ms * 1e3,
+        "projected_speedup": ar_ms * PAGES_ACCEPT_LEN / step_ms,
+        "gpu_launches": launches,
+        "roofline": {"bound": "hbm", "kernel": "gemm_tc_kernel", "achieved": achieved,
+                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
+                     "peak_source": src,
+                     "bytes_per_launch": g["bytes"] / g["n"] if g["n"] else None,
+                     "launches_per_step": g["launches_per_step"],
+                     "ms_per_step": g["ms_per_step"]},
+        "kernel_ms_per_step": {k: v["ms_per_step"] for k, v in prof.items()},
+        "clocks": clocks,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": 4 * b,
+                "d2h_bytes_per_step": 4 * b * B + 8 * b},
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+    eng.close()
+
+
+KERNEL_REV = "gemm-v1"
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="qwen3_8b_b1",
+                    choices=["qwen3_8b_b1", "qwen3_8b_b32", "qwen3_8b_slice_b1", "tiny_f32_e2e",
+                             "mini_bf16_e2e"])
+    ap.add_argument("--prof-steps", type=int, default=10)
+    ap.add_argument("--ar-steps", type=int, default=50)
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    w = wl.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -69,6 +69,11 @@ _SIGS = {
     "dflash_launch_count": ([_P], ctypes.c_int64),
     "dflash_debug_view": ([_P, ctypes.c_char_p, _I, ctypes.POINTER(_P), ctypes.POINTER(ctypes.c_int64)], _I),
     "dflash_destroy": ([_P], None),
+    "dflash_block_attention": ([_I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, ctypes.c_int64, _P], _I),
+    "dflash_block_attention_workspace": ([_I, _I, _I, _I, _I], ctypes.c_int64),
+    "dflash_profile": ([_P, _I], _I),
+    "dflash_profile_read": ([_P, _I, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double),
+                             ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)], _I),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -203,3 +208,33 @@ def dflash_debug_view(ctx, name: str, layer: int = 0):
     n = ctypes.c_int64()
     _check(ctx, load().dflash_debug_view(ctx, name.encode(), layer, ctypes.byref(p), ctypes.byref(n)))
     return p.value, n.value
+
+
+def dflash_block_attention(batch, n_heads, n_kv_heads, ctx_len, block, causal, q, k, v, out,
+                           workspace=None, stream=None) -> None:
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = load().dflash_block_attention(batch, n_heads, n_kv_heads, ctx_len, block, causal, _ptr(q),
+                                       _ptr(k), _ptr(v), _ptr(out), _ptr(workspace), nbytes,
+                                       _stream(stream))
+    if st != 0:
+        raise DFlashError(st, "dflash_block_attention")
+
+
+def dflash_block_attention_workspace(batch, n_heads, n_kv_heads, ctx_len, block) -> int:
+    return int(load().dflash_block_attention_workspace(batch, n_heads, n_kv_heads, ctx_len, block))
+
+
+def dflash_profile(ctx, enable: bool) -> None:
+    _check(ctx, load().dflash_profile(ctx, 1 if enable else 0))
+
+
+PROF_GEMM, PROF_ATTN, PROF_ROW, PROF_VOCAB, PROF_SPEC, PROF_ALL = 0, 1, 2, 3, 4, -1
+
+
+def dflash_profile_read(ctx, kind: int):
+    """(launches, ms, algorithmic bytes, flops) of one kernel class."""
+    n = ctypes.c_int64()
+    ms, b, f = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
+    _check(ctx, load().dflash_profile_read(ctx, kind, ctypes.byref(n), ctypes.byref(ms),
+                                           ctypes.byref(b), ctypes.byref(f)))
+    return n.value, ms.value, b.value, f.value

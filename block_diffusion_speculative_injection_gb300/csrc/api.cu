@@ -403,6 +403,7 @@ void dflash_destroy(dflash_ctx* ctx) {
                   ctx->inj_pos, ctx->path,       ctx->rope_cos, ctx->rope_sin};
   for (void* p : ptrs)
     if (p) cudaFree(p);
+  for (cudaEvent_t e : ctx->prof_ev) cudaEventDestroy(e);
   auto it = g_draft_meta.find(ctx);
   if (it != g_draft_meta.end()) {
     if (it->second.seq) cudaFree(it->second.seq);
@@ -674,6 +675,55 @@ dflash_status dflash_check(dflash_ctx* ctx) {
     case kDevTimeout: return fail(ctx, DFLASH_E_TIMEOUT, "device: bounded wait expired");
     default: return fail(ctx, DFLASH_E_DEVICE_CHECK, "device: argument check failed");
   }
+}
+
+dflash_status dflash_block_attention(int32_t batch, int32_t n_heads, int32_t n_kv_heads,
+                                     int32_t ctx_len, int32_t block, int32_t causal,
+                                     const void* q_dev, const void* k_dev, const void* v_dev,
+                                     void* out_dev, void* workspace_dev, int64_t workspace_bytes,
+                                     dflash_stream_t stream) {
+  if (workspace_bytes < 0) return DFLASH_E_INVALID_ARG;
+  return block_attention(batch, n_heads, n_kv_heads, 128, ctx_len, block, causal ? 1 : 0, q_dev,
+                         k_dev, v_dev, out_dev, workspace_dev, workspace_bytes,
+                         (cudaStream_t)stream);
+}
+
+int64_t dflash_block_attention_workspace(int32_t batch, int32_t n_heads, int32_t n_kv_heads,
+                                         int32_t ctx_len, int32_t block) {
+  return block_attention_workspace(batch, n_heads, n_kv_heads, 128, ctx_len, block);
+}
+
+dflash_status dflash_profile(dflash_ctx* ctx, int32_t enable) {
+  if (!ctx) return DFLASH_E_INVALID_ARG;
+  if (enable) {
+    if (ctx->prof_ev.empty()) {
+      ctx->prof_ev.resize(1 << 16);
+      for (auto& e : ctx->prof_ev) DF_CUDA_TRY(ctx, cudaEventCreate(&e));
+    }
+    ctx->prof_recs.clear();
+    ctx->prof_next = 0;
+  }
+  ctx->prof_on = enable != 0;
+  return DFLASH_OK;
+}
+
+dflash_status dflash_profile_read(dflash_ctx* ctx, int32_t kind, int64_t* launches, double* ms,
+                                  double* bytes, double* flops) {
+  if (!ctx || !launches || !ms || !bytes || !flops) return DFLASH_E_INVALID_ARG;
+  *launches = 0;
+  *ms = *bytes = *flops = 0.0;
+  if (!ctx->prof_recs.empty())
+    DF_CUDA_TRY(ctx, cudaEventSynchronize(ctx->prof_ev[ctx->prof_recs.back().ev + 1]));
+  for (const ProfRec& r : ctx->prof_recs) {
+    if (kind >= 0 && r.kind != kind) continue;
+    float t = 0.f;
+    DF_CUDA_TRY(ctx, cudaEventElapsedTime(&t, ctx->prof_ev[r.ev], ctx->prof_ev[r.ev + 1]));
+    *launches += 1;
+    *ms += t;
+    *bytes += r.bytes;
+    *flops += r.flops;
+  }
+  return DFLASH_OK;
 }
 
 const char* dflash_last_error(const dflash_ctx* ctx) {

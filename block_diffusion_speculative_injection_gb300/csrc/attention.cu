@@ -16,6 +16,8 @@
 // registers (exp2 domain).  Long contexts are split across CTAs; a combine
 // kernel merges the partial (m, l, O).
 #include <cfloat>
+#include <cmath>
+#include <cstring>
 
 #include "internal.cuh"
 
@@ -38,7 +40,20 @@ struct AttnK {
   float* part_ml;
   int rows_total;
   float scale_log2;
+  int uni_ctx, uni_blk;  // used when pass_seq == nullptr: seq = b, same lengths
 };
+
+__device__ __forceinline__ void seq_meta(const AttnK& p, int b, int& seq, int& ctx, int& blk) {
+  if (p.pass_seq) {
+    seq = p.pass_seq[b];
+    ctx = p.pass_ctx[b];
+    blk = p.pass_blk[b];
+  } else {
+    seq = b;
+    ctx = p.uni_ctx;
+    blk = p.uni_blk;
+  }
+}
 
 // ---------------------------------------------------------------------------
 // small PTX wrappers (legacy warp-level MMA path)
@@ -106,11 +121,10 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const AttnK p) {
   const int G = p.G, POS = 64 / G;
   const int b = blockIdx.z / p.n_splits, split = blockIdx.z % p.n_splits;
   const int kvh = blockIdx.y;
-  const int blk = p.pass_blk[b];
+  int seq, ctx_len, blk;
+  seq_meta(p, b, seq, ctx_len, blk);
   const int j0 = blockIdx.x * POS;
   if (j0 >= blk) return;
-  const int seq = p.pass_seq[b];
-  const int ctx_len = p.pass_ctx[b];
   const int jmax = min(j0 + POS, blk);  // exclusive
   int key_end = (p.mask == kMaskCausal) ? ctx_len + jmax : ctx_len + blk;
   const int k_begin = split * p.keys_per_split;
@@ -353,7 +367,9 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const AttnK p) {
 __global__ void attn_combine_kernel(const AttnK p) {
   const int row = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
   const int b = row / p.q_stride, j = row % p.q_stride;
-  if (j >= p.pass_blk[b]) return;
+  int seq_, ctx_, blk_;
+  seq_meta(p, b, seq_, ctx_, blk_);
+  if (j >= blk_) return;
   float mmax = -INFINITY;
   for (int s = 0; s < p.n_splits; ++s)
     mmax = fmaxf(mmax, p.part_ml[(((size_t)s * p.rows_total + row) * p.H + h) * 2]);
@@ -377,9 +393,9 @@ __global__ void attn_simt_f32_kernel(const AttnK p) {
   if (wid >= p.rows_total * p.H) return;
   const int row = wid / p.H, h = wid % p.H;
   const int b = row / p.q_stride, j = row % p.q_stride;
-  const int blk = p.pass_blk[b];
+  int seq, ctx_len, blk;
+  seq_meta(p, b, seq, ctx_len, blk);
   if (j >= blk) return;
-  const int seq = p.pass_seq[b], ctx_len = p.pass_ctx[b];
   const int kvh = h / p.G;
   const int per = p.hd / 32;  // head_dim <= 128
   const float* qv = static_cast<const float*>(p.q) + ((size_t)row * p.H + h) * p.hd;
@@ -410,7 +426,45 @@ __global__ void attn_simt_f32_kernel(const AttnK p) {
   for (int i = 0; i < per; ++i) og[lane + 32 * i] = acc[i] / l;
 }
 
+// number of KV splits and keys per split for a launch of `ctas` CTAs
+static void plan_splits(int sm_count, int ctas, int64_t max_keys, size_t part_cap, int rows_heads,
+                        int* n_splits, int* keys_per_split) {
+  const int64_t key_tiles = (max_keys + kTileKeys - 1) / kTileKeys;
+  int splits = (2 * sm_count + ctas - 1) / ctas;
+  if (splits > key_tiles) splits = (int)key_tiles;
+  if (splits < 1) splits = 1;
+  while (splits > 1 && (size_t)splits * rows_heads > part_cap) --splits;
+  *keys_per_split = 1 << 30;
+  if (splits > 1) {
+    const int64_t tiles_per = (key_tiles + splits - 1) / splits;
+    *keys_per_split = (int)(tiles_per * kTileKeys);
+    splits = (int)((key_tiles + tiles_per - 1) / tiles_per);
+  }
+  *n_splits = splits;
+}
+
+static int device_sms() {
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 1;
+  }
+  return sms;
+}
+
+static cudaError_t ensure_attn_smem() {
+  static bool attr = false;
+  if (attr) return cudaSuccess;
+  cudaError_t e =
+      cudaFuncSetAttribute(attn_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
+  if (e == cudaSuccess) attr = true;
+  return e;
+}
+
 dflash_status attention(dflash_ctx* ctx, const AttnArgs& a, cudaStream_t st) {
+  ProfScope prof(ctx, kProfAttn, st);
   const dflash_config& c = ctx->cfg;
   AttnK p;
   p.q = a.q;
@@ -435,6 +489,7 @@ dflash_status attention(dflash_ctx* ctx, const AttnArgs& a, cudaStream_t st) {
   p.part_ml = ctx->part_ml;
   p.n_splits = 1;
   p.keys_per_split = 1 << 30;
+  p.uni_ctx = p.uni_blk = 0;
 
   if (c.dtype == DFLASH_F32) {
     const int warps = p.rows_total * p.H;
@@ -449,23 +504,11 @@ dflash_status attention(dflash_ctx* ctx, const AttnArgs& a, cudaStream_t st) {
   const int POS = 64 / p.G;
   const int q_tiles = (a.q_stride + POS - 1) / POS;
   const int ctas = q_tiles * c.n_kv_heads * a.batch;
-  const int64_t key_tiles = (a.max_keys_ub + kTileKeys - 1) / kTileKeys;
-  int splits = (int)((2 * ctx->sm_count + ctas - 1) / ctas);
-  if (splits > key_tiles) splits = (int)key_tiles;
-  if (splits < 1) splits = 1;
-  while (splits > 1 && (size_t)splits * p.rows_total * p.H > ctx->part_rows_cap) --splits;
-  if (splits > 1) {
-    const int64_t tiles_per = (key_tiles + splits - 1) / splits;
-    p.keys_per_split = (int)(tiles_per * kTileKeys);
-    splits = (int)((key_tiles + tiles_per - 1) / tiles_per);
-  }
+  int splits = 1;
+  plan_splits(ctx->sm_count, ctas, a.max_keys_ub, ctx->part_rows_cap, p.rows_total * p.H, &splits,
+              &p.keys_per_split);
   p.n_splits = splits;
-  static bool attr = false;
-  if (!attr) {
-    DF_CUDA_TRY(ctx, cudaFuncSetAttribute(attn_mma_kernel,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem));
-    attr = true;
-  }
+  DF_CUDA_TRY(ctx, ensure_attn_smem());
   dim3 grid(q_tiles, c.n_kv_heads, a.batch * splits);
   attn_mma_kernel<<<grid, 128, kAttnSmem, st>>>(p);
   DF_LAUNCHED(ctx);
@@ -475,6 +518,71 @@ dflash_status attention(dflash_ctx* ctx, const AttnArgs& a, cudaStream_t st) {
     DF_LAUNCHED(ctx);
   }
   return DFLASH_OK;
+}
+
+// ---------------------------------------------------------------------------
+// op-level entry: block attention over caller-provided K/V
+// ---------------------------------------------------------------------------
+static bool op_shape_ok(int batch, int H, int Hkv, int hd, int ctx_len, int block) {
+  return batch >= 1 && H >= 1 && Hkv >= 1 && H % Hkv == 0 && hd == kHd && 64 % (H / Hkv) == 0 &&
+         ctx_len >= 0 && block >= 1 && block <= 64 && (int64_t)ctx_len + block < (1 << 30);
+}
+
+int64_t block_attention_workspace(int batch, int H, int Hkv, int hd, int ctx_len, int block) {
+  if (!op_shape_ok(batch, H, Hkv, hd, ctx_len, block)) return -1;
+  const int G = H / Hkv, POS = 64 / G;
+  const int ctas = ((block + POS - 1) / POS) * Hkv * batch;
+  int splits = 1, kps = 0;
+  plan_splits(device_sms(), ctas, ctx_len + block, (size_t)1 << 40, batch * block * H, &splits,
+              &kps);
+  if (splits == 1) return 0;
+  return (int64_t)splits * batch * block * H * (kHd + 2) * (int64_t)sizeof(float);
+}
+
+dflash_status block_attention(int batch, int H, int Hkv, int hd, int ctx_len, int block, int causal,
+                              const void* q, const void* k, const void* v, void* out,
+                              void* workspace, int64_t workspace_bytes, cudaStream_t st) {
+  if (!op_shape_ok(batch, H, Hkv, hd, ctx_len, block)) return DFLASH_E_INVALID_ARG;
+  if (!q || !k || !v || !out) return DFLASH_E_INVALID_ARG;
+  AttnK p;
+  memset(&p, 0, sizeof(p));
+  p.q = q;
+  p.out = out;
+  p.kc = k;
+  p.vc = v;
+  p.q_stride = block;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.G = H / Hkv;
+  p.hd = hd;
+  p.max_ctx = ctx_len + block;
+  p.mask = causal ? kMaskCausal : kMaskNone;
+  p.rows_total = batch * block;
+  p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)hd));
+  p.uni_ctx = ctx_len;
+  p.uni_blk = block;
+  const int POS = 64 / p.G;
+  const int q_tiles = (block + POS - 1) / POS;
+  const int ctas = q_tiles * Hkv * batch;
+  // splits limited by the caller's workspace
+  const size_t per_split = (size_t)p.rows_total * H * (kHd + 2) * sizeof(float);
+  const size_t cap_units = workspace ? (size_t)workspace_bytes / per_split * p.rows_total * H : 0;
+  int splits = 1;
+  plan_splits(device_sms(), ctas, p.max_ctx, cap_units, p.rows_total * H, &splits,
+              &p.keys_per_split);
+  if (splits > 1) {
+    p.part_o = static_cast<float*>(workspace);
+    p.part_ml = p.part_o + (size_t)splits * p.rows_total * H * kHd;
+  }
+  p.n_splits = splits;
+  if (ensure_attn_smem() != cudaSuccess) return DFLASH_E_CUDA;
+  dim3 grid(q_tiles, Hkv, batch * splits);
+  attn_mma_kernel<<<grid, 128, kAttnSmem, st>>>(p);
+  if (splits > 1) {
+    dim3 g2(p.rows_total, H);
+    attn_combine_kernel<<<g2, kHd, 0, st>>>(p);
+  }
+  return cudaGetLastError() == cudaSuccess ? DFLASH_OK : DFLASH_E_CUDA;
 }
 
 }  // namespace dflash

@@ -262,6 +262,8 @@ dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs&
   int N = 0;
   for (int i = 0; i < segs.n; ++i) N += segs.rows[i];
   if (segs.n < 1 || segs.n > kMaxSeg) return DFLASH_E_INVALID_ARG;
+  ProfScope prof(ctx, kProfGemm, st, ((double)N * K + (double)M * K) * ctx->esize + 4.0 * M * N,
+                 2.0 * M * N * K);
 
   if (ctx->cfg.dtype == DFLASH_F32) {
     SegPtrs sp;

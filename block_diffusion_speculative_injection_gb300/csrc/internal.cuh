@@ -49,6 +49,16 @@ struct LayerW {
 
 }  // namespace dflash
 
+namespace dflash {
+enum ProfKind { kProfGemm = 0, kProfAttn = 1, kProfRow = 2, kProfVocab = 3, kProfSpec = 4,
+                kProfKinds = 5 };
+struct ProfRec {
+  int kind;
+  int ev;  // index of the start event; the end event is ev + 1
+  double bytes, flops;
+};
+}  // namespace dflash
+
 struct dflash_ctx {
   dflash_config cfg;
   int device = 0;
@@ -109,6 +119,11 @@ struct dflash_ctx {
 
   int64_t launches = 0;
   std::string last_error;
+  // optional per-launch timing (dflash_profile): a pool of CUDA events
+  bool prof_on = false;
+  std::vector<cudaEvent_t> prof_ev;
+  std::vector<dflash::ProfRec> prof_recs;
+  size_t prof_next = 0;
   std::map<std::tuple<const void*, int64_t, int64_t, int>, CUtensorMap> tmaps;
 };
 
@@ -181,6 +196,30 @@ dflash_status launch_tree_accept(dflash_ctx* ctx, int batch, const int32_t* seq_
                                  cudaStream_t st);
 
 void set_error(dflash_ctx* ctx, const char* fmt, ...);
+
+// Brackets the launches of one launcher with CUDA events when profiling is
+// on; `bytes` / `flops` are the algorithmic traffic and work of the launch.
+struct ProfScope {
+  dflash_ctx* ctx;
+  cudaStream_t st;
+  int idx = -1;
+  ProfScope(dflash_ctx* c, int kind, cudaStream_t s, double bytes = 0, double flops = 0)
+      : ctx(c), st(s) {
+    if (!c->prof_on || c->prof_next + 2 > c->prof_ev.size()) return;
+    idx = (int)c->prof_next;
+    c->prof_next += 2;
+    cudaEventRecord(c->prof_ev[idx], s);
+    c->prof_recs.push_back(ProfRec{kind, idx, bytes, flops});
+  }
+  ~ProfScope() {
+    if (idx >= 0) cudaEventRecord(ctx->prof_ev[idx + 1], st);
+  }
+};
+
+int64_t block_attention_workspace(int batch, int H, int Hkv, int hd, int ctx_len, int block);
+dflash_status block_attention(int batch, int H, int Hkv, int hd, int ctx_len, int block, int causal,
+                              const void* q, const void* k, const void* v, void* out,
+                              void* workspace, int64_t workspace_bytes, cudaStream_t st);
 
 #define DF_CUDA_TRY(ctx, expr)                                                    \
   do {                                                                            \

@@ -101,6 +101,7 @@ dflash_status launch_pass_setup_full(dflash_ctx* ctx, int batch, const int32_t* 
                                      const int32_t* n_nodes, int kind, int last_only,
                                      const int32_t* anchor, int32_t* block_out, int32_t* pseq,
                                      int32_t* pctx, int32_t* pblk, cudaStream_t st) {
+  ProfScope prof__(ctx, kProfRow, st);
   PassSetupArgs a;
   a.seq_ids = seq_ids;
   a.q_lens = q_lens;
@@ -160,6 +161,7 @@ __global__ void embed_kernel(const int32_t* __restrict__ tokens, const T* __rest
 
 dflash_status launch_embed(dflash_ctx* ctx, const int32_t* tokens, int rows, int draft_block,
                            int block, cudaStream_t st) {
+  ProfScope prof__(ctx, kProfRow, st);
   const int d = ctx->cfg.d_model;
   if (ctx->cfg.dtype == DFLASH_BF16)
     embed_kernel<bf16><<<rows, 256, 0, st>>>(tokens, static_cast<const bf16*>(ctx->tok_emb),
@@ -263,6 +265,7 @@ __global__ void __launch_bounds__(kNormThreads)
 dflash_status launch_resid_norm(dflash_ctx* ctx, int rows, int splits, const void* gain,
                                 void* out, const int32_t* out_rows, int n_out, void* capture,
                                 int cap_slot, bool add, cudaStream_t st) {
+  ProfScope prof__(ctx, kProfRow, st);
   const int d = ctx->cfg.d_model;
   const float eps = ctx->cfg.rms_eps;
   if (out_rows) {
@@ -344,6 +347,7 @@ __global__ void qkv_epilogue_kernel(const float* __restrict__ ws, int splits, lo
 
 dflash_status launch_qkv_epilogue(dflash_ctx* ctx, int rows, int splits, void* kc, void* vc,
                                   cudaStream_t st) {
+  ProfScope prof__(ctx, kProfRow, st);
   const dflash_config& c = ctx->cfg;
   const long long sstride = (long long)rows * (c.n_heads + 2 * c.n_kv_heads) * c.head_dim;
   if (c.dtype == DFLASH_BF16)
@@ -381,6 +385,7 @@ __global__ void swiglu_kernel(const float* __restrict__ ws, int splits, long lon
 }
 
 dflash_status launch_swiglu(dflash_ctx* ctx, int rows, int splits, cudaStream_t st) {
+  ProfScope prof__(ctx, kProfRow, st);
   const int F = ctx->cfg.ffn_dim;
   const long long sstride = (long long)rows * 2 * F;
   const size_t n = (size_t)rows * F;
@@ -410,6 +415,7 @@ __global__ void store_act_kernel(const float* __restrict__ ws, int splits, long 
 
 dflash_status launch_store_act(dflash_ctx* ctx, int rows, int n, int splits, void* out,
                                cudaStream_t st) {
+  ProfScope prof__(ctx, kProfRow, st);
   const size_t tot = (size_t)rows * n;
   int blocks = (int)((tot + 255) / 256);
   if (blocks > 8 * ctx->sm_count) blocks = 8 * ctx->sm_count;
@@ -477,6 +483,7 @@ __global__ void inject_epilogue_kernel(const float* __restrict__ ws, int splits,
 dflash_status launch_inject_epilogue(dflash_ctx* ctx, int rows, int splits, int layer0,
                                      int n_layers, const int32_t* inj_seq,
                                      const int32_t* inj_pos, cudaStream_t st) {
+  ProfScope prof__(ctx, kProfRow, st);
   const dflash_config& c = ctx->cfg;
   const long long sstride = (long long)rows * n_layers * 2 * c.n_kv_heads * c.head_dim;
   if (c.dtype == DFLASH_BF16)

@@ -67,6 +67,7 @@ dflash_status launch_accept_linear(dflash_ctx* ctx, int batch, const int32_t* se
                                    const int32_t* block, const int32_t* argmax, int q, int mode,
                                    int32_t* accept_len, int32_t* next_anchor, int32_t* emitted,
                                    cudaStream_t st) {
+  ProfScope prof__(ctx, kProfSpec, st);
   (void)seq_ids;
   accept_linear_kernel<<<(batch + 127) / 128, 128, 0, st>>>(
       batch, q, mode, block, argmax, ctx->pass_seq, ctx->pass_ctx, ctx->pass_blk, ctx->seq_len,
@@ -200,6 +201,7 @@ __global__ void tree_build_kernel(int depth_max, int topk, int budget,
 dflash_status launch_tree_build(dflash_ctx* ctx, int batch, const int32_t* anchor,
                                 const int32_t* ids, const float* logp, int topk, int depth,
                                 int budget, const dtree_buffers* t, cudaStream_t st) {
+  ProfScope prof__(ctx, kProfSpec, st);
   tree_build_kernel<<<batch, 32, 0, st>>>(depth, topk, budget, anchor, ids, logp, *t);
   DF_LAUNCHED(ctx);
   return DFLASH_OK;
@@ -307,6 +309,7 @@ dflash_status launch_tree_accept(dflash_ctx* ctx, int batch, const int32_t* seq_
                                  const dtree_buffers* t, const int32_t* argmax,
                                  int32_t* accept_len, int32_t* next_anchor, int32_t* emitted,
                                  cudaStream_t st) {
+  ProfScope prof__(ctx, kProfSpec, st);
   (void)seq_ids;
   const dflash_config& c = ctx->cfg;
   tree_accept_kernel<<<(batch + 127) / 128, 128, 0, st>>>(

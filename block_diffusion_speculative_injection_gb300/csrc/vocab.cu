@@ -182,6 +182,7 @@ dflash_status launch_vocab_reduce(dflash_ctx* ctx, int rows, int vocab, const in
                                   int n_out, int topk, int32_t* argmax, float* margin,
                                   int32_t* topk_ids, float* topk_logp, float* logits_copy,
                                   cudaStream_t st) {
+  ProfScope prof__(ctx, kProfVocab, st);
   (void)n_out;
   if (rows <= 0) return DFLASH_OK;
   const int K = topk > 2 ? topk : 2;

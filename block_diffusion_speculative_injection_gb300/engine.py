@@ -286,3 +286,13 @@ def device_view(ptr: int, shape, dtype: torch.dtype) -> torch.Tensor:
         return torch.as_tensor(_CudaArray(ptr, shape, "<i2"), device="cuda").view(torch.bfloat16)
     code = {torch.int32: "<i4", torch.float32: "<f4", torch.int64: "<i8"}[dtype]
     return torch.as_tensor(_CudaArray(ptr, shape, code), device="cuda")
+
+
+def device_operand(which: str, n_rows: int, width: int = 128, device: str = "cuda") -> torch.Tensor:
+    """Seeded N(0,1) bf16 attention operand rows built on the device (same
+    bytes as workloads.attn_operand_rows)."""
+    pool = torch.from_numpy(wl.value_pool(wl.ATTN_SEED, 1.0, "bf16")).to(device).to(torch.bfloat16)
+    ext = torch.cat([pool, pool[:width]])
+    idx = {"q": 0, "k": 1, "v": 2, "kb": 3, "vb": 4}[which]
+    off = torch.from_numpy(wl.row_offsets(wl.ATTN_SEED, idx, n_rows)).to(device)
+    return ext.unfold(0, width, 1)[off].contiguous()

@@ -245,6 +245,49 @@ DFLASH_API dflash_status dflash_debug_view(const dflash_ctx *ctx, const char *na
 
 DFLASH_API void dflash_destroy(dflash_ctx *ctx);
 
+/* ---- op-level block attention (no context) --------------------------------
+ * The attention of one block-draft layer (Deep Research Report, "Key points":
+ * the drafter's B block positions see the injected context; report's MTP
+ * table and "Why DFlash beats EAGLE-3" item 3: bidirectional inside the
+ * block), over caller-provided bf16 tensors, head_dim 128:
+ *   q_dev   [batch][block][n_heads][128]
+ *   k_dev, v_dev [batch][n_kv_heads][ctx_len + block][128]: slots
+ *           0..ctx_len-1 hold the context, slots ctx_len.. the block's keys
+ *   out_dev [batch][block][n_heads][128]
+ * Query head h reads KV head h / (n_heads / n_kv_heads); scale 1/sqrt(128).
+ * causal = 0: every block position sees the whole block (block draft);
+ * causal = 1: block position j sees block keys 0..j (verify).
+ * workspace_dev holds split-KV partials (fp32); pass at least
+ * dflash_block_attention_workspace(...) bytes, or NULL / 0 to run without
+ * splitting the context (slower at small batch, same result up to rounding).
+ * Returns DFLASH_E_INVALID_ARG for unsupported shapes (block 1..64,
+ * n_heads / n_kv_heads must divide 64). */
+DFLASH_API dflash_status dflash_block_attention(int32_t batch, int32_t n_heads, int32_t n_kv_heads,
+                                                int32_t ctx_len, int32_t block, int32_t causal,
+                                                const void *q_dev, const void *k_dev,
+                                                const void *v_dev, void *out_dev,
+                                                void *workspace_dev, int64_t workspace_bytes,
+                                                dflash_stream_t stream);
+
+/* Bytes of workspace dflash_block_attention uses for these sizes on the
+ * current device (0: no split needed; -1: unsupported shape). */
+DFLASH_API int64_t dflash_block_attention_workspace(int32_t batch, int32_t n_heads,
+                                                    int32_t n_kv_heads, int32_t ctx_len,
+                                                    int32_t block);
+
+/* ---- per-kernel timing ------------------------------------------------------
+ * enable != 0 starts recording a CUDA event pair around every kernel launch of
+ * this context (clearing earlier records); 0 stops recording. */
+DFLASH_API dflash_status dflash_profile(dflash_ctx *ctx, int32_t enable);
+
+/* Sums the recorded launches of one kernel class (0 GEMM, 1 attention,
+ * 2 row-wise ops, 3 vocabulary reductions, 4 accept / tree; -1 all): their
+ * count, total device milliseconds, and the algorithmic bytes and flops the
+ * library assigns them (GEMM: weights + activations + fp32 output; other
+ * classes report 0).  Waits for the recorded events. */
+DFLASH_API dflash_status dflash_profile_read(dflash_ctx *ctx, int32_t kind, int64_t *launches,
+                                             double *ms, double *bytes, double *flops);
+
 #ifdef __cplusplus
 }
 #endif

@@ -26,15 +26,19 @@ def check_close(gpu, ref, atol, rtol, what):
                              f"max abs diff={np.abs(gpu - ref).max():.3e}")
 
 
-def check_argmax(gpu_ids, logits, what):
+def check_argmax(gpu_ids, logits, what, atol=2e-2, rtol=1e-2):
+    """Exact where the oracle margin exceeds 1e-2; at exempt (near-tie)
+    positions the GPU's pick must still be a near-maximal logit: within
+    twice the logit tolerance of the oracle's maximum."""
     n_checked = 0
     for j, (g, row) in enumerate(zip(gpu_ids, logits)):
         if nm.top2_margin(row) > MARGIN:
             assert int(g) == nm.argmax_lowest(row), f"{what} row {j}: gpu {g} oracle {nm.argmax_lowest(row)}"
             n_checked += 1
         else:
-            top2 = np.argsort(-row, kind="stable")[:2]
-            assert int(g) in top2, f"{what} row {j}: near-tie but gpu {g} not in top-2 {top2}"
+            top = float(np.max(row))
+            assert row[int(g)] >= top - 2 * (atol + rtol * abs(top)), \
+                f"{what} row {j}: near-tie but gpu {g} (logit {row[int(g)]}) far from max {top}"
     return n_checked
 
 

@@ -103,7 +103,14 @@ MINI_BF16_WIDE = ModelShape(
     ffn_dim=1536, vocab=5000, rope_theta=5e5, n_draft_layers=1,
     inject_layers=(1,), dtype="bf16")
 
-SHAPES: Dict[str, ModelShape] = {s.name: s for s in (TINY, QWEN3_8B, LLAMA31_8B, MINI_BF16, MINI_BF16_WIDE)}
+# Two Qwen3-8B-shaped target layers and one draft layer: the same GEMM,
+# attention and lm_head launch shapes as the full model at ~2 GB of weights
+# (used to profile single kernels).
+QWEN3_8B_SLICE = dataclasses.replace(QWEN3_8B, name="qwen3_8b_slice", n_layers=2,
+                                     n_draft_layers=1, inject_layers=(0, 1))
+
+SHAPES: Dict[str, ModelShape] = {s.name: s for s in (TINY, QWEN3_8B, LLAMA31_8B, MINI_BF16,
+                                                     MINI_BF16_WIDE, QWEN3_8B_SLICE)}
 
 
 @dataclass(frozen=True)
@@ -132,6 +139,7 @@ WORKLOADS: Dict[str, Workload] = {
                  tree_budget=64, topk=8),
         Workload("mini_bf16_e2e", MINI_BF16, 16, 3, (40, 160), 48),
         Workload("mini_bf16_ddtree", MINI_BF16, 16, 2, (96, 130), 40, tree_budget=64, topk=8),
+        Workload("qwen3_8b_slice_b1", QWEN3_8B_SLICE, 16, 1, (2048, 2048), 256),
     )
 }
 
