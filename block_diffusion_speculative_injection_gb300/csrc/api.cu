@@ -9,6 +9,7 @@
 #include <cstring>
 #include <string>
 
+#include "epilogue.cuh"
 #include "internal.cuh"
 
 namespace dflash {
@@ -170,29 +171,58 @@ static size_t cache_bytes_per_layer(const dflash_config& c, int esize) {
 // ---------------------------------------------------------------------------
 // one transformer layer (target or draft) over the rows of the current pass
 // ---------------------------------------------------------------------------
+static EpiArgs epi_base(dflash_ctx* ctx, int kind) {
+  const dflash_config& c = ctx->cfg;
+  EpiArgs e;
+  memset(&e, 0, sizeof(e));
+  e.kind = kind;
+  e.row_pos = ctx->row_pos;
+  e.row_slot = ctx->row_slot;
+  e.row_seq = ctx->row_seq;
+  e.rcos = ctx->rope_cos;
+  e.rsin = ctx->rope_sin;
+  e.H = c.n_heads;
+  e.Hkv = c.n_kv_heads;
+  e.hd = c.head_dim;
+  e.max_ctx = c.max_ctx;
+  e.max_batch = c.max_batch;
+  e.layer_elems = ctx->layer_cache_elems;
+  e.F = c.ffn_dim;
+  e.n_inject = c.n_inject;
+  e.resid = ctx->resid;
+  return e;
+}
+
 static dflash_status run_layer(dflash_ctx* ctx, const LayerW& w, int rows, void* kc, void* vc,
                                const AttnArgs& attn_base, const void* next_gain, void* capture,
                                int cap_slot, cudaStream_t st) {
   const dflash_config& c = ctx->cfg;
   const int d = c.d_model, qd = c.n_heads * c.head_dim, kvd = c.n_kv_heads * c.head_dim;
   int sp = 1;
+  EpiArgs eq = epi_base(ctx, kEpiQKV);
+  eq.q_out = ctx->qb;
+  eq.kc = kc;
+  eq.vc = vc;
   GemmSegs qkv{{w.wq, w.wk, w.wv}, {qd, kvd, kvd}, 3};
-  DF_TRY(gemm(ctx, ctx->xn, rows, d, qkv, ctx->ws, 16, &sp, st));
-  DF_TRY(launch_qkv_epilogue(ctx, rows, sp, kc, vc, st));
+  DF_TRY(gemm(ctx, ctx->xn, rows, d, qkv, eq, 16, &sp, st));
   AttnArgs a = attn_base;
   a.kc = kc;
   a.vc = vc;
   DF_TRY(attention(ctx, a, st));
+  EpiArgs er = epi_base(ctx, kEpiResid);
   GemmSegs o{{w.wo}, {d}, 1};
-  DF_TRY(gemm(ctx, ctx->ao, rows, qd, o, ctx->ws, 16, &sp, st));
-  DF_TRY(launch_resid_norm(ctx, rows, sp, w.ffn_norm, ctx->xn, nullptr, 0, nullptr, 0, true, st));
+  DF_TRY(gemm(ctx, ctx->ao, rows, qd, o, er, 16, &sp, st));
+  DF_TRY(launch_norm(ctx, rows, nullptr, w.ffn_norm, ctx->xn, st));
+  EpiArgs es = epi_base(ctx, kEpiSwiGLU);
+  es.act = ctx->act;
   GemmSegs gu{{w.w_gate, w.w_up}, {c.ffn_dim, c.ffn_dim}, 2};
-  DF_TRY(gemm(ctx, ctx->xn, rows, d, gu, ctx->ws, 16, &sp, st));
-  DF_TRY(launch_swiglu(ctx, rows, sp, st));
+  DF_TRY(gemm(ctx, ctx->xn, rows, d, gu, es, 16, &sp, st));
+  EpiArgs ed = epi_base(ctx, kEpiResid);
+  ed.capture = capture;
+  ed.cap_slot = cap_slot;
   GemmSegs dn{{w.w_down}, {d}, 1};
-  DF_TRY(gemm(ctx, ctx->act, rows, c.ffn_dim, dn, ctx->ws, 16, &sp, st));
-  DF_TRY(launch_resid_norm(ctx, rows, sp, next_gain, next_gain ? ctx->xn : nullptr, nullptr, 0,
-                           capture, cap_slot, true, st));
+  DF_TRY(gemm(ctx, ctx->act, rows, c.ffn_dim, dn, ed, 16, &sp, st));
+  if (next_gain) DF_TRY(launch_norm(ctx, rows, nullptr, next_gain, ctx->xn, st));
   return DFLASH_OK;
 }
 
@@ -209,7 +239,7 @@ static dflash_status run_lm_head(dflash_ctx* ctx, int n, int topk, int32_t* argm
     GemmSegs lm{{ctx->lm_head}, {c.vocab}, 1};
     int sp = 1;
     const void* x = static_cast<const uint8_t*>(ctx->lm_in) + (size_t)i0 * c.d_model * ctx->esize;
-    DF_TRY(gemm(ctx, x, m, c.d_model, lm, ctx->ws, 1, &sp, st));
+    DF_TRY(gemm(ctx, x, m, c.d_model, lm, epi_base(ctx, kEpiSlab), 1, &sp, st));
     DF_TRY(launch_vocab_reduce(ctx, m, c.vocab, lm_arg + i0, m, topk, argmax, margin, topk_ids,
                                topk_logp, logits, st));
   }
@@ -234,8 +264,7 @@ static dflash_status target_pass(dflash_ctx* ctx, int batch, int q, int mask,
   ab.anc = anc;
   ab.anc_words = anc_words;
   ab.max_keys_ub = c.max_ctx;
-  DF_TRY(launch_resid_norm(ctx, rows, 1, ctx->tl[0].attn_norm, ctx->xn, nullptr, 0, nullptr, 0,
-                           false, st));
+  DF_TRY(launch_norm(ctx, rows, nullptr, ctx->tl[0].attn_norm, ctx->xn, st));
   int inj = 0;
   for (int l = 0; l < c.n_target_layers; ++l) {
     const size_t off = (size_t)l * ctx->layer_cache_elems * ctx->esize;
@@ -251,8 +280,7 @@ static dflash_status target_pass(dflash_ctx* ctx, int batch, int q, int mask,
     DF_TRY(run_layer(ctx, ctx->tl[l], rows, kc, vc, ab, next_gain, cap, slot, st));
   }
   const int n_lm = last_only ? batch : rows;
-  DF_TRY(launch_resid_norm(ctx, 0, 1, ctx->final_norm, ctx->lm_in, ctx->lm_rows, n_lm, nullptr, 0,
-                           false, st));
+  DF_TRY(launch_norm(ctx, n_lm, ctx->lm_rows, ctx->final_norm, ctx->lm_in, st));
   DF_CUDA_TRY(ctx, cudaMemsetAsync(argmax, 0xFF, sizeof(int32_t) * rows, st));
   DF_TRY(run_lm_head(ctx, n_lm, 0, argmax, margin, nullptr, nullptr, logits, st));
   ctx->pending_rows = 0;
@@ -323,6 +351,7 @@ dflash_status dflash_create(const dflash_config* cfg, dflash_ctx** out) {
   };
   const size_t cache_layer_bytes = cache_bytes_per_layer(c, ctx->esize);
   alloc((void**)&ctx->seq_len, sizeof(int32_t) * c.max_batch);
+  alloc((void**)&ctx->gen_count, sizeof(int32_t) * c.max_batch);
   alloc((void**)&ctx->dev_status, sizeof(int32_t) * 4);
   alloc(&ctx->kc, cache_layer_bytes * c.n_target_layers);
   alloc(&ctx->vc, cache_layer_bytes * c.n_target_layers);
@@ -349,6 +378,8 @@ dflash_status dflash_create(const dflash_config* cfg, dflash_ctx** out) {
   alloc((void**)&ctx->inj_seq, sizeof(int32_t) * R);
   alloc((void**)&ctx->inj_pos, sizeof(int32_t) * R);
   alloc((void**)&ctx->path, sizeof(int32_t) * c.max_batch * 34);
+  ctx->n_tile_counters = 1 << 16;
+  alloc((void**)&ctx->tile_counters, sizeof(int32_t) * ctx->n_tile_counters);
   alloc((void**)&ctx->rope_cos, sizeof(float) * ctx->rope_len * (c.head_dim / 2));
   alloc((void**)&ctx->rope_sin, sizeof(float) * ctx->rope_len * (c.head_dim / 2));
   DraftMeta dm{nullptr, nullptr, nullptr};
@@ -368,6 +399,8 @@ dflash_status dflash_create(const dflash_config* cfg, dflash_ctx** out) {
              cudaMemset(ctx->dkc, 0, cache_layer_bytes * c.n_draft_layers) == cudaSuccess &&
              cudaMemset(ctx->dvc, 0, cache_layer_bytes * c.n_draft_layers) == cudaSuccess &&
              cudaMemset(ctx->seq_len, 0, sizeof(int32_t) * c.max_batch) == cudaSuccess &&
+             cudaMemset(ctx->gen_count, 0, sizeof(int32_t) * c.max_batch) == cudaSuccess &&
+             cudaMemset(ctx->tile_counters, 0, sizeof(int32_t) * ctx->n_tile_counters) == cudaSuccess &&
              cudaMemset(ctx->dev_status, 0, sizeof(int32_t) * 4) == cudaSuccess &&
              cudaMemset(ctx->inj_seq, 0xFF, sizeof(int32_t) * R) == cudaSuccess &&
              cudaMemset(ctx->capture, 0, R * c.n_inject * d * es) == cudaSuccess &&
@@ -395,12 +428,13 @@ dflash_status dflash_create(const dflash_config* cfg, dflash_ctx** out) {
 
 void dflash_destroy(dflash_ctx* ctx) {
   if (!ctx) return;
-  void* ptrs[] = {ctx->seq_len, ctx->dev_status, ctx->kc,      ctx->vc,      ctx->dkc,
+  void* ptrs[] = {ctx->seq_len, ctx->gen_count, ctx->dev_status, ctx->kc,      ctx->vc,      ctx->dkc,
                   ctx->dvc,     ctx->capture,    ctx->resid,   ctx->xn,      ctx->qb,
                   ctx->ao,      ctx->act,        ctx->fb,      ctx->lm_in,   ctx->ws,
                   ctx->part_o,  ctx->part_ml,    ctx->vk_part, ctx->vv_part, ctx->pass_seq,
                   ctx->row_pos, ctx->row_slot,   ctx->row_seq, ctx->lm_rows, ctx->inj_seq,
-                  ctx->inj_pos, ctx->path,       ctx->rope_cos, ctx->rope_sin};
+                  ctx->inj_pos, ctx->path,       ctx->rope_cos, ctx->rope_sin,
+                  ctx->tile_counters};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   for (cudaEvent_t e : ctx->prof_ev) cudaEventDestroy(e);
@@ -441,6 +475,8 @@ dflash_status dflash_reset_seq(dflash_ctx* ctx, int32_t seq_id, dflash_stream_t 
   if (seq_id < 0 || seq_id >= ctx->cfg.max_batch)
     return fail(ctx, DFLASH_E_INVALID_ARG, "seq_id %d out of range", seq_id);
   DF_CUDA_TRY(ctx, cudaMemsetAsync(ctx->seq_len + seq_id, 0, sizeof(int32_t),
+                                   (cudaStream_t)stream));
+  DF_CUDA_TRY(ctx, cudaMemsetAsync(ctx->gen_count + seq_id, 0, sizeof(int32_t),
                                    (cudaStream_t)stream));
   return DFLASH_OK;
 }
@@ -511,8 +547,7 @@ dflash_status dflash_draft_block(dflash_ctx* ctx, int32_t batch, const int32_t* 
   ctx->pass_seq = dm.seq;
   ctx->pass_ctx = dm.ctx;
   ctx->pass_blk = dm.blk;
-  dflash_status s = launch_resid_norm(ctx, rows, 1, ctx->dl[0].attn_norm, ctx->xn, nullptr, 0,
-                                      nullptr, 0, false, st);
+  dflash_status s = launch_norm(ctx, rows, nullptr, ctx->dl[0].attn_norm, ctx->xn, st);
   for (int l = 0; s == DFLASH_OK && l < c.n_draft_layers; ++l) {
     const size_t off = (size_t)l * ctx->layer_cache_elems * ctx->esize;
     void* kc = static_cast<uint8_t*>(ctx->dkc) + off;
@@ -525,8 +560,7 @@ dflash_status dflash_draft_block(dflash_ctx* ctx, int32_t batch, const int32_t* 
   ctx->pass_blk = save[2];
   if (s != DFLASH_OK) return s;
   const int n_lm = batch * (B - 1);
-  DF_TRY(launch_resid_norm(ctx, 0, 1, ctx->draft_final_norm, ctx->lm_in, ctx->lm_rows, n_lm,
-                           nullptr, 0, false, st));
+  DF_TRY(launch_norm(ctx, n_lm, ctx->lm_rows, ctx->draft_final_norm, ctx->lm_in, st));
   DF_TRY(run_lm_head(ctx, n_lm, topk, block_dev, nullptr, topk_ids_dev, topk_logp_dev, logits_dev,
                      st));
   return DFLASH_OK;
@@ -592,8 +626,9 @@ dflash_status dflash_inject_kv(dflash_ctx* ctx, int32_t n_rows, const int32_t* r
   const int d = c.d_model, kvd = c.n_kv_heads * c.head_dim;
   int sp = 1;
   GemmSegs fz{{ctx->fuse}, {d}, 1};
-  DF_TRY(gemm(ctx, hidden, rows, c.n_inject * d, fz, ctx->ws, 16, &sp, st));
-  DF_TRY(launch_store_act(ctx, rows, d, sp, ctx->fb, st));
+  EpiArgs ef = epi_base(ctx, kEpiStore);
+  ef.out = ctx->fb;
+  DF_TRY(gemm(ctx, hidden, rows, c.n_inject * d, fz, ef, 16, &sp, st));
   for (int l0 = 0; l0 < c.n_draft_layers; l0 += 6) {
     const int nl = std::min(6, c.n_draft_layers - l0);
     GemmSegs kv;
@@ -604,8 +639,13 @@ dflash_status dflash_inject_kv(dflash_ctx* ctx, int32_t n_rows, const int32_t* r
       kv.rows[2 * i] = kvd;
       kv.rows[2 * i + 1] = kvd;
     }
-    DF_TRY(gemm(ctx, ctx->fb, rows, d, kv, ctx->ws, 16, &sp, st));
-    DF_TRY(launch_inject_epilogue(ctx, rows, sp, l0, nl, rseq, rpos, st));
+    EpiArgs ei = epi_base(ctx, kEpiInject);
+    ei.row_seq = rseq;
+    ei.row_pos = rpos;
+    ei.kc = ctx->dkc;
+    ei.vc = ctx->dvc;
+    ei.layer0 = l0;
+    DF_TRY(gemm(ctx, ctx->fb, rows, d, kv, ei, 16, &sp, st));
   }
   if (!hidden_dev) ctx->pending_rows = 0;
   return DFLASH_OK;
@@ -750,6 +790,11 @@ dflash_status dflash_debug_view(const dflash_ctx* ctx, const char* name, int32_t
     if (layer < 0 || layer >= c.n_draft_layers) return DFLASH_E_INVALID_ARG;
     *dev_ptr = static_cast<const uint8_t*>(n[1] == 'k' ? ctx->dkc : ctx->dvc) + layer * lb;
     *bytes = (int64_t)lb;
+    return DFLASH_OK;
+  }
+  if (n == "gen_count") {
+    *dev_ptr = ctx->gen_count;
+    *bytes = (int64_t)c.max_batch * sizeof(int32_t);
     return DFLASH_OK;
   }
   if (n == "capture") {

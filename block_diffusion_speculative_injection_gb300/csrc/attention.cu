@@ -94,6 +94,15 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// (x0, x1) -> packed bf16 high parts and packed bf16 residuals x - hi
+__device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const __nv_bfloat162 l =
+      __floats2bfloat162_rn(x0 - __low2float(h), x1 - __high2float(h));
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
 // byte offset of 16-byte chunk c (0..15) of row r in a [rows][256 B] tile
 __device__ __forceinline__ uint32_t swz(int r, int c) {
   return (uint32_t)(r * 256 + ((c ^ (r & 7)) << 4));
@@ -305,14 +314,17 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const AttnK p) {
       o[nt][2] *= al1;
       o[nt][3] *= al1;
     }
-    // O += P V
+    // O += P V.  P is split into a bf16 high part and a bf16 residual
+    // (P = P_hi + P_lo, ~16 significant bits) and both halves go through the
+    // tensor cores, so the probabilities keep fp32-like precision; the extra
+    // MMAs are free in this HBM-bound loop.
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      uint32_t a[4];
-      a[0] = pack_bf16(s[2 * c][0], s[2 * c][1]);
-      a[1] = pack_bf16(s[2 * c][2], s[2 * c][3]);
-      a[2] = pack_bf16(s[2 * c + 1][0], s[2 * c + 1][1]);
-      a[3] = pack_bf16(s[2 * c + 1][2], s[2 * c + 1][3]);
+      uint32_t a[4], alo[4];
+      split_bf16(s[2 * c][0], s[2 * c][1], a[0], alo[0]);
+      split_bf16(s[2 * c][2], s[2 * c][3], a[1], alo[1]);
+      split_bf16(s[2 * c + 1][0], s[2 * c + 1][1], a[2], alo[2]);
+      split_bf16(s[2 * c + 1][2], s[2 * c + 1][3], a[3], alo[3]);
 #pragma unroll
       for (int np = 0; np < 8; ++np) {
         const int mi = lane >> 3;
@@ -322,6 +334,8 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const AttnK p) {
         ldsm_x4_t(smem_u32(vs + swz(r, cc)), b0, b1, b2, b3);
         mma_bf16(o[2 * np], a, b0, b1);
         mma_bf16(o[2 * np + 1], a, b2, b3);
+        mma_bf16(o[2 * np], alo, b0, b1);
+        mma_bf16(o[2 * np + 1], alo, b2, b3);
       }
     }
     __syncthreads();

@@ -1,0 +1,179 @@
+// Fused GEMM epilogues.  A GEMM writes fp32 partial tiles ("slabs", one per
+// K split); the CTA that finishes a tile (or a tile pair, for SwiGLU) last
+// sums the slabs in split order -- so the result does not depend on which
+// CTA finishes last -- and applies the operation that follows the
+// projection in the pass:
+//   QKV    RoPE on Q and K at the row's position; Q -> q_out, K/V -> cache
+//   SWIGLU act = SiLU(gate) * up            (tile pair: gate tile, up tile)
+//   RESID  residual += projection (+ bf16 capture of an injected layer)
+//   STORE  out = projection in the storage type
+//   INJECT per draft layer: K = RoPE(.), V -> draft cache at the row position
+//   SLAB   nothing (the fp32 slab is the result, e.g. lm_head logits)
+#pragma once
+
+#include "internal.cuh"
+
+namespace dflash {
+
+enum EpiKind { kEpiSlab = 0, kEpiQKV = 1, kEpiSwiGLU = 2, kEpiResid = 3, kEpiStore = 4,
+               kEpiInject = 5 };
+
+struct EpiArgs {
+  int kind;
+  int M, N, splits;
+  long long split_stride;  // elements between slabs (= M * N)
+  const float* slab;
+  int32_t* counters;
+  // QKV / INJECT
+  const int32_t* row_pos;
+  const int32_t* row_slot;
+  const int32_t* row_seq;
+  const float* rcos;
+  const float* rsin;
+  void* q_out;
+  void* kc;  // QKV: this layer's cache base; INJECT: draft cache base (all layers)
+  void* vc;
+  int H, Hkv, hd, max_ctx, max_batch;
+  size_t layer_elems;
+  int layer0;
+  // SWIGLU
+  void* act;
+  int F;
+  // RESID
+  float* resid;
+  void* capture;
+  int cap_slot, n_inject;
+  // STORE
+  void* out;
+  int32_t* status;
+};
+
+template <typename T>
+__device__ __forceinline__ float slab_sum(const EpiArgs& e, int t, int n) {
+  const float* p = e.slab + (size_t)t * e.N + n;
+  float v = 0.f;
+  int s = 0;
+  for (; s + 4 <= e.splits; s += 4) {
+    const float a = p[(size_t)s * e.split_stride], b = p[(size_t)(s + 1) * e.split_stride];
+    const float c = p[(size_t)(s + 2) * e.split_stride], d = p[(size_t)(s + 3) * e.split_stride];
+    v += a;
+    v += b;
+    v += c;
+    v += d;
+  }
+  for (; s < e.splits; ++s) v += p[(size_t)s * e.split_stride];
+  return v;
+}
+
+// RoPE-rotated head (64 pairs of one 128-wide tile) for rows m0..m1.
+template <typename T, bool kInject>
+__device__ void epi_rotate_head(const EpiArgs& e, int n0, int m0, int m1, T* dst_base, int head,
+                                bool is_q) {
+  const int half = e.hd / 2;
+  for (int idx = threadIdx.x; idx < (m1 - m0) * half; idx += blockDim.x) {
+    const int t = m0 + idx / half, i = idx % half;
+    int pos, seq, slot;
+    if (kInject) {
+      seq = e.row_seq[t];
+      pos = e.row_pos[t];
+      slot = pos;
+      if (seq < 0) continue;
+      if (seq >= e.max_batch || pos < 0 || pos >= e.max_ctx) {
+        set_dev_status(e.status, kDevCheck);
+        continue;
+      }
+    } else {
+      pos = e.row_pos[t];
+      if (pos < 0) continue;
+      seq = e.row_seq[t];
+      slot = e.row_slot[t];
+    }
+    const float lo = slab_sum<T>(e, t, n0 + i), hi = slab_sum<T>(e, t, n0 + i + half);
+    const float c = e.rcos[(size_t)pos * half + i], s = e.rsin[(size_t)pos * half + i];
+    T* dst = is_q ? dst_base + ((size_t)t * e.H + head) * e.hd
+                  : dst_base + (((size_t)seq * e.Hkv + head) * e.max_ctx + slot) * e.hd;
+    st_f(dst + i, lo * c - hi * s);
+    st_f(dst + i + half, hi * c + lo * s);
+  }
+}
+
+template <typename T, bool kInject>
+__device__ void epi_copy_head(const EpiArgs& e, int n0, int m0, int m1, T* dst_base, int head) {
+  for (int idx = threadIdx.x; idx < (m1 - m0) * e.hd; idx += blockDim.x) {
+    const int t = m0 + idx / e.hd, c = idx % e.hd;
+    int seq, slot;
+    if (kInject) {
+      seq = e.row_seq[t];
+      slot = e.row_pos[t];
+      if (seq < 0 || seq >= e.max_batch || slot < 0 || slot >= e.max_ctx) continue;
+    } else {
+      if (e.row_pos[t] < 0) continue;
+      seq = e.row_seq[t];
+      slot = e.row_slot[t];
+    }
+    st_f(dst_base + (((size_t)seq * e.Hkv + head) * e.max_ctx + slot) * e.hd + c,
+         slab_sum<T>(e, t, n0 + c));
+  }
+}
+
+// Runs the epilogue of the 128-feature tile starting at n0, rows m0..m0+BN-1.
+// All threads of the CTA take part (any block size).
+template <typename T>
+__device__ void run_epilogue(const EpiArgs& e, int n0, int m0, int BN) {
+  const int m1 = min(e.M, m0 + BN);
+  switch (e.kind) {
+    case kEpiQKV: {  // a 128-wide tile holds 128 / head_dim whole heads
+      for (int h0 = n0; h0 < min(e.N, n0 + 128); h0 += e.hd) {
+        const int head = h0 / e.hd;
+        if (head < e.H)
+          epi_rotate_head<T, false>(e, h0, m0, m1, static_cast<T*>(e.q_out), head, true);
+        else if (head < e.H + e.Hkv)
+          epi_rotate_head<T, false>(e, h0, m0, m1, static_cast<T*>(e.kc), head - e.H, false);
+        else
+          epi_copy_head<T, false>(e, h0, m0, m1, static_cast<T*>(e.vc), head - e.H - e.Hkv);
+      }
+      break;
+    }
+    case kEpiInject: {
+      const int kvd = e.Hkv * e.hd;
+      for (int h0 = n0; h0 < min(e.N, n0 + 128); h0 += e.hd) {
+        const int l = h0 / (2 * kvd), o = h0 % (2 * kvd);
+        T* kbase = static_cast<T*>(e.kc) + (size_t)(e.layer0 + l) * e.layer_elems;
+        T* vbase = static_cast<T*>(e.vc) + (size_t)(e.layer0 + l) * e.layer_elems;
+        if (o < kvd)
+          epi_rotate_head<T, true>(e, h0, m0, m1, kbase, o / e.hd, false);
+        else
+          epi_copy_head<T, true>(e, h0, m0, m1, vbase, (o - kvd) / e.hd);
+      }
+      break;
+    }
+    case kEpiSwiGLU: {
+      for (int f = n0 + (int)threadIdx.x; f < min(e.F, n0 + 128); f += blockDim.x)
+        for (int t = m0; t < m1; ++t) {
+          const float g = slab_sum<T>(e, t, f), u = slab_sum<T>(e, t, e.F + f);
+          st_f(static_cast<T*>(e.act) + (size_t)t * e.F + f, g / (1.f + __expf(-g)) * u);
+        }
+      break;
+    }
+    case kEpiResid: {
+      T* cap = static_cast<T*>(e.capture);
+      for (int n = n0 + (int)threadIdx.x; n < min(e.N, n0 + 128); n += blockDim.x)
+        for (int t = m0; t < m1; ++t) {
+          const float r = e.resid[(size_t)t * e.N + n] + slab_sum<T>(e, t, n);
+          e.resid[(size_t)t * e.N + n] = r;
+          if (cap) st_f(cap + ((size_t)t * e.n_inject + e.cap_slot) * e.N + n, r);
+        }
+      break;
+    }
+    case kEpiStore: {
+      for (int n = n0 + (int)threadIdx.x; n < min(e.N, n0 + 128); n += blockDim.x)
+        for (int t = m0; t < m1; ++t)
+          st_f(static_cast<T*>(e.out) + (size_t)t * e.N + n, slab_sum<T>(e, t, n));
+      break;
+    }
+    default:
+      break;
+  }
+}
+
+}  // namespace dflash

@@ -13,6 +13,7 @@
 #include <cstdio>
 #include <cstring>
 
+#include "epilogue.cuh"
 #include "internal.cuh"
 
 namespace dflash {
@@ -31,6 +32,7 @@ struct TcParams {
   float* out;
   long long split_stride;
   int32_t* status;
+  EpiArgs epi;
 };
 
 __global__ void __launch_bounds__(128, 1)
@@ -130,6 +132,37 @@ __global__ void __launch_bounds__(128, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, tmem_cols);
+  if (p.epi.kind == kEpiSlab) return;
+
+  // fused epilogue: the CTA that completes a tile (pair) last reduces it
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  int n0_epi = n0;
+  if (threadIdx.x == 0) {
+    int group, expect;
+    if (p.epi.kind == kEpiSwiGLU) {
+      const int half_tiles = (p.epi.F + 127) / 128;
+      group = (blockIdx.x % half_tiles) * gridDim.y + blockIdx.y;
+      expect = 2 * gridDim.z;
+    } else {
+      group = blockIdx.x * gridDim.y + blockIdx.y;
+      expect = gridDim.z;
+    }
+    const int old = atomicAdd(&p.epi.counters[group], 1);
+    s_last = (old == expect - 1);
+    if (s_last) p.epi.counters[group] = 0;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (p.epi.kind == kEpiSwiGLU) n0_epi = (blockIdx.x % ((p.epi.F + 127) / 128)) * 128;
+  run_epilogue<bf16>(p.epi, n0_epi, m0, BN);
+}
+
+// fp32 storage: the epilogue runs as its own kernel over the slab (splits = 1)
+__global__ void __launch_bounds__(128) epilogue_f32_kernel(const EpiArgs e) {
+  run_epilogue<float>(e, blockIdx.x * 128, 0, e.M);
 }
 
 // ---------------------------------------------------------------------------
@@ -254,7 +287,8 @@ static size_t tc_smem_bytes(int BN, int stages) {
 }
 
 dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs& segs,
-                   float* out, int max_splits, int* splits_used, cudaStream_t st) {
+                   const EpiArgs& epi_in, int max_splits, int* splits_used, cudaStream_t st) {
+  float* out = ctx->ws;
   if (M <= 0) {
     *splits_used = 1;
     return DFLASH_OK;
@@ -282,6 +316,18 @@ dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs&
     gemm_f32_kernel<<<grid, 256, 0, st>>>(static_cast<const float*>(x), M, K, sp, N, out);
     DF_LAUNCHED(ctx);
     *splits_used = 1;
+    if (epi_in.kind != kEpiSlab) {
+      EpiArgs e = epi_in;
+      e.M = M;
+      e.N = N;
+      e.splits = 1;
+      e.split_stride = (long long)M * N;
+      e.slab = out;
+      e.status = ctx->dev_status;
+      const int groups = e.kind == kEpiSwiGLU ? (e.F + 127) / 128 : (N + 127) / 128;
+      epilogue_f32_kernel<<<groups, 128, 0, st>>>(e);
+      DF_LAUNCHED(ctx);
+    }
     return DFLASH_OK;
   }
 
@@ -339,6 +385,18 @@ dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs&
   p.out = out;
   p.split_stride = (long long)M * N;
   p.status = ctx->dev_status;
+  p.epi = epi_in;
+  p.epi.M = M;
+  p.epi.N = N;
+  p.epi.splits = splits;
+  p.epi.split_stride = (long long)M * N;
+  p.epi.slab = out;
+  p.epi.counters = ctx->tile_counters;
+  p.epi.status = ctx->dev_status;
+  if (p.epi.kind != kEpiSlab && (size_t)n_tiles * m_tiles > ctx->n_tile_counters) {
+    set_error(ctx, "GEMM has more tiles than tile counters");
+    return DFLASH_E_CAPACITY;
+  }
 
   static bool attr_set = false;
   if (!attr_set) {

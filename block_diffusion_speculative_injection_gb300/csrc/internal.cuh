@@ -73,6 +73,7 @@ struct dflash_ctx {
 
   // per-sequence state
   int32_t* seq_len = nullptr;        // [max_batch] committed length
+  int32_t* gen_count = nullptr;      // [max_batch] tokens emitted since reset
   std::vector<int64_t> host_len_ub;  // host upper bound of each slot's length
   int32_t* dev_status = nullptr;     // [1]
 
@@ -117,6 +118,9 @@ struct dflash_ctx {
   int last_batch = 0, last_q = 0;
   int pending_rows = 0;  // rows of the injection queue (capture rows)
 
+  int32_t* tile_counters = nullptr;  // GEMM split-K completion tickets (self-resetting)
+  size_t n_tile_counters = 0;
+
   int64_t launches = 0;
   std::string last_error;
   // optional per-launch timing (dflash_profile): a pool of CUDA events
@@ -138,10 +142,12 @@ struct GemmSegs {
   int n;
 };
 
-// out[split][M][N] (fp32) = X[M][K] . W^T, W = vertical stack of the segments.
-// Returns the number of K splits used (the caller reduces them).
+struct EpiArgs;
+// X[M][K] . W^T with W the vertical stack of the segments, then the fused
+// epilogue described by `epi` (see epilogue.cuh).  The fp32 result / K-split
+// slabs live in ctx->ws; *splits_used reports the split count.
 dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs& segs,
-                   float* out, int max_splits, int* splits_used, cudaStream_t st);
+                   const EpiArgs& epi, int max_splits, int* splits_used, cudaStream_t st);
 
 enum MaskKind { kMaskNone = 0, kMaskCausal = 1, kMaskTree = 2 };
 
@@ -166,17 +172,9 @@ dflash_status launch_pass_setup_full(dflash_ctx* ctx, int batch, const int32_t* 
                                      int32_t* pctx, int32_t* pblk, cudaStream_t st);
 dflash_status launch_embed(dflash_ctx* ctx, const int32_t* tokens, int rows, int draft_block,
                            int block, cudaStream_t st);
-dflash_status launch_resid_norm(dflash_ctx* ctx, int rows, int splits, const void* gain,
-                                void* out, const int32_t* out_rows, int n_out, void* capture,
-                                int cap_slot, bool add, cudaStream_t st);
-dflash_status launch_qkv_epilogue(dflash_ctx* ctx, int rows, int splits, void* kc, void* vc,
-                                  cudaStream_t st);
-dflash_status launch_swiglu(dflash_ctx* ctx, int rows, int splits, cudaStream_t st);
-dflash_status launch_store_act(dflash_ctx* ctx, int rows, int n, int splits, void* out,
-                               cudaStream_t st);
-dflash_status launch_inject_epilogue(dflash_ctx* ctx, int rows, int splits, int layer0,
-                                     int n_layers, const int32_t* inj_seq,
-                                     const int32_t* inj_pos, cudaStream_t st);
+// out[i] = RMSNorm(resid[rows_in ? rows_in[i] : i]) * gain, i < n_out
+dflash_status launch_norm(dflash_ctx* ctx, int n_out, const int32_t* rows_in, const void* gain,
+                          void* out, cudaStream_t st);
 dflash_status launch_vocab_reduce(dflash_ctx* ctx, int rows, int vocab, const int32_t* row_out,
                                   int n_out, int topk, int32_t* argmax, float* margin,
                                   int32_t* topk_ids, float* topk_logp, float* logits_copy,

@@ -178,7 +178,7 @@ dflash_status launch_embed(dflash_ctx* ctx, const int32_t* tokens, int rows, int
 }
 
 // ---------------------------------------------------------------------------
-// residual add + RMSNorm (+ capture), and the gathered final norm
+// RMSNorm of residual rows into the next GEMM's input (optionally gathered)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float block_sum(float v, float* red) {
 #pragma unroll
@@ -198,49 +198,11 @@ constexpr int kNormMaxPer = 32;  // d_model <= 8192
 
 template <typename T>
 __global__ void __launch_bounds__(kNormThreads)
-    resid_norm_kernel(float* __restrict__ resid, const float* __restrict__ ws, int splits,
-                      long long split_stride, int d, const T* __restrict__ gain,
-                      T* __restrict__ out, T* __restrict__ capture, int cap_slot, int n_inject,
-                      float eps, int add) {
-  __shared__ float red[32];
-  const int r = blockIdx.x;
-  float x[kNormMaxPer];
-  float ss = 0.f;
-  const int per = (d + kNormThreads - 1) / kNormThreads;
-#pragma unroll
-  for (int k = 0; k < kNormMaxPer; ++k) {
-    if (k >= per) break;
-    const int i = threadIdx.x + k * kNormThreads;
-    float v = 0.f;
-    if (i < d) {
-      v = resid[(size_t)r * d + i];
-      if (add) {
-        for (int s = 0; s < splits; ++s) v += ws[(size_t)s * split_stride + (size_t)r * d + i];
-        resid[(size_t)r * d + i] = v;
-      }
-      if (capture) st_f(capture + ((size_t)r * n_inject + cap_slot) * d + i, v);
-    }
-    x[k] = v;
-    ss += v * v;
-  }
-  if (!out) return;
-  const float tot = block_sum(ss, red);
-  const float inv = rsqrtf(tot / (float)d + eps);
-#pragma unroll
-  for (int k = 0; k < kNormMaxPer; ++k) {
-    if (k >= per) break;
-    const int i = threadIdx.x + k * kNormThreads;
-    if (i < d) st_f(out + (size_t)r * d + i, x[k] * inv * ld_f(gain + i));
-  }
-}
-
-template <typename T>
-__global__ void __launch_bounds__(kNormThreads)
-    gather_norm_kernel(const float* __restrict__ resid, const int32_t* __restrict__ rows_in,
-                       int d, const T* __restrict__ gain, T* __restrict__ out, float eps) {
+    norm_kernel(const float* __restrict__ resid, const int32_t* __restrict__ rows_in, int d,
+                const T* __restrict__ gain, T* __restrict__ out, float eps) {
   __shared__ float red[32];
   const int i_out = blockIdx.x;
-  const int r = rows_in[i_out];
+  const int r = rows_in ? rows_in[i_out] : i_out;
   float x[kNormMaxPer];
   float ss = 0.f;
   const int per = (d + kNormThreads - 1) / kNormThreads;
@@ -262,240 +224,18 @@ __global__ void __launch_bounds__(kNormThreads)
   }
 }
 
-dflash_status launch_resid_norm(dflash_ctx* ctx, int rows, int splits, const void* gain,
-                                void* out, const int32_t* out_rows, int n_out, void* capture,
-                                int cap_slot, bool add, cudaStream_t st) {
+dflash_status launch_norm(dflash_ctx* ctx, int n_out, const int32_t* rows_in, const void* gain,
+                          void* out, cudaStream_t st) {
   ProfScope prof__(ctx, kProfRow, st);
+  if (n_out <= 0) return DFLASH_OK;
   const int d = ctx->cfg.d_model;
   const float eps = ctx->cfg.rms_eps;
-  if (out_rows) {
-    if (ctx->cfg.dtype == DFLASH_BF16)
-      gather_norm_kernel<bf16><<<n_out, kNormThreads, 0, st>>>(
-          ctx->resid, out_rows, d, static_cast<const bf16*>(gain), static_cast<bf16*>(out), eps);
-    else
-      gather_norm_kernel<float><<<n_out, kNormThreads, 0, st>>>(
-          ctx->resid, out_rows, d, static_cast<const float*>(gain), static_cast<float*>(out),
-          eps);
-    DF_LAUNCHED(ctx);
-    return DFLASH_OK;
-  }
-  const long long stride = (long long)rows * d;
   if (ctx->cfg.dtype == DFLASH_BF16)
-    resid_norm_kernel<bf16><<<rows, kNormThreads, 0, st>>>(
-        ctx->resid, ctx->ws, splits, stride, d, static_cast<const bf16*>(gain),
-        static_cast<bf16*>(out), static_cast<bf16*>(capture), cap_slot, ctx->cfg.n_inject, eps,
-        add ? 1 : 0);
+    norm_kernel<bf16><<<n_out, kNormThreads, 0, st>>>(
+        ctx->resid, rows_in, d, static_cast<const bf16*>(gain), static_cast<bf16*>(out), eps);
   else
-    resid_norm_kernel<float><<<rows, kNormThreads, 0, st>>>(
-        ctx->resid, ctx->ws, splits, stride, d, static_cast<const float*>(gain),
-        static_cast<float*>(out), static_cast<float*>(capture), cap_slot, ctx->cfg.n_inject, eps,
-        add ? 1 : 0);
-  DF_LAUNCHED(ctx);
-  return DFLASH_OK;
-}
-
-// ---------------------------------------------------------------------------
-// QKV epilogue: RoPE on Q and K at the row's position; Q -> qb, K/V -> cache
-// ---------------------------------------------------------------------------
-template <typename T>
-__global__ void qkv_epilogue_kernel(const float* __restrict__ ws, int splits, long long sstride,
-                                    const int32_t* __restrict__ row_pos,
-                                    const int32_t* __restrict__ row_slot,
-                                    const int32_t* __restrict__ row_seq,
-                                    const float* __restrict__ rcos, const float* __restrict__ rsin,
-                                    T* __restrict__ qb, T* __restrict__ kc, T* __restrict__ vc,
-                                    int H, int Hkv, int hd, int max_ctx) {
-  const int r = blockIdx.x;
-  const int pos = row_pos[r];
-  if (pos < 0) return;
-  const int slot = row_slot[r], seq = row_seq[r];
-  const int half = hd / 2;
-  const int N = (H + 2 * Hkv) * hd;
-  const float* src = ws + (size_t)r * N;
-  const int n_pairs = (H + Hkv) * half;  // rotated pairs (Q and K heads)
-  for (int i = threadIdx.x; i < n_pairs + Hkv * hd; i += blockDim.x) {
-    if (i < n_pairs) {
-      const int head = i / half, p = i % half;  // head < H: query, else key
-      const int col = head * hd + p;
-      float lo = 0.f, hi = 0.f;
-      for (int s = 0; s < splits; ++s) {
-        lo += src[(size_t)s * sstride + col];
-        hi += src[(size_t)s * sstride + col + half];
-      }
-      const float c = rcos[(size_t)pos * half + p], sn = rsin[(size_t)pos * half + p];
-      const float olo = lo * c - hi * sn, ohi = hi * c + lo * sn;
-      if (head < H) {
-        T* dst = qb + ((size_t)r * H + head) * hd;
-        st_f(dst + p, olo);
-        st_f(dst + p + half, ohi);
-      } else {
-        const int kh = head - H;
-        T* dst = kc + (((size_t)seq * Hkv + kh) * max_ctx + slot) * hd;
-        st_f(dst + p, olo);
-        st_f(dst + p + half, ohi);
-      }
-    } else {
-      const int v = i - n_pairs;
-      const int kh = v / hd, e = v % hd;
-      const int col = (H + Hkv) * hd + v;
-      float acc = 0.f;
-      for (int s = 0; s < splits; ++s) acc += src[(size_t)s * sstride + col];
-      st_f(vc + (((size_t)seq * Hkv + kh) * max_ctx + slot) * hd + e, acc);
-    }
-  }
-}
-
-dflash_status launch_qkv_epilogue(dflash_ctx* ctx, int rows, int splits, void* kc, void* vc,
-                                  cudaStream_t st) {
-  ProfScope prof__(ctx, kProfRow, st);
-  const dflash_config& c = ctx->cfg;
-  const long long sstride = (long long)rows * (c.n_heads + 2 * c.n_kv_heads) * c.head_dim;
-  if (c.dtype == DFLASH_BF16)
-    qkv_epilogue_kernel<bf16><<<rows, 256, 0, st>>>(
-        ctx->ws, splits, sstride, ctx->row_pos, ctx->row_slot, ctx->row_seq, ctx->rope_cos,
-        ctx->rope_sin, static_cast<bf16*>(ctx->qb), static_cast<bf16*>(kc),
-        static_cast<bf16*>(vc), c.n_heads, c.n_kv_heads, c.head_dim, c.max_ctx);
-  else
-    qkv_epilogue_kernel<float><<<rows, 256, 0, st>>>(
-        ctx->ws, splits, sstride, ctx->row_pos, ctx->row_slot, ctx->row_seq, ctx->rope_cos,
-        ctx->rope_sin, static_cast<float*>(ctx->qb), static_cast<float*>(kc),
-        static_cast<float*>(vc), c.n_heads, c.n_kv_heads, c.head_dim, c.max_ctx);
-  DF_LAUNCHED(ctx);
-  return DFLASH_OK;
-}
-
-// ---------------------------------------------------------------------------
-// SwiGLU: act = SiLU(gate) * up  (GEMM columns: [gate | up])
-// ---------------------------------------------------------------------------
-template <typename T>
-__global__ void swiglu_kernel(const float* __restrict__ ws, int splits, long long sstride,
-                              int rows, int F, T* __restrict__ act) {
-  const size_t n = (size_t)rows * F;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
-       i += (size_t)gridDim.x * blockDim.x) {
-    const size_t r = i / F, f = i % F;
-    float g = 0.f, u = 0.f;
-    for (int s = 0; s < splits; ++s) {
-      g += ws[(size_t)s * sstride + r * 2 * F + f];
-      u += ws[(size_t)s * sstride + r * 2 * F + F + f];
-    }
-    const float silu = g / (1.f + __expf(-g));
-    st_f(act + i, silu * u);
-  }
-}
-
-dflash_status launch_swiglu(dflash_ctx* ctx, int rows, int splits, cudaStream_t st) {
-  ProfScope prof__(ctx, kProfRow, st);
-  const int F = ctx->cfg.ffn_dim;
-  const long long sstride = (long long)rows * 2 * F;
-  const size_t n = (size_t)rows * F;
-  int blocks = (int)((n + 255) / 256);
-  if (blocks > 8 * ctx->sm_count) blocks = 8 * ctx->sm_count;
-  if (ctx->cfg.dtype == DFLASH_BF16)
-    swiglu_kernel<bf16><<<blocks, 256, 0, st>>>(ctx->ws, splits, sstride, rows, F,
-                                                static_cast<bf16*>(ctx->act));
-  else
-    swiglu_kernel<float><<<blocks, 256, 0, st>>>(ctx->ws, splits, sstride, rows, F,
-                                                 static_cast<float*>(ctx->act));
-  DF_LAUNCHED(ctx);
-  return DFLASH_OK;
-}
-
-// out[r][n] = sum of splits, in the storage type
-template <typename T>
-__global__ void store_act_kernel(const float* __restrict__ ws, int splits, long long sstride,
-                                 size_t n, T* __restrict__ out) {
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
-       i += (size_t)gridDim.x * blockDim.x) {
-    float v = 0.f;
-    for (int s = 0; s < splits; ++s) v += ws[(size_t)s * sstride + i];
-    st_f(out + i, v);
-  }
-}
-
-dflash_status launch_store_act(dflash_ctx* ctx, int rows, int n, int splits, void* out,
-                               cudaStream_t st) {
-  ProfScope prof__(ctx, kProfRow, st);
-  const size_t tot = (size_t)rows * n;
-  int blocks = (int)((tot + 255) / 256);
-  if (blocks > 8 * ctx->sm_count) blocks = 8 * ctx->sm_count;
-  if (ctx->cfg.dtype == DFLASH_BF16)
-    store_act_kernel<bf16><<<blocks, 256, 0, st>>>(ctx->ws, splits, (long long)tot, tot,
-                                                   static_cast<bf16*>(out));
-  else
-    store_act_kernel<float><<<blocks, 256, 0, st>>>(ctx->ws, splits, (long long)tot, tot,
-                                                    static_cast<float*>(out));
-  DF_LAUNCHED(ctx);
-  return DFLASH_OK;
-}
-
-// ---------------------------------------------------------------------------
-// KV injection epilogue: GEMM columns per draft layer l: [K_l (kv) | V_l (kv)]
-// ---------------------------------------------------------------------------
-template <typename T>
-__global__ void inject_epilogue_kernel(const float* __restrict__ ws, int splits,
-                                       long long sstride, const int32_t* __restrict__ inj_seq,
-                                       const int32_t* __restrict__ inj_pos,
-                                       const float* __restrict__ rcos,
-                                       const float* __restrict__ rsin, T* __restrict__ dkc,
-                                       T* __restrict__ dvc, size_t layer_elems, int layer0,
-                                       int n_layers, int Hkv, int hd, int max_ctx, int max_batch,
-                                       int32_t* status) {
-  const int r = blockIdx.x;
-  const int seq = inj_seq[r], pos = inj_pos[r];
-  if (seq < 0) return;
-  if (seq >= max_batch || pos < 0 || pos >= max_ctx) {
-    set_dev_status(status, kDevCheck);
-    return;
-  }
-  const int half = hd / 2;
-  const int kv = Hkv * hd;
-  const int N = n_layers * 2 * kv;
-  const float* src = ws + (size_t)r * N;
-  const int per_layer = Hkv * half + kv;  // rotated K pairs + V elements
-  for (int i = threadIdx.x; i < n_layers * per_layer; i += blockDim.x) {
-    const int l = i / per_layer, w = i % per_layer;
-    const size_t lbase = (size_t)(layer0 + l) * layer_elems;
-    const int cbase = l * 2 * kv;
-    if (w < Hkv * half) {
-      const int kh = w / half, p = w % half;
-      const int col = cbase + kh * hd + p;
-      float lo = 0.f, hi = 0.f;
-      for (int s = 0; s < splits; ++s) {
-        lo += src[(size_t)s * sstride + col];
-        hi += src[(size_t)s * sstride + col + half];
-      }
-      const float c = rcos[(size_t)pos * half + p], sn = rsin[(size_t)pos * half + p];
-      T* dst = dkc + lbase + (((size_t)seq * Hkv + kh) * max_ctx + pos) * hd;
-      st_f(dst + p, lo * c - hi * sn);
-      st_f(dst + p + half, hi * c + lo * sn);
-    } else {
-      const int v = w - Hkv * half;
-      const int kh = v / hd, e = v % hd;
-      const int col = cbase + kv + v;
-      float acc = 0.f;
-      for (int s = 0; s < splits; ++s) acc += src[(size_t)s * sstride + col];
-      st_f(dvc + lbase + (((size_t)seq * Hkv + kh) * max_ctx + pos) * hd + e, acc);
-    }
-  }
-}
-
-dflash_status launch_inject_epilogue(dflash_ctx* ctx, int rows, int splits, int layer0,
-                                     int n_layers, const int32_t* inj_seq,
-                                     const int32_t* inj_pos, cudaStream_t st) {
-  ProfScope prof__(ctx, kProfRow, st);
-  const dflash_config& c = ctx->cfg;
-  const long long sstride = (long long)rows * n_layers * 2 * c.n_kv_heads * c.head_dim;
-  if (c.dtype == DFLASH_BF16)
-    inject_epilogue_kernel<bf16><<<rows, 256, 0, st>>>(
-        ctx->ws, splits, sstride, inj_seq, inj_pos, ctx->rope_cos, ctx->rope_sin,
-        static_cast<bf16*>(ctx->dkc), static_cast<bf16*>(ctx->dvc), ctx->layer_cache_elems,
-        layer0, n_layers, c.n_kv_heads, c.head_dim, c.max_ctx, c.max_batch, ctx->dev_status);
-  else
-    inject_epilogue_kernel<float><<<rows, 256, 0, st>>>(
-        ctx->ws, splits, sstride, inj_seq, inj_pos, ctx->rope_cos, ctx->rope_sin,
-        static_cast<float*>(ctx->dkc), static_cast<float*>(ctx->dvc), ctx->layer_cache_elems,
-        layer0, n_layers, c.n_kv_heads, c.head_dim, c.max_ctx, c.max_batch, ctx->dev_status);
+    norm_kernel<float><<<n_out, kNormThreads, 0, st>>>(
+        ctx->resid, rows_in, d, static_cast<const float*>(gain), static_cast<float*>(out), eps);
   DF_LAUNCHED(ctx);
   return DFLASH_OK;
 }

@@ -25,7 +25,8 @@ __global__ void accept_linear_kernel(int batch, int q, int mode, const int32_t* 
                                      const int32_t* __restrict__ pass_seq,
                                      const int32_t* __restrict__ pass_ctx,
                                      const int32_t* __restrict__ pass_blk,
-                                     int32_t* __restrict__ seq_len, int32_t* __restrict__ accept_len,
+                                     int32_t* __restrict__ seq_len, int32_t* __restrict__ gen_count,
+                                     int32_t* __restrict__ accept_len,
                                      int32_t* __restrict__ next_anchor,
                                      int32_t* __restrict__ emitted, int32_t* __restrict__ inj_seq,
                                      int32_t* __restrict__ inj_pos) {
@@ -56,7 +57,10 @@ __global__ void accept_linear_kernel(int batch, int q, int mode, const int32_t* 
     next_anchor[b] = y;
     commit = a + 1;
   }
-  if (n > 0) seq_len[seq] = ctx + commit;
+  if (n > 0) {
+    seq_len[seq] = ctx + commit;
+    gen_count[seq] += mode == DFLASH_ACCEPT_ALL ? 1 : commit;
+  }
   for (int j = 0; j < q; ++j) {
     inj_seq[base + j] = j < commit ? seq : -1;
     inj_pos[base + j] = ctx + j;
@@ -71,7 +75,7 @@ dflash_status launch_accept_linear(dflash_ctx* ctx, int batch, const int32_t* se
   (void)seq_ids;
   accept_linear_kernel<<<(batch + 127) / 128, 128, 0, st>>>(
       batch, q, mode, block, argmax, ctx->pass_seq, ctx->pass_ctx, ctx->pass_blk, ctx->seq_len,
-      accept_len, next_anchor, emitted, ctx->inj_seq, ctx->inj_pos);
+      ctx->gen_count, accept_len, next_anchor, emitted, ctx->inj_seq, ctx->inj_pos);
   DF_LAUNCHED(ctx);
   return DFLASH_OK;
 }
@@ -216,7 +220,8 @@ __global__ void tree_accept_kernel(int batch, dtree_buffers t, const int32_t* __
                                    const int32_t* __restrict__ pass_seq,
                                    const int32_t* __restrict__ pass_ctx,
                                    const int32_t* __restrict__ pass_blk,
-                                   int32_t* __restrict__ seq_len, int32_t* __restrict__ accept_len,
+                                   int32_t* __restrict__ seq_len, int32_t* __restrict__ gen_count,
+                                   int32_t* __restrict__ accept_len,
                                    int32_t* __restrict__ next_anchor, int32_t* __restrict__ emitted,
                                    int32_t* __restrict__ inj_seq, int32_t* __restrict__ inj_pos,
                                    int32_t* __restrict__ path, int32_t* status) {
@@ -270,6 +275,7 @@ __global__ void tree_accept_kernel(int batch, dtree_buffers t, const int32_t* __
     inj_pos[base + pb[2 + i]] = ctx + i;
   }
   seq_len[seq] = ctx + a + 1;
+  gen_count[seq] += a + 1;
 }
 
 // One CTA per (layer, sequence, KV head): gather every accepted row first,
@@ -313,7 +319,8 @@ dflash_status launch_tree_accept(dflash_ctx* ctx, int batch, const int32_t* seq_
   (void)seq_ids;
   const dflash_config& c = ctx->cfg;
   tree_accept_kernel<<<(batch + 127) / 128, 128, 0, st>>>(
-      batch, *t, argmax, ctx->pass_seq, ctx->pass_ctx, ctx->pass_blk, ctx->seq_len, accept_len,
+      batch, *t, argmax, ctx->pass_seq, ctx->pass_ctx, ctx->pass_blk, ctx->seq_len, ctx->gen_count,
+      accept_len,
       next_anchor, emitted, ctx->inj_seq, ctx->inj_pos, ctx->path, ctx->dev_status);
   DF_LAUNCHED(ctx);
   dim3 grid(c.n_target_layers * batch, c.n_kv_heads);

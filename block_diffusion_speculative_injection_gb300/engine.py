@@ -144,6 +144,11 @@ class DFlashEngine:
         torch.cuda.synchronize()
         return v[:batch].tolist()
 
+    def gen_counts(self) -> torch.Tensor:
+        """Live device view of the per-slot emitted-token counters."""
+        return device_view(capi.dflash_debug_view(self.ctx, "gen_count")[0], (self.max_batch,),
+                           torch.int32)
+
     def debug_view(self, name: str, layer: int = 0) -> torch.Tensor:
         """Zero-copy view of an internal buffer (see dflash_debug_view)."""
         ptr, nbytes = capi.dflash_debug_view(self.ctx, name, layer)
@@ -296,3 +301,21 @@ def device_operand(which: str, n_rows: int, width: int = 128, device: str = "cud
     idx = {"q": 0, "k": 1, "v": 2, "kb": 3, "vb": 4}[which]
     off = torch.from_numpy(wl.row_offsets(wl.ATTN_SEED, idx, n_rows)).to(device)
     return ext.unfold(0, width, 1)[off].contiguous()
+
+
+def capture_step_graph(eng: "DFlashEngine", seq_ids: torch.Tensor, tree: bool = False,
+                       topk: int = 8, budget: int = 64) -> torch.cuda.CUDAGraph:
+    """Captures one whole step (the C calls of draft, verify, accept and
+    injection) into a CUDA graph.  The step reads its anchors from the
+    library's next-anchor buffer, so successive replays continue decoding.
+    Every buffer and launch shape is fixed at capture; per-sequence lengths
+    live on the device, so the graph stays valid as the sequences grow."""
+    b = seq_ids.numel()
+    anchors = eng.next_anchor[:b]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        if tree:
+            eng.tree_step(seq_ids, anchors, topk, budget)
+        else:
+            eng.step(seq_ids, anchors)
+    return g

@@ -239,7 +239,9 @@ DFLASH_API int64_t dflash_launch_count(const dflash_ctx *ctx);
  *   "k_cache"/"v_cache"   target layer `layer`: [max_batch][n_kv_heads][max_ctx][head_dim]
  *   "dk_cache"/"dv_cache" draft layer `layer`: same layout
  *   "capture"             [max_rows][n_inject][d_model] (row = b*q + j of the last pass)
- * Element type = the storage dtype.  *bytes receives the view's size. */
+ *   "gen_count"           [max_batch] int32: tokens emitted per slot since its reset
+ *                         (prefill counts its first token; a step counts a + 1)
+ * Element type = the storage dtype unless stated.  *bytes receives the view's size. */
 DFLASH_API dflash_status dflash_debug_view(const dflash_ctx *ctx, const char *name, int32_t layer,
                                 const void **dev_ptr, int64_t *bytes);
 
