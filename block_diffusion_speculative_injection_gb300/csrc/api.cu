@@ -310,6 +310,8 @@ dflash_status dflash_create(const dflash_config* cfg, dflash_ctx** out) {
   ctx->cfg = *cfg;
   const dflash_config& c = ctx->cfg;
   ctx->esize = c.dtype == DFLASH_BF16 ? 2 : 4;
+  // programmatic dependent launch between kernels (DFLASH_NO_PDL=1 turns it off)
+  ctx->pdl = getenv("DFLASH_NO_PDL") == nullptr;
   if (cudaGetDevice(&ctx->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&ctx->sm_count, cudaDevAttrMultiProcessorCount, ctx->device) !=
           cudaSuccess) {

@@ -89,11 +89,6 @@ __device__ __forceinline__ void mma_bf16(float* c, const uint32_t* a, uint32_t b
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
 // (x0, x1) -> packed bf16 high parts and packed bf16 residuals x - hi
 __device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t& hi, uint32_t& lo) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
@@ -123,6 +118,8 @@ constexpr int kHd = 128;
 constexpr int kAttnSmem = 3 * 64 * 256 * 2 - 64 * 256;  // Q + 2 x (K, V) = 80 KB
 
 __global__ void __launch_bounds__(128) attn_mma_kernel(const AttnK p) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(128) uint8_t sm[];
   uint8_t* qs = sm;                   // 64 x 256 B
   uint8_t* ks0 = sm + 64 * 256;       // 2 stages x (K 16 KB, V 16 KB)
@@ -379,6 +376,8 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const AttnK p) {
 
 // merge split partials: one CTA (128 threads = head_dim) per (row, head)
 __global__ void attn_combine_kernel(const AttnK p) {
+  pdl_wait();
+  pdl_trigger();
   const int row = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
   const int b = row / p.q_stride, j = row % p.q_stride;
   int seq_, ctx_, blk_;
@@ -403,6 +402,8 @@ __global__ void attn_combine_kernel(const AttnK p) {
 // fp32 storage: one warp per (row, query head), keys visited in order
 // ---------------------------------------------------------------------------
 __global__ void attn_simt_f32_kernel(const AttnK p) {
+  pdl_wait();
+  pdl_trigger();
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (wid >= p.rows_total * p.H) return;
   const int row = wid / p.H, h = wid % p.H;
@@ -507,7 +508,7 @@ dflash_status attention(dflash_ctx* ctx, const AttnArgs& a, cudaStream_t st) {
 
   if (c.dtype == DFLASH_F32) {
     const int warps = p.rows_total * p.H;
-    attn_simt_f32_kernel<<<(warps + 3) / 4, 128, 0, st>>>(p);
+    DF_CUDA_TRY(ctx, launch_k(ctx->pdl, attn_simt_f32_kernel, dim3((warps + 3) / 4), dim3(128), 0, st, p));
     DF_LAUNCHED(ctx);
     return DFLASH_OK;
   }
@@ -524,11 +525,11 @@ dflash_status attention(dflash_ctx* ctx, const AttnArgs& a, cudaStream_t st) {
   p.n_splits = splits;
   DF_CUDA_TRY(ctx, ensure_attn_smem());
   dim3 grid(q_tiles, c.n_kv_heads, a.batch * splits);
-  attn_mma_kernel<<<grid, 128, kAttnSmem, st>>>(p);
+  DF_CUDA_TRY(ctx, launch_k(ctx->pdl, attn_mma_kernel, dim3(grid), dim3(128), kAttnSmem, st, p));
   DF_LAUNCHED(ctx);
   if (splits > 1) {
     dim3 g2(p.rows_total, c.n_heads);
-    attn_combine_kernel<<<g2, kHd, 0, st>>>(p);
+    DF_CUDA_TRY(ctx, launch_k(ctx->pdl, attn_combine_kernel, dim3(g2), dim3(kHd), 0, st, p));
     DF_LAUNCHED(ctx);
   }
   return DFLASH_OK;
@@ -591,12 +592,14 @@ dflash_status block_attention(int batch, int H, int Hkv, int hd, int ctx_len, in
   p.n_splits = splits;
   if (ensure_attn_smem() != cudaSuccess) return DFLASH_E_CUDA;
   dim3 grid(q_tiles, Hkv, batch * splits);
-  attn_mma_kernel<<<grid, 128, kAttnSmem, st>>>(p);
+  if (launch_k(true, attn_mma_kernel, dim3(grid), dim3(128), kAttnSmem, st, p) != cudaSuccess)
+    return DFLASH_E_CUDA;
   if (splits > 1) {
     dim3 g2(p.rows_total, H);
-    attn_combine_kernel<<<g2, kHd, 0, st>>>(p);
+    if (launch_k(true, attn_combine_kernel, dim3(g2), dim3(kHd), 0, st, p) != cudaSuccess)
+      return DFLASH_E_CUDA;
   }
-  return cudaGetLastError() == cudaSuccess ? DFLASH_OK : DFLASH_E_CUDA;
+  return DFLASH_OK;
 }
 
 }  // namespace dflash

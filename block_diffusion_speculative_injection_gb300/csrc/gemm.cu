@@ -82,8 +82,19 @@ __global__ void __launch_bounds__(128, 1)
     // TMA producer
     tma_prefetch_desc(&wmaps.m[seg]);
     tma_prefetch_desc(&xmap);
-    int issued = 0;
-    for (int i = 0; i < nkb; ++i) {
+    // Weights are never written by an earlier kernel: fill the first stages'
+    // weight tiles before waiting on the preceding kernel (programmatic
+    // dependent launch), then add the activation tiles.
+    const int pre = min(S, nkb);
+    for (int i = 0; i < pre; ++i) {
+      mbar_arrive_expect_tx(&full[i], a_bytes + b_bytes);
+      tma_load_2d(a_s + i * a_bytes, &wmaps.m[seg], (kb0 + i) * 64, wrow0, &full[i]);
+    }
+    pdl_wait();
+    for (int i = 0; i < pre; ++i)
+      tma_load_2d(b_s + i * b_bytes, &xmap, (kb0 + i) * 64, m0, &full[i]);
+    int issued = pre;
+    for (int i = pre; i < nkb; ++i) {
       const int s = i % S;
       const uint32_t ph = (uint32_t)(i / S) & 1u;
       if (!mbar_wait(&empty[s], ph ^ 1u, p.status)) break;
@@ -114,7 +125,10 @@ __global__ void __launch_bounds__(128, 1)
     tc_commit(accum);
   }
 
-  // epilogue: TMEM lane = weight row (output feature), column = token row
+  // epilogue: TMEM lane = weight row (output feature), column = token row.
+  // Every thread orders itself after the preceding kernel before writing.
+  pdl_wait();
+  pdl_trigger();
   mbar_wait(accum, 0, p.status);
   __syncwarp();
   tc_fence_after();
@@ -162,6 +176,8 @@ __global__ void __launch_bounds__(128, 1)
 
 // fp32 storage: the epilogue runs as its own kernel over the slab (splits = 1)
 __global__ void __launch_bounds__(128) epilogue_f32_kernel(const EpiArgs e) {
+  pdl_wait();
+  pdl_trigger();
   run_epilogue<float>(e, blockIdx.x * 128, 0, e.M);
 }
 
@@ -177,6 +193,8 @@ struct SegPtrs {
 __global__ void __launch_bounds__(256) gemm_f32_kernel(const float* __restrict__ x, int M, int K,
                                                        const SegPtrs segs, int N,
                                                        float* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float xs[16][64 + 1];
   __shared__ float wsm[16][64 + 1];
   const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
@@ -313,7 +331,7 @@ dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs&
       return DFLASH_E_CAPACITY;
     }
     dim3 grid((N + 63) / 64, (M + 63) / 64);
-    gemm_f32_kernel<<<grid, 256, 0, st>>>(static_cast<const float*>(x), M, K, sp, N, out);
+    DF_CUDA_TRY(ctx, launch_k(ctx->pdl, gemm_f32_kernel, dim3(grid), dim3(256), 0, st, static_cast<const float*>(x), M, K, sp, N, out));
     DF_LAUNCHED(ctx);
     *splits_used = 1;
     if (epi_in.kind != kEpiSlab) {
@@ -325,7 +343,7 @@ dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs&
       e.slab = out;
       e.status = ctx->dev_status;
       const int groups = e.kind == kEpiSwiGLU ? (e.F + 127) / 128 : (N + 127) / 128;
-      epilogue_f32_kernel<<<groups, 128, 0, st>>>(e);
+      DF_CUDA_TRY(ctx, launch_k(ctx->pdl, epilogue_f32_kernel, dim3(groups), dim3(128), 0, st, e));
       DF_LAUNCHED(ctx);
     }
     return DFLASH_OK;
@@ -348,8 +366,11 @@ dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs&
   const int n_tiles = (N + 127) / 128;
   const int n_kb = K / 64;
   const int ctas = n_tiles * m_tiles;
+  // K splits: as many as fit in ONE wave of resident CTAs (a partial second
+  // wave would double the latency of these short, bandwidth-bound launches)
   const int per_sm = (BN <= 32) ? 2 : 1;
-  int splits = (per_sm * ctx->sm_count + ctas - 1) / ctas;
+  const int slots = per_sm * ctx->sm_count;
+  int splits = ctas >= slots ? 1 : slots / ctas;
   if (splits > max_splits) splits = max_splits;
   if (splits > n_kb / 4) splits = n_kb / 4;
   if (splits < 1) splits = 1;
@@ -401,11 +422,12 @@ dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs&
   static bool attr_set = false;
   if (!attr_set) {
     DF_CUDA_TRY(ctx, cudaFuncSetAttribute(gemm_tc_kernel,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024));
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 210 * 1024));
     attr_set = true;
   }
   dim3 grid(n_tiles, m_tiles, splits);
-  gemm_tc_kernel<<<grid, 128, tc_smem_bytes(BN, stages), st>>>(maps, *xm, p);
+  const size_t smem_bytes = tc_smem_bytes(BN, stages);
+  DF_CUDA_TRY(ctx, launch_k(ctx->pdl, gemm_tc_kernel, dim3(grid), dim3(128), smem_bytes, st, maps, *xm, p));
   DF_LAUNCHED(ctx);
   *splits_used = splits;
   return DFLASH_OK;

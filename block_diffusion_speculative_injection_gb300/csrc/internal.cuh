@@ -8,6 +8,8 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <cstring>
+#include <utility>
 #include <map>
 #include <string>
 #include <tuple>
@@ -121,6 +123,7 @@ struct dflash_ctx {
   int32_t* tile_counters = nullptr;  // GEMM split-K completion tickets (self-resetting)
   size_t n_tile_counters = 0;
 
+  bool pdl = true;  // programmatic dependent launch between this context's kernels
   int64_t launches = 0;
   std::string last_error;
   // optional per-launch timing (dflash_profile): a pool of CUDA events
@@ -261,6 +264,34 @@ template <>
 __device__ __forceinline__ void st_f<float>(float* p, float v) { *p = v; }
 template <>
 __device__ __forceinline__ void st_f<bf16>(bf16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+// ---------------------------------------------------------------------------
+// programmatic dependent launch: a kernel may start while its predecessor
+// drains; it must call pdl_wait() before touching any memory an earlier
+// kernel writes or reads-then-rewrites.  Both are no-ops without the launch
+// attribute.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                            size_t smem, cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -25,6 +25,8 @@ struct PassSetupArgs {
 };
 
 __global__ void pass_setup_kernel(PassSetupArgs a) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int s_blk[1024];
   __shared__ int s_ctx[1024];
   for (int b = threadIdx.x; b < a.batch; b += blockDim.x) {
@@ -126,7 +128,7 @@ dflash_status launch_pass_setup_full(dflash_ctx* ctx, int batch, const int32_t* 
   a.max_batch = ctx->cfg.max_batch;
   a.max_ctx = ctx->cfg.max_ctx;
   a.status = ctx->dev_status;
-  pass_setup_kernel<<<1, 1024, 0, st>>>(a);
+  DF_CUDA_TRY(ctx, launch_k(ctx->pdl, pass_setup_kernel, dim3(1), dim3(1024), 0, st, a));
   DF_LAUNCHED(ctx);
   return DFLASH_OK;
 }
@@ -140,6 +142,8 @@ __global__ void embed_kernel(const int32_t* __restrict__ tokens, const T* __rest
                              const T* __restrict__ mask_emb, const int32_t* __restrict__ row_pos,
                              float* __restrict__ resid, int d, int vocab, int draft_block,
                              int block, int32_t* status) {
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.x;
   float* out = resid + (size_t)r * d;
   const T* src = nullptr;
@@ -164,15 +168,15 @@ dflash_status launch_embed(dflash_ctx* ctx, const int32_t* tokens, int rows, int
   ProfScope prof__(ctx, kProfRow, st);
   const int d = ctx->cfg.d_model;
   if (ctx->cfg.dtype == DFLASH_BF16)
-    embed_kernel<bf16><<<rows, 256, 0, st>>>(tokens, static_cast<const bf16*>(ctx->tok_emb),
+    DF_CUDA_TRY(ctx, launch_k(ctx->pdl, embed_kernel<bf16>, dim3(rows), dim3(256), 0, st, tokens, static_cast<const bf16*>(ctx->tok_emb),
                                              static_cast<const bf16*>(ctx->mask_emb), ctx->row_pos,
                                              ctx->resid, d, ctx->cfg.vocab, draft_block, block,
-                                             ctx->dev_status);
+                                             ctx->dev_status));
   else
-    embed_kernel<float><<<rows, 256, 0, st>>>(tokens, static_cast<const float*>(ctx->tok_emb),
+    DF_CUDA_TRY(ctx, launch_k(ctx->pdl, embed_kernel<float>, dim3(rows), dim3(256), 0, st, tokens, static_cast<const float*>(ctx->tok_emb),
                                               static_cast<const float*>(ctx->mask_emb),
                                               ctx->row_pos, ctx->resid, d, ctx->cfg.vocab,
-                                              draft_block, block, ctx->dev_status);
+                                              draft_block, block, ctx->dev_status));
   DF_LAUNCHED(ctx);
   return DFLASH_OK;
 }
@@ -200,6 +204,8 @@ template <typename T>
 __global__ void __launch_bounds__(kNormThreads)
     norm_kernel(const float* __restrict__ resid, const int32_t* __restrict__ rows_in, int d,
                 const T* __restrict__ gain, T* __restrict__ out, float eps) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[32];
   const int i_out = blockIdx.x;
   const int r = rows_in ? rows_in[i_out] : i_out;
@@ -231,11 +237,11 @@ dflash_status launch_norm(dflash_ctx* ctx, int n_out, const int32_t* rows_in, co
   const int d = ctx->cfg.d_model;
   const float eps = ctx->cfg.rms_eps;
   if (ctx->cfg.dtype == DFLASH_BF16)
-    norm_kernel<bf16><<<n_out, kNormThreads, 0, st>>>(
-        ctx->resid, rows_in, d, static_cast<const bf16*>(gain), static_cast<bf16*>(out), eps);
+    DF_CUDA_TRY(ctx, launch_k(ctx->pdl, norm_kernel<bf16>, dim3(n_out), dim3(kNormThreads), 0, st, 
+        ctx->resid, rows_in, d, static_cast<const bf16*>(gain), static_cast<bf16*>(out), eps));
   else
-    norm_kernel<float><<<n_out, kNormThreads, 0, st>>>(
-        ctx->resid, rows_in, d, static_cast<const float*>(gain), static_cast<float*>(out), eps);
+    DF_CUDA_TRY(ctx, launch_k(ctx->pdl, norm_kernel<float>, dim3(n_out), dim3(kNormThreads), 0, st, 
+        ctx->resid, rows_in, d, static_cast<const float*>(gain), static_cast<float*>(out), eps));
   DF_LAUNCHED(ctx);
   return DFLASH_OK;
 }

@@ -30,6 +30,8 @@ __global__ void accept_linear_kernel(int batch, int q, int mode, const int32_t* 
                                      int32_t* __restrict__ next_anchor,
                                      int32_t* __restrict__ emitted, int32_t* __restrict__ inj_seq,
                                      int32_t* __restrict__ inj_pos) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= batch) return;
   const int seq = pass_seq[b], ctx = pass_ctx[b], n = pass_blk[b];
@@ -73,9 +75,9 @@ dflash_status launch_accept_linear(dflash_ctx* ctx, int batch, const int32_t* se
                                    cudaStream_t st) {
   ProfScope prof__(ctx, kProfSpec, st);
   (void)seq_ids;
-  accept_linear_kernel<<<(batch + 127) / 128, 128, 0, st>>>(
+  DF_CUDA_TRY(ctx, launch_k(ctx->pdl, accept_linear_kernel, dim3((batch + 127) / 128), dim3(128), 0, st, 
       batch, q, mode, block, argmax, ctx->pass_seq, ctx->pass_ctx, ctx->pass_blk, ctx->seq_len,
-      ctx->gen_count, accept_len, next_anchor, emitted, ctx->inj_seq, ctx->inj_pos);
+      ctx->gen_count, accept_len, next_anchor, emitted, ctx->inj_seq, ctx->inj_pos));
   DF_LAUNCHED(ctx);
   return DFLASH_OK;
 }
@@ -103,6 +105,8 @@ __global__ void tree_build_kernel(int depth_max, int topk, int budget,
                                   const int32_t* __restrict__ anchor,
                                   const int32_t* __restrict__ ids, const float* __restrict__ logp,
                                   dtree_buffers t) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ HeapEnt heap[kMaxTreeNodes + 2];
   __shared__ float node_score[kMaxTreeNodes];
   __shared__ int n_nodes_s;
@@ -206,7 +210,7 @@ dflash_status launch_tree_build(dflash_ctx* ctx, int batch, const int32_t* ancho
                                 const int32_t* ids, const float* logp, int topk, int depth,
                                 int budget, const dtree_buffers* t, cudaStream_t st) {
   ProfScope prof__(ctx, kProfSpec, st);
-  tree_build_kernel<<<batch, 32, 0, st>>>(depth, topk, budget, anchor, ids, logp, *t);
+  DF_CUDA_TRY(ctx, launch_k(ctx->pdl, tree_build_kernel, dim3(batch), dim3(32), 0, st, depth, topk, budget, anchor, ids, logp, *t));
   DF_LAUNCHED(ctx);
   return DFLASH_OK;
 }
@@ -225,6 +229,8 @@ __global__ void tree_accept_kernel(int batch, dtree_buffers t, const int32_t* __
                                    int32_t* __restrict__ next_anchor, int32_t* __restrict__ emitted,
                                    int32_t* __restrict__ inj_seq, int32_t* __restrict__ inj_pos,
                                    int32_t* __restrict__ path, int32_t* status) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= batch) return;
   const int q = t.max_nodes;
@@ -286,6 +292,8 @@ __global__ void tree_compact_kernel(const int32_t* __restrict__ path,
                                     const int32_t* __restrict__ pass_seq,
                                     const int32_t* __restrict__ pass_blk, T* kc, T* vc,
                                     size_t layer_elems, int batch, int Hkv, int hd, int max_ctx) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ uint8_t buf[];
   const int l = blockIdx.x / batch, b = blockIdx.x % batch, kh = blockIdx.y;
   if (pass_blk[b] <= 0) return;
@@ -318,23 +326,23 @@ dflash_status launch_tree_accept(dflash_ctx* ctx, int batch, const int32_t* seq_
   ProfScope prof__(ctx, kProfSpec, st);
   (void)seq_ids;
   const dflash_config& c = ctx->cfg;
-  tree_accept_kernel<<<(batch + 127) / 128, 128, 0, st>>>(
+  DF_CUDA_TRY(ctx, launch_k(ctx->pdl, tree_accept_kernel, dim3((batch + 127) / 128), dim3(128), 0, st, 
       batch, *t, argmax, ctx->pass_seq, ctx->pass_ctx, ctx->pass_blk, ctx->seq_len, ctx->gen_count,
       accept_len,
-      next_anchor, emitted, ctx->inj_seq, ctx->inj_pos, ctx->path, ctx->dev_status);
+      next_anchor, emitted, ctx->inj_seq, ctx->inj_pos, ctx->path, ctx->dev_status));
   DF_LAUNCHED(ctx);
   dim3 grid(c.n_target_layers * batch, c.n_kv_heads);
   const size_t smem = 2 * 16 * (size_t)c.head_dim * ctx->esize;
   if (c.dtype == DFLASH_BF16)
-    tree_compact_kernel<bf16><<<grid, 128, smem, st>>>(
+    DF_CUDA_TRY(ctx, launch_k(ctx->pdl, tree_compact_kernel<bf16>, dim3(grid), dim3(128), smem, st, 
         ctx->path, ctx->pass_seq, ctx->pass_blk, static_cast<bf16*>(ctx->kc),
         static_cast<bf16*>(ctx->vc), ctx->layer_cache_elems, batch, c.n_kv_heads, c.head_dim,
-        c.max_ctx);
+        c.max_ctx));
   else
-    tree_compact_kernel<float><<<grid, 128, smem, st>>>(
+    DF_CUDA_TRY(ctx, launch_k(ctx->pdl, tree_compact_kernel<float>, dim3(grid), dim3(128), smem, st, 
         ctx->path, ctx->pass_seq, ctx->pass_blk, static_cast<float*>(ctx->kc),
         static_cast<float*>(ctx->vc), ctx->layer_cache_elems, batch, c.n_kv_heads, c.head_dim,
-        c.max_ctx);
+        c.max_ctx));
   DF_LAUNCHED(ctx);
   return DFLASH_OK;
 }

@@ -62,6 +62,8 @@ __global__ void __launch_bounds__(kVocabThreads)
                        const int32_t* __restrict__ vec_idx, float* __restrict__ logits_copy,
                        int32_t* __restrict__ part_id, float* __restrict__ part_v,
                        float* __restrict__ part_lse, int n_chunks) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ Cand red[32];
   __shared__ Cand best[kMaxK];
   __shared__ float mred[32];
@@ -126,6 +128,8 @@ __global__ void __launch_bounds__(kVocabThreads)
                        const int32_t* __restrict__ arg_idx, const int32_t* __restrict__ vec_idx,
                        int32_t* __restrict__ argmax, float* __restrict__ margin,
                        int32_t* __restrict__ topk_ids, float* __restrict__ topk_logp) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ Cand red[32];
   __shared__ Cand best[kMaxK];
   __shared__ float lse_s;
@@ -197,12 +201,12 @@ dflash_status launch_vocab_reduce(dflash_ctx* ctx, int rows, int vocab, const in
   float* part_v = ctx->vv_part;
   float* part_lse = ctx->vv_part + ctx->vpart_cap;
   dim3 g1(rows, n_chunks);
-  vocab_pass1_kernel<<<g1, kVocabThreads, 0, st>>>(ctx->ws, vocab, K, vec_idx, logits_copy,
-                                                   ctx->vk_part, part_v, part_lse, n_chunks);
+  DF_CUDA_TRY(ctx, launch_k(ctx->pdl, vocab_pass1_kernel, dim3(g1), dim3(kVocabThreads), 0, st, ctx->ws, vocab, K, vec_idx, logits_copy,
+                                                   ctx->vk_part, part_v, part_lse, n_chunks));
   DF_LAUNCHED(ctx);
-  vocab_pass2_kernel<<<rows, kVocabThreads, 0, st>>>(K, topk, n_chunks, ctx->vk_part, part_v,
+  DF_CUDA_TRY(ctx, launch_k(ctx->pdl, vocab_pass2_kernel, dim3(rows), dim3(kVocabThreads), 0, st, K, topk, n_chunks, ctx->vk_part, part_v,
                                                      part_lse, arg_idx, vec_idx, argmax, margin,
-                                                     topk_ids, topk_logp);
+                                                     topk_ids, topk_logp));
   DF_LAUNCHED(ctx);
   return DFLASH_OK;
 }
