@@ -72,6 +72,7 @@ _SIGS = {
     "dflash_block_attention": ([_I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, ctypes.c_int64, _P], _I),
     "dflash_block_attention_workspace": ([_I, _I, _I, _I, _I], ctypes.c_int64),
     "dflash_profile": ([_P, _I], _I),
+    "dflash_debug_trace": ([_P, _P, ctypes.c_int64], _I),
     "dflash_profile_read": ([_P, _I, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double),
                              ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)], _I),
 }
@@ -238,3 +239,34 @@ def dflash_profile_read(ctx, kind: int):
     _check(ctx, load().dflash_profile_read(ctx, kind, ctypes.byref(n), ctypes.byref(ms),
                                            ctypes.byref(b), ctypes.byref(f)))
     return n.value, ms.value, b.value, f.value
+
+
+def dflash_profile(ctx, enable: bool) -> None:
+    _check(ctx, load().dflash_profile(ctx, 1 if enable else 0))
+
+
+PROF_GEMM, PROF_ATTN, PROF_ROW, PROF_VOCAB, PROF_SPEC, PROF_ALL = 0, 1, 2, 3, 4, -1
+
+
+def dflash_profile_read(ctx, kind: int):
+    """(launches, ms, algorithmic bytes, flops) of one kernel class."""
+    n = ctypes.c_int64()
+    ms, b, f = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
+    _check(ctx, load().dflash_profile_read(ctx, kind, ctypes.byref(n), ctypes.byref(ms),
+                                           ctypes.byref(b), ctypes.byref(f)))
+    return n.value, ms.value, b.value, f.value
+
+
+def dflash_block_attention_noalloc(batch, n_heads, n_kv_heads, ctx_len, block, causal, q, k, v, out,
+                                   stream=None) -> None:
+    """Block attention with the library's fixed scratch array (no allocation)."""
+    st = load().dflash_block_attention_noalloc(batch, n_heads, n_kv_heads, ctx_len, block, causal,
+                                               _ptr(q), _ptr(k), _ptr(v), _ptr(out), _stream(stream))
+    if st != 0:
+        raise DFlashError(st, "dflash_block_attention_noalloc")
+
+
+def dflash_debug_trace(ctx, dst=None) -> None:
+    """Registers (or clears with None) a [L][max_rows][d] fp32 residual trace."""
+    nbytes = dst.numel() * dst.element_size() if dst is not None else 0
+    _check(ctx, load().dflash_debug_trace(ctx, _ptr(dst), nbytes))

@@ -195,7 +195,7 @@ static EpiArgs epi_base(dflash_ctx* ctx, int kind) {
 
 static dflash_status run_layer(dflash_ctx* ctx, const LayerW& w, int rows, void* kc, void* vc,
                                const AttnArgs& attn_base, const void* next_gain, void* capture,
-                               int cap_slot, cudaStream_t st) {
+                               int cap_slot, float* trace, cudaStream_t st) {
   const dflash_config& c = ctx->cfg;
   const int d = c.d_model, qd = c.n_heads * c.head_dim, kvd = c.n_kv_heads * c.head_dim;
   int sp = 1;
@@ -220,6 +220,7 @@ static dflash_status run_layer(dflash_ctx* ctx, const LayerW& w, int rows, void*
   EpiArgs ed = epi_base(ctx, kEpiResid);
   ed.capture = capture;
   ed.cap_slot = cap_slot;
+  ed.trace = trace;
   GemmSegs dn{{w.w_down}, {d}, 1};
   DF_TRY(gemm(ctx, ctx->act, rows, c.ffn_dim, dn, ed, 16, &sp, st));
   if (next_gain) DF_TRY(launch_norm(ctx, rows, nullptr, next_gain, ctx->xn, st));
@@ -277,7 +278,8 @@ static dflash_status target_pass(dflash_ctx* ctx, int batch, int q, int mask,
       cap = ctx->capture;
       slot = inj++;
     }
-    DF_TRY(run_layer(ctx, ctx->tl[l], rows, kc, vc, ab, next_gain, cap, slot, st));
+    float* tr = ctx->trace ? ctx->trace + (size_t)l * c.max_rows * c.d_model : nullptr;
+    DF_TRY(run_layer(ctx, ctx->tl[l], rows, kc, vc, ab, next_gain, cap, slot, tr, st));
   }
   const int n_lm = last_only ? batch : rows;
   DF_TRY(launch_norm(ctx, n_lm, ctx->lm_rows, ctx->final_norm, ctx->lm_in, st));
@@ -555,7 +557,7 @@ dflash_status dflash_draft_block(dflash_ctx* ctx, int32_t batch, const int32_t* 
     void* kc = static_cast<uint8_t*>(ctx->dkc) + off;
     void* vc = static_cast<uint8_t*>(ctx->dvc) + off;
     const void* next_gain = l + 1 < c.n_draft_layers ? ctx->dl[l + 1].attn_norm : nullptr;
-    s = run_layer(ctx, ctx->dl[l], rows, kc, vc, ab, next_gain, nullptr, 0, st);
+    s = run_layer(ctx, ctx->dl[l], rows, kc, vc, ab, next_gain, nullptr, 0, nullptr, st);
   }
   ctx->pass_seq = save[0];
   ctx->pass_ctx = save[1];
@@ -733,6 +735,15 @@ dflash_status dflash_block_attention(int32_t batch, int32_t n_heads, int32_t n_k
 int64_t dflash_block_attention_workspace(int32_t batch, int32_t n_heads, int32_t n_kv_heads,
                                          int32_t ctx_len, int32_t block) {
   return block_attention_workspace(batch, n_heads, n_kv_heads, 128, ctx_len, block);
+}
+
+dflash_status dflash_debug_trace(dflash_ctx* ctx, float* dst_dev, int64_t bytes) {
+  if (!ctx) return DFLASH_E_INVALID_ARG;
+  const dflash_config& c = ctx->cfg;
+  if (dst_dev && bytes < (int64_t)c.n_target_layers * c.max_rows * c.d_model * (int64_t)sizeof(float))
+    return fail(ctx, DFLASH_E_CAPACITY, "trace buffer needs n_target_layers*max_rows*d_model floats");
+  ctx->trace = dst_dev;
+  return DFLASH_OK;
 }
 
 dflash_status dflash_profile(dflash_ctx* ctx, int32_t enable) {

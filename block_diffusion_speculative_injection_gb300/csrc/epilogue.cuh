@@ -43,6 +43,7 @@ struct EpiArgs {
   float* resid;
   void* capture;
   int cap_slot, n_inject;
+  float* trace;  // optional fp32 copy of the updated residual rows
   // STORE
   void* out;
   int32_t* status;
@@ -162,6 +163,7 @@ __device__ void run_epilogue(const EpiArgs& e, int n0, int m0, int BN) {
           const float r = e.resid[(size_t)t * e.N + n] + slab_sum<T>(e, t, n);
           e.resid[(size_t)t * e.N + n] = r;
           if (cap) st_f(cap + ((size_t)t * e.n_inject + e.cap_slot) * e.N + n, r);
+          if (e.trace) e.trace[(size_t)t * e.N + n] = r;
         }
       break;
     }

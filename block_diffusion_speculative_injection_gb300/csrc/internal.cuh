@@ -123,6 +123,7 @@ struct dflash_ctx {
   int32_t* tile_counters = nullptr;  // GEMM split-K completion tickets (self-resetting)
   size_t n_tile_counters = 0;
 
+  float* trace = nullptr;  // debug: residual after every target layer [L][max_rows][d]
   bool pdl = true;  // programmatic dependent launch between this context's kernels
   int64_t launches = 0;
   std::string last_error;

@@ -245,6 +245,13 @@ DFLASH_API int64_t dflash_launch_count(const dflash_ctx *ctx);
 DFLASH_API dflash_status dflash_debug_view(const dflash_ctx *ctx, const char *name, int32_t layer,
                                 const void **dev_ptr, int64_t *bytes);
 
+/* Debug: while dst_dev is set (non-NULL), every target pass also writes the
+ * residual stream after each target layer, fp32, to
+ * dst_dev[layer][row][d_model] (row = b*q + j of the pass; rows past a
+ * sequence's block are left as they were).  bytes must cover
+ * n_target_layers * max_rows * d_model floats.  NULL switches it off. */
+DFLASH_API dflash_status dflash_debug_trace(dflash_ctx *ctx, float *dst_dev, int64_t bytes);
+
 DFLASH_API void dflash_destroy(dflash_ctx *ctx);
 
 /* ---- op-level block attention (no context) --------------------------------
