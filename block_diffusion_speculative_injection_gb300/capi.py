@@ -71,6 +71,7 @@ _SIGS = {
     "dflash_destroy": ([_P], None),
     "dflash_block_attention": ([_I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, ctypes.c_int64, _P], _I),
     "dflash_block_attention_workspace": ([_I, _I, _I, _I, _I], ctypes.c_int64),
+    "dflash_block_attention_noalloc": ([_I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P], _I),
     "dflash_profile": ([_P, _I], _I),
     "dflash_debug_trace": ([_P, _P, ctypes.c_int64], _I),
     "dflash_profile_read": ([_P, _I, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double),
@@ -223,22 +224,6 @@ def dflash_block_attention(batch, n_heads, n_kv_heads, ctx_len, block, causal, q
 
 def dflash_block_attention_workspace(batch, n_heads, n_kv_heads, ctx_len, block) -> int:
     return int(load().dflash_block_attention_workspace(batch, n_heads, n_kv_heads, ctx_len, block))
-
-
-def dflash_profile(ctx, enable: bool) -> None:
-    _check(ctx, load().dflash_profile(ctx, 1 if enable else 0))
-
-
-PROF_GEMM, PROF_ATTN, PROF_ROW, PROF_VOCAB, PROF_SPEC, PROF_ALL = 0, 1, 2, 3, 4, -1
-
-
-def dflash_profile_read(ctx, kind: int):
-    """(launches, ms, algorithmic bytes, flops) of one kernel class."""
-    n = ctypes.c_int64()
-    ms, b, f = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
-    _check(ctx, load().dflash_profile_read(ctx, kind, ctypes.byref(n), ctypes.byref(ms),
-                                           ctypes.byref(b), ctypes.byref(f)))
-    return n.value, ms.value, b.value, f.value
 
 
 def dflash_profile(ctx, enable: bool) -> None:

@@ -284,6 +284,30 @@ DFLASH_API int64_t dflash_block_attention_workspace(int32_t batch, int32_t n_hea
                                                     int32_t n_kv_heads, int32_t ctx_len,
                                                     int32_t block);
 
+/* The same block attention for callers that cannot allocate device memory
+ * where they run it: an engine's per-request path that may only use buffers
+ * from the engine's own pool, a serving loop that bans cudaMalloc after
+ * start-up (it can synchronize the device and fragment memory), or a plugin
+ * execute call that is handed no allocator.  The pages have no counterpart;
+ * this is a library convenience.
+ * Arguments and result are those of dflash_block_attention; the split-KV
+ * partials go to a fixed 16 MiB array in device global memory that belongs to
+ * the library image (every GPU that loads the library holds it until the
+ * process exits), so nothing is allocated by this call.
+ * Sizes whose partials exceed 16 MiB (dflash_block_attention_workspace(...)
+ * > 16 MiB) are rejected with DFLASH_E_CAPACITY and a message on stderr.
+ * The first call on a device looks up the array's device address for that
+ * device; make that first call before any stream capture.  All calls share
+ * the one array and it keeps the last call's contents (nothing in it needs
+ * to start at zero), so calls that overlap on the GPU -- on two streams at
+ * once -- race and must be serialized by the caller. */
+DFLASH_API dflash_status dflash_block_attention_noalloc(int32_t batch, int32_t n_heads,
+                                                        int32_t n_kv_heads, int32_t ctx_len,
+                                                        int32_t block, int32_t causal,
+                                                        const void *q_dev, const void *k_dev,
+                                                        const void *v_dev, void *out_dev,
+                                                        dflash_stream_t stream);
+
 /* ---- per-kernel timing ------------------------------------------------------
  * enable != 0 starts recording a CUDA event pair around every kernel launch of
  * this context (clearing earlier records); 0 stops recording. */
