@@ -58,18 +58,6 @@ __device__ __forceinline__ void seq_meta(const AttnK& p, int b, int& seq, int& c
 // ---------------------------------------------------------------------------
 // small PTX wrappers (legacy warp-level MMA path)
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-               "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                         uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -374,28 +362,42 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const AttnK p) {
   }
 }
 
-// merge split partials: one CTA (128 threads = head_dim) per (row, head)
+constexpr int kMaxSplits = 256;
+
+// merge split partials: one CTA (128 threads = head_dim) per (row, head); all
+// partial loads are issued independently
 __global__ void attn_combine_kernel(const AttnK p) {
   pdl_wait();
   pdl_trigger();
+  __shared__ float sw[kMaxSplits];
+  __shared__ float s_inv;
   const int row = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
   const int b = row / p.q_stride, j = row % p.q_stride;
   int seq_, ctx_, blk_;
   seq_meta(p, b, seq_, ctx_, blk_);
   if (j >= blk_) return;
-  float mmax = -INFINITY;
-  for (int s = 0; s < p.n_splits; ++s)
-    mmax = fmaxf(mmax, p.part_ml[(((size_t)s * p.rows_total + row) * p.H + h) * 2]);
-  if (mmax == -INFINITY) mmax = 0.f;
-  float acc = 0.f, l = 0.f;
-  for (int s = 0; s < p.n_splits; ++s) {
-    const size_t base = ((size_t)s * p.rows_total + row) * p.H + h;
-    const float w = exp2f(p.part_ml[base * 2] - mmax);
-    l += w * p.part_ml[base * 2 + 1];
-    acc += w * p.part_o[base * kHd + d];
+  const int S = p.n_splits;
+  const size_t stride = (size_t)p.rows_total * p.H;  // (row, head) units between splits
+  const size_t base = (size_t)row * p.H + h;
+  for (int s = d; s < S; s += blockDim.x) sw[s] = p.part_ml[(base + s * stride) * 2];
+  __syncthreads();
+  if (d == 0) {
+    float m = -INFINITY;
+    for (int s = 0; s < S; ++s) m = fmaxf(m, sw[s]);
+    if (m == -INFINITY) m = 0.f;
+    float l = 0.f;
+    for (int s = 0; s < S; ++s) {
+      const float w = exp2f(sw[s] - m);
+      sw[s] = w;
+      l += w * p.part_ml[(base + s * stride) * 2 + 1];
+    }
+    s_inv = l > 0.f ? 1.f / l : 0.f;
   }
-  static_cast<bf16*>(p.out)[((size_t)row * p.H + h) * kHd + d] =
-      __float2bfloat16_rn(l > 0.f ? acc / l : 0.f);
+  __syncthreads();
+  float acc = 0.f;
+#pragma unroll 8
+  for (int s = 0; s < S; ++s) acc += sw[s] * p.part_o[(base + s * stride) * kHd + d];
+  static_cast<bf16*>(p.out)[base * kHd + d] = __float2bfloat16_rn(acc * s_inv);
 }
 
 // ---------------------------------------------------------------------------
@@ -446,7 +448,9 @@ static void plan_splits(int sm_count, int ctas, int64_t max_keys, size_t part_ca
                         int* n_splits, int* keys_per_split) {
   const int64_t key_tiles = (max_keys + kTileKeys - 1) / kTileKeys;
   int splits = (2 * sm_count + ctas - 1) / ctas;
-  if (splits > key_tiles) splits = (int)key_tiles;
+  // at least 4 key tiles (256 keys) per split, at most kMaxSplits splits
+  if (splits > (key_tiles + 3) / 4) splits = (int)((key_tiles + 3) / 4);
+  if (splits > kMaxSplits) splits = kMaxSplits;
   if (splits < 1) splits = 1;
   while (splits > 1 && (size_t)splits * rows_heads > part_cap) --splits;
   *keys_per_split = 1 << 30;

@@ -78,7 +78,8 @@ __global__ void __launch_bounds__(128, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0 && lane == 0) {
+  if (warp == 0) {
+   if (lane == 0) {
     // TMA producer
     tma_prefetch_desc(&wmaps.m[seg]);
     tma_prefetch_desc(&xmap);
@@ -107,7 +108,10 @@ __global__ void __launch_bounds__(128, 1)
     // drain: every issued copy has landed before this thread leaves
     for (int i = max(0, issued - S); i < issued; ++i)
       mbar_wait(&full[i % S], (uint32_t)(i / S) & 1u, p.status);
-  } else if (warp == 1 && lane == 0) {
+   }
+    __syncwarp();  // lanes 1..31 park here instead of spinning beside the producer
+  } else if (warp == 1) {
+   if (lane == 0) {
     // MMA issuer
     const uint32_t idesc = idesc_bf16_f32(128, BN);
     for (int i = 0; i < nkb; ++i) {
@@ -123,13 +127,15 @@ __global__ void __launch_bounds__(128, 1)
       tc_commit(&empty[s]);
     }
     tc_commit(accum);
+   }
+    __syncwarp();
   }
 
   // epilogue: TMEM lane = weight row (output feature), column = token row.
   // Every thread orders itself after the preceding kernel before writing.
   pdl_wait();
   pdl_trigger();
-  mbar_wait(accum, 0, p.status);
+  mbar_wait_sleep(accum, 0, p.status);
   __syncwarp();
   tc_fence_after();
   const int feat = n0 + warp * 32 + lane;
@@ -171,7 +177,8 @@ __global__ void __launch_bounds__(128, 1)
   if (!s_last) return;
   __threadfence();
   if (p.epi.kind == kEpiSwiGLU) n0_epi = (blockIdx.x % ((p.epi.F + 127) / 128)) * 128;
-  run_epilogue<bf16>(p.epi, n0_epi, m0, BN);
+  run_epilogue_staged<bf16>(p.epi, n0_epi, m0, BN, reinterpret_cast<float*>(smem),
+                            (int)(S * (a_bytes + b_bytes) / 4));
 }
 
 // fp32 storage: the epilogue runs as its own kernel over the slab (splits = 1)

@@ -230,18 +230,77 @@ __global__ void __launch_bounds__(kNormThreads)
   }
 }
 
+// Vectorised variant for d_model % 1024 == 0: VPT float4 groups per thread,
+// all loads issued before the reduction.
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 ld4(const bf16* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&u.x);
+  const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&u.y);
+  return make_float4(__low2float(a), __high2float(a), __low2float(b), __high2float(b));
+}
+__device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ void st4(bf16* p, float4 v) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
+template <typename T, int VPT>
+__global__ void __launch_bounds__(kNormThreads)
+    norm_vec_kernel(const float* __restrict__ resid, const int32_t* __restrict__ rows_in, int d,
+                    const T* __restrict__ gain, T* __restrict__ out, float eps) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float red[32];
+  const int i_out = blockIdx.x;
+  const int r = rows_in ? rows_in[i_out] : i_out;
+  float4 x[VPT], g[VPT];
+  float ss = 0.f;
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    const int i = (threadIdx.x + v * kNormThreads) * 4;
+    x[v] = r >= 0 ? ld4(resid + (size_t)r * d + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    g[v] = ld4(gain + i);
+  }
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) ss += x[v].x * x[v].x + x[v].y * x[v].y + x[v].z * x[v].z + x[v].w * x[v].w;
+  const float inv = rsqrtf(block_sum(ss, red) / (float)d + eps);
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    const int i = (threadIdx.x + v * kNormThreads) * 4;
+    st4(out + (size_t)i_out * d + i, make_float4(x[v].x * inv * g[v].x, x[v].y * inv * g[v].y,
+                                                 x[v].z * inv * g[v].z, x[v].w * inv * g[v].w));
+  }
+}
+
+template <typename T>
+static cudaError_t launch_norm_t(dflash_ctx* ctx, int n_out, const int32_t* rows_in,
+                                 const void* gain, void* out, cudaStream_t st) {
+  const int d = ctx->cfg.d_model;
+  const float eps = ctx->cfg.rms_eps;
+  const T* g = static_cast<const T*>(gain);
+  T* o = static_cast<T*>(out);
+  const int vpt = d % 1024 == 0 ? d / 1024 : 0;
+  switch (vpt) {
+    case 1: return launch_k(ctx->pdl, norm_vec_kernel<T, 1>, dim3(n_out), dim3(kNormThreads), 0, st, ctx->resid, rows_in, d, g, o, eps);
+    case 2: return launch_k(ctx->pdl, norm_vec_kernel<T, 2>, dim3(n_out), dim3(kNormThreads), 0, st, ctx->resid, rows_in, d, g, o, eps);
+    case 4: return launch_k(ctx->pdl, norm_vec_kernel<T, 4>, dim3(n_out), dim3(kNormThreads), 0, st, ctx->resid, rows_in, d, g, o, eps);
+    case 8: return launch_k(ctx->pdl, norm_vec_kernel<T, 8>, dim3(n_out), dim3(kNormThreads), 0, st, ctx->resid, rows_in, d, g, o, eps);
+    default: return launch_k(ctx->pdl, norm_kernel<T>, dim3(n_out), dim3(kNormThreads), 0, st, ctx->resid, rows_in, d, g, o, eps);
+  }
+}
+
 dflash_status launch_norm(dflash_ctx* ctx, int n_out, const int32_t* rows_in, const void* gain,
                           void* out, cudaStream_t st) {
   ProfScope prof__(ctx, kProfRow, st);
   if (n_out <= 0) return DFLASH_OK;
-  const int d = ctx->cfg.d_model;
-  const float eps = ctx->cfg.rms_eps;
   if (ctx->cfg.dtype == DFLASH_BF16)
-    DF_CUDA_TRY(ctx, launch_k(ctx->pdl, norm_kernel<bf16>, dim3(n_out), dim3(kNormThreads), 0, st, 
-        ctx->resid, rows_in, d, static_cast<const bf16*>(gain), static_cast<bf16*>(out), eps));
+    DF_CUDA_TRY(ctx, (launch_norm_t<bf16>(ctx, n_out, rows_in, gain, out, st)));
   else
-    DF_CUDA_TRY(ctx, launch_k(ctx->pdl, norm_kernel<float>, dim3(n_out), dim3(kNormThreads), 0, st, 
-        ctx->resid, rows_in, d, static_cast<const float*>(gain), static_cast<float*>(out), eps));
+    DF_CUDA_TRY(ctx, (launch_norm_t<float>(ctx, n_out, rows_in, gain, out, st)));
   DF_LAUNCHED(ctx);
   return DFLASH_OK;
 }
