@@ -179,132 +179,111 @@ __device__ void run_epilogue(const EpiArgs& e, int n0, int m0, int BN) {
 }
 
 // ---------------------------------------------------------------------------
-// Staged variant for the tensor-core GEMM (bf16, head_dim 128, N % 128 == 0):
-// the tile's K-split slabs -- and, for the residual add, the residual tile --
-// are copied into shared memory in one burst of cp.async (all loads in
-// flight at once), then reduced and transformed from shared memory.  Rows
-// are processed in chunks that fit `sbuf`.  Every thread of the CTA calls it.
+// Cluster variant for the tensor-core GEMM (bf16, head_dim 128, N % 128 == 0).
+// The thread-block cluster holds the K splits of one 128-feature output tile
+// (SwiGLU: of a gate tile and the matching up tile, interleaved by rank:
+// rank = h + 2*split with h = 0 gate, 1 up).  Each CTA has its fp32 partial
+// tile in its own shared memory as part[token][feature]; after a cluster
+// barrier, CTA `rank` takes every csize-th work item of the tile, sums the
+// partials of all splits through distributed shared memory in split order,
+// and applies the epilogue operation.  meta[u] = (position, sequence, slot)
+// of tile row u (QKV / INJECT).
 // ---------------------------------------------------------------------------
 template <typename T>
-__device__ void run_epilogue_staged(const EpiArgs& e, int n0, int m0, int BN, float* sbuf,
-                                    int sbuf_floats) {
-  const int m1 = min(e.M, m0 + BN);
-  const bool two = e.kind == kEpiSwiGLU;
-  const bool with_resid = e.kind == kEpiResid;
+__device__ void run_epilogue_cluster(const EpiArgs& e, int n0, int m0, int BN, const float* part,
+                                     const int32_t* meta) {
   const int S = e.splits;
-  const int parts = S * (two ? 2 : 1) + (with_resid ? 1 : 0);
-  int chunk = sbuf_floats / (parts * 128);
-  if (chunk < 1) chunk = 1;
-  const int tid = threadIdx.x, nth = blockDim.x;
-  for (int c0 = m0; c0 < m1; c0 += chunk) {
-    const int cn = min(chunk, m1 - c0);
-    for (int i = tid; i < cn * parts * 32; i += nth) {
-      const int q = i & 31, part = (i >> 5) % parts, u = (i >> 5) / parts;
-      const int t = c0 + u;
-      const float* src;
-      if (with_resid && part == parts - 1) {
-        src = e.resid + (size_t)t * e.N + n0;
+  const bool two = e.kind == kEpiSwiGLU;
+  const int csize = two ? 2 * S : S;
+  const int rank = (int)cluster_ctarank();
+  const int cn = min(BN, e.M - m0);
+  const uint32_t local = smem_u32(part);
+  uint32_t peer[16];
+#pragma unroll
+  for (int r = 0; r < 16; ++r)
+    if (r < csize) peer[r] = map_peer(local, (uint32_t)r);
+  auto val = [&](int u, int c, int h) {
+    const uint32_t off = (uint32_t)((u * 128 + c) * 4);
+    float v = 0.f;
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+      if (s < S) v += ld_peer_f32(peer[two ? h + 2 * s : s] + off);
+    return v;
+  };
+  const int first = rank * (int)blockDim.x + (int)threadIdx.x;
+  const int step = csize * (int)blockDim.x;
+  switch (e.kind) {
+    case kEpiResid: {
+      T* cap = static_cast<T*>(e.capture);
+      for (int i = first; i < cn * 128; i += step) {
+        const int u = i >> 7, c = i & 127, t = m0 + u, n = n0 + c;
+        const float r = e.resid[(size_t)t * e.N + n] + val(u, c, 0);
+        e.resid[(size_t)t * e.N + n] = r;
+        if (cap) st_f(cap + ((size_t)t * e.n_inject + e.cap_slot) * e.N + n, r);
+        if (e.trace) e.trace[(size_t)t * e.N + n] = r;
+      }
+      break;
+    }
+    case kEpiStore: {
+      for (int i = first; i < cn * 128; i += step) {
+        const int u = i >> 7, c = i & 127;
+        st_f(static_cast<T*>(e.out) + (size_t)(m0 + u) * e.N + n0 + c, val(u, c, 0));
+      }
+      break;
+    }
+    case kEpiSwiGLU: {
+      for (int i = first; i < cn * 128; i += step) {
+        const int u = i >> 7, c = i & 127;
+        const float g = val(u, c, 0), up = val(u, c, 1);
+        st_f(static_cast<T*>(e.act) + (size_t)(m0 + u) * e.F + n0 + c, g / (1.f + __expf(-g)) * up);
+      }
+      break;
+    }
+    case kEpiQKV:
+    case kEpiInject: {
+      const bool inject = e.kind == kEpiInject;
+      const int kvd = e.Hkv * 128;
+      int head, layer = 0;
+      bool is_q = false, is_v = false;
+      if (!inject) {
+        head = n0 / 128;
+        if (head < e.H) is_q = true;
+        else if (head < e.H + e.Hkv) head -= e.H;
+        else { head -= e.H + e.Hkv; is_v = true; }
       } else {
-        const int s = part % S;
-        const int col = (two && part >= S) ? e.F + n0 : n0;
-        src = e.slab + (size_t)s * e.split_stride + (size_t)t * e.N + col;
+        layer = n0 / (2 * kvd);
+        const int o = n0 % (2 * kvd);
+        is_v = o >= kvd;
+        head = (is_v ? o - kvd : o) / 128;
       }
-      cp_async16(smem_u32(sbuf + (u * parts + part) * 128 + q * 4), src + q * 4, 16);
-    }
-    cp_async_commit();
-    cp_async_wait<0>();
-    __syncthreads();
-    // value of the tile at row u (chunk-local), column c (0..127), part group g
-    auto val = [&](int u, int c, int g) {
-      const float* p = sbuf + (u * parts + g * S) * 128 + c;
-      float v = 0.f;
-      for (int s = 0; s < S; ++s) v += p[s * 128];
-      return v;
-    };
-    switch (e.kind) {
-      case kEpiResid: {
-        T* cap = static_cast<T*>(e.capture);
-        for (int i = tid; i < cn * 128; i += nth) {
-          const int u = i >> 7, c = i & 127, t = c0 + u, n = n0 + c;
-          const float r = sbuf[(u * parts + parts - 1) * 128 + c] + val(u, c, 0);
-          e.resid[(size_t)t * e.N + n] = r;
-          if (cap) st_f(cap + ((size_t)t * e.n_inject + e.cap_slot) * e.N + n, r);
-          if (e.trace) e.trace[(size_t)t * e.N + n] = r;
+      T* base;
+      if (is_q) base = static_cast<T*>(e.q_out);
+      else base = static_cast<T*>(is_v ? e.vc : e.kc) +
+                  (inject ? (size_t)(e.layer0 + layer) * e.layer_elems : 0);
+      const int per = is_v ? 128 : 64;
+      for (int i = first; i < cn * per; i += step) {
+        const int u = i / per, c = i % per, t = m0 + u;
+        const int pos = meta[u * 3], seq = meta[u * 3 + 1], slot = meta[u * 3 + 2];
+        if (pos < 0 || seq < 0) continue;
+        if (inject && (seq >= e.max_batch || pos >= e.max_ctx)) {
+          set_dev_status(e.status, kDevCheck);
+          continue;
         }
-        break;
-      }
-      case kEpiStore: {
-        for (int i = tid; i < cn * 128; i += nth) {
-          const int u = i >> 7, c = i & 127;
-          st_f(static_cast<T*>(e.out) + (size_t)(c0 + u) * e.N + n0 + c, val(u, c, 0));
-        }
-        break;
-      }
-      case kEpiSwiGLU: {
-        for (int i = tid; i < cn * 128; i += nth) {
-          const int u = i >> 7, c = i & 127;
-          const float g = val(u, c, 0), up = val(u, c, 1);
-          st_f(static_cast<T*>(e.act) + (size_t)(c0 + u) * e.F + n0 + c, g / (1.f + __expf(-g)) * up);
-        }
-        break;
-      }
-      case kEpiQKV:
-      case kEpiInject: {
-        // one 128-wide tile = one head: Q, K (rotated) or V
-        const bool inject = e.kind == kEpiInject;
-        const int kvd = e.Hkv * 128;
-        int head, layer = 0;
-        bool is_q = false, is_v = false;
-        if (!inject) {
-          head = n0 / 128;
-          if (head < e.H) is_q = true;
-          else if (head < e.H + e.Hkv) head -= e.H;
-          else { head -= e.H + e.Hkv; is_v = true; }
+        T* dst = is_q ? base + ((size_t)t * e.H + head) * 128
+                      : base + (((size_t)seq * e.Hkv + head) * e.max_ctx + slot) * 128;
+        if (is_v) {
+          st_f(dst + c, val(u, c, 0));
         } else {
-          layer = n0 / (2 * kvd);
-          const int o = n0 % (2 * kvd);
-          is_v = o >= kvd;
-          head = (is_v ? o - kvd : o) / 128;
+          const float lo = val(u, c, 0), hi = val(u, c + 64, 0);
+          const float cs = e.rcos[(size_t)pos * 64 + c], sn = e.rsin[(size_t)pos * 64 + c];
+          st_f(dst + c, lo * cs - hi * sn);
+          st_f(dst + c + 64, hi * cs + lo * sn);
         }
-        T* base;
-        if (is_q) base = static_cast<T*>(e.q_out);
-        else base = static_cast<T*>(is_v ? e.vc : e.kc) +
-                    (inject ? (size_t)(e.layer0 + layer) * e.layer_elems : 0);
-        const int per = is_v ? 128 : 64;
-        for (int i = tid; i < cn * per; i += nth) {
-          const int u = i / per, c = i % per, t = c0 + u;
-          int pos, seq, slot;
-          if (inject) {
-            seq = e.row_seq[t];
-            pos = slot = e.row_pos[t];
-            if (seq < 0) continue;
-            if (seq >= e.max_batch || pos < 0 || pos >= e.max_ctx) {
-              set_dev_status(e.status, kDevCheck);
-              continue;
-            }
-          } else {
-            pos = e.row_pos[t];
-            if (pos < 0) continue;
-            seq = e.row_seq[t];
-            slot = e.row_slot[t];
-          }
-          T* dst = is_q ? base + ((size_t)t * e.H + head) * 128
-                        : base + (((size_t)seq * e.Hkv + head) * e.max_ctx + slot) * 128;
-          if (is_v) {
-            st_f(dst + c, val(u, c, 0));
-          } else {
-            const float lo = val(u, c, 0), hi = val(u, c + 64, 0);
-            const float cs = e.rcos[(size_t)pos * 64 + c], sn = e.rsin[(size_t)pos * 64 + c];
-            st_f(dst + c, lo * cs - hi * sn);
-            st_f(dst + c + 64, hi * cs + lo * sn);
-          }
-        }
-        break;
       }
-      default:
-        break;
+      break;
     }
-    __syncthreads();
+    default:
+      break;
   }
 }
 

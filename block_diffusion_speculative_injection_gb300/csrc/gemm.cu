@@ -52,7 +52,12 @@ __global__ void __launch_bounds__(128, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * 128, m0 = blockIdx.y * BN;
+  // SwiGLU clusters pair a gate tile with its up tile: x = 2c + h
+  const int half_tiles = p.epi.F / 128;
+  const int tile_n = p.epi.kind == kEpiSwiGLU
+                         ? ((blockIdx.x & 1) ? (int)(blockIdx.x >> 1) + half_tiles : (int)(blockIdx.x >> 1))
+                         : (int)blockIdx.x;
+  const int n0 = tile_n * 128, m0 = blockIdx.y * BN;
   const int kb0 = blockIdx.z * p.kb_per_split;
   const int kb1 = min(p.n_kb, kb0 + p.kb_per_split);
   const int nkb = kb1 - kb0;
@@ -138,47 +143,52 @@ __global__ void __launch_bounds__(128, 1)
   mbar_wait_sleep(accum, 0, p.status);
   __syncwarp();
   tc_fence_after();
-  const int feat = n0 + warp * 32 + lane;
-  float* outp = p.out + (size_t)blockIdx.z * (size_t)p.split_stride;
+  if (p.epi.kind == kEpiSlab) {  // plain fp32 result (lm_head logits), no K split
+    const int feat = n0 + warp * 32 + lane;
+    for (int c = 0; c < BN; c += 16) {
+      float v[16];
+      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, v);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int t = m0 + c + i;
+        if (t < p.M && feat < p.N) p.out[(size_t)t * p.N + feat] = v[i];
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, tmem_cols);
+    return;
+  }
+
+  // fused epilogue over the cluster of K splits: partial tile -> own smem
+  // (the pipeline buffers are idle now), then a cluster-wide reduction
+  __shared__ int32_t s_meta[256 * 3];
+  float* part = reinterpret_cast<float*>(smem);
   for (int c = 0; c < BN; c += 16) {
     float v[16];
     tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, v);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int t = m0 + c + i;
-      if (t < p.M && feat < p.N) outp[(size_t)t * p.N + feat] = v[i];
+    for (int i = 0; i < 16; ++i) part[(c + i) * 128 + warp * 32 + lane] = v[i];
+  }
+  for (int u = threadIdx.x; u < BN; u += blockDim.x) {
+    const int t = m0 + u;
+    int pos = -1, seq = -1, slot = -1;
+    if (t < p.M && (p.epi.kind == kEpiQKV || p.epi.kind == kEpiInject)) {
+      pos = p.epi.row_pos[t];
+      seq = p.epi.row_seq[t];
+      slot = p.epi.kind == kEpiQKV ? p.epi.row_slot[t] : pos;
     }
+    s_meta[u * 3] = pos;
+    s_meta[u * 3 + 1] = seq;
+    s_meta[u * 3 + 2] = slot;
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, tmem_cols);
-  if (p.epi.kind == kEpiSlab) return;
-
-  // fused epilogue: the CTA that completes a tile (pair) last reduces it
-  __shared__ int s_last;
-  __threadfence();
-  __syncthreads();
-  int n0_epi = n0;
-  if (threadIdx.x == 0) {
-    int group, expect;
-    if (p.epi.kind == kEpiSwiGLU) {
-      const int half_tiles = (p.epi.F + 127) / 128;
-      group = (blockIdx.x % half_tiles) * gridDim.y + blockIdx.y;
-      expect = 2 * gridDim.z;
-    } else {
-      group = blockIdx.x * gridDim.y + blockIdx.y;
-      expect = gridDim.z;
-    }
-    const int old = atomicAdd(&p.epi.counters[group], 1);
-    s_last = (old == expect - 1);
-    if (s_last) p.epi.counters[group] = 0;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  if (p.epi.kind == kEpiSwiGLU) n0_epi = (blockIdx.x % ((p.epi.F + 127) / 128)) * 128;
-  run_epilogue_staged<bf16>(p.epi, n0_epi, m0, BN, reinterpret_cast<float*>(smem),
-                            (int)(S * (a_bytes + b_bytes) / 4));
+  cluster_sync();
+  const int n0_epi = p.epi.kind == kEpiSwiGLU ? (int)(blockIdx.x >> 1) * 128 : n0;
+  run_epilogue_cluster<bf16>(p.epi, n0_epi, m0, BN, part, s_meta);
+  cluster_sync();  // peers may still be reading this CTA's partial tile
 }
 
 // fp32 storage: the epilogue runs as its own kernel over the slab (splits = 1)
@@ -378,13 +388,20 @@ dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs&
   const int per_sm = (BN <= 32) ? 2 : 1;
   const int slots = per_sm * ctx->sm_count;
   int splits = ctas >= slots ? 1 : slots / ctas;
+  // the K splits of a tile form one thread-block cluster (portable size <= 8;
+  // a SwiGLU cluster also holds the matching up tile)
+  const int max_cluster_splits = epi_in.kind == kEpiSwiGLU ? 4 : 8;
+  if (splits > max_cluster_splits) splits = max_cluster_splits;
   if (splits > max_splits) splits = max_splits;
   if (splits > n_kb / 4) splits = n_kb / 4;
-  if (splits < 1) splits = 1;
-  while (splits > 1 && (size_t)splits * M * N > ctx->ws_elems) --splits;
-  if ((size_t)M * N > ctx->ws_elems) {
+  if (splits < 1 || epi_in.kind == kEpiSlab) splits = 1;
+  if (epi_in.kind == kEpiSlab && (size_t)M * N > ctx->ws_elems) {
     set_error(ctx, "GEMM output %dx%d exceeds workspace", M, N);
     return DFLASH_E_CAPACITY;
+  }
+  if (epi_in.kind == kEpiSwiGLU && (N % 256 != 0 || epi_in.F * 2 != N)) {
+    set_error(ctx, "SwiGLU GEMM needs gate and up segments of F %% 128 == 0 rows");
+    return DFLASH_E_UNSUPPORTED;
   }
   const int kb_per = (n_kb + splits - 1) / splits;
   splits = (n_kb + kb_per - 1) / kb_per;
@@ -419,12 +436,7 @@ dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs&
   p.epi.splits = splits;
   p.epi.split_stride = (long long)M * N;
   p.epi.slab = out;
-  p.epi.counters = ctx->tile_counters;
   p.epi.status = ctx->dev_status;
-  if (p.epi.kind != kEpiSlab && (size_t)n_tiles * m_tiles > ctx->n_tile_counters) {
-    set_error(ctx, "GEMM has more tiles than tile counters");
-    return DFLASH_E_CAPACITY;
-  }
 
   static bool attr_set = false;
   if (!attr_set) {
@@ -434,7 +446,9 @@ dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs&
   }
   dim3 grid(n_tiles, m_tiles, splits);
   const size_t smem_bytes = tc_smem_bytes(BN, stages);
-  DF_CUDA_TRY(ctx, launch_k(ctx->pdl, gemm_tc_kernel, dim3(grid), dim3(128), smem_bytes, st, maps, *xm, p));
+  const dim3 cluster(epi_in.kind == kEpiSwiGLU ? 2 : 1, 1, splits);
+  DF_CUDA_TRY(ctx, launch_k_cluster(ctx->pdl, cluster, gemm_tc_kernel, grid, dim3(128), smem_bytes,
+                                    st, maps, *xm, p));
   DF_LAUNCHED(ctx);
   *splits_used = splits;
   return DFLASH_OK;
