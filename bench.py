@@ -120,7 +120,7 @@ class OracleSample:
         s = w.shape
         self.w, self.s, self.nm = w, s, nm
         self.W = Weights(wl.SyntheticWeights(s, w.seed))
-        P = w.prompt_len[0]
+        P = (w.prompt_len[0] + w.prompt_len[1]) // 2
         rng = np.random.default_rng(5)
         self.P = P
         self.ck = nm.round_bf16(rng.standard_normal((P, s.n_kv_heads, s.head_dim)))
@@ -163,16 +163,20 @@ class OracleSample:
         t = time.perf_counter()
         nm.linear(self.hcat, W["draft.fuse"])
         t_inj = time.perf_counter() - t
-        per_step = B * (s.n_layers * t_tl + s.n_draft_layers * t_dl) + (2 * B - 1) * t_lm + t_inj
+        rows_v = self.w.tree_budget + 1 if self.w.tree_budget else B
+        per_seq = (rows_v * s.n_layers * t_tl + B * s.n_draft_layers * t_dl
+                   + (rows_v + B - 1) * t_lm + t_inj)
         sampled = 2 * t_tl + 2 * t_dl + t_lm / 16 + t_inj
-        return per_step, sampled
+        return per_seq * self.w.batch, sampled
 
     def describe(self, sampled):
-        s, B = self.s, self.w.block_size
+        s, B, b = self.s, self.w.block_size, self.w.batch
+        rows_v = self.w.tree_budget + 1 if self.w.tree_budget else B
         return (f"oracle (fp64 numpy) on 2 rows of 1 target layer and 1 draft layer at context "
                 f"{self.P}, 1/16 of the lm_head for 1 row, the fuse projection for 1 row; "
-                f"extrapolated to {B} rows x ({s.n_layers}+{s.n_draft_layers}) layers and "
-                f"{2 * B - 1} lm_head rows per step; {sampled:.2f}s of CPU work per sample")
+                f"extrapolated per sequence to {rows_v} verify rows x {s.n_layers} target layers, "
+                f"{B} draft rows x {s.n_draft_layers} draft layers and {rows_v + B - 1} lm_head "
+                f"rows, times {b} sequence(s) per step; {sampled:.2f}s of CPU work per sample")
 
 
 def cpu_cores() -> int:
@@ -196,7 +200,7 @@ def run_reference(args, w: wl.Workload) -> None:
         sampled.append(cpu_s)
     per_step = statistics.median(times)
     info = smp.describe(statistics.median(sampled)) + f"; {args.steps} samples, median"
-    value = w.batch * 1.0 / per_step  # random-init weights: one verified token per step
+    value = w.batch * 1.0 / per_step  # random-init weights: one verified token per sequence and step
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -240,20 +244,32 @@ def run_ours(args, w: wl.Workload) -> None:
     prompts = wl.prompts(w)
     total_steps = args.warmup + args.steps + args.prof_steps + args.e2e_steps + 4
     max_ctx = max(lens) + B * (total_steps + 2) + args.ar_steps + 64
-    eng = DFlashEngine(w.shape, B, b, max_ctx, max_rows=max(max(lens), b * B), seed=w.seed)
+    tree = w.tree_budget > 0
+    nmax = w.tree_budget + 1 if tree else 0
+    max_ctx += nmax
+    eng = DFlashEngine(w.shape, B, b, max_ctx, max_rows=max(max(lens), b * max(B, nmax)),
+                       max_tree_nodes=nmax, seed=w.seed)
+
+    def one_step(anchor_buf):
+        if tree:
+            r = eng.tree_step(sid, anchor_buf, w.topk, w.tree_budget)
+            return r["emitted"], r["accept_len"], r["next_anchor"]
+        o = eng.step(sid, anchor_buf)
+        return o.emitted, o.accept_len, o.next_anchor
+
     ctx = eng.ctx
     sid = eng.seq_ids(b)
     stream = torch.cuda.current_stream()
 
     anchors = eng.prefill(prompts)
     for _ in range(args.warmup):
-        eng.step(sid, anchors)
+        one_step(anchors)
         anchors = eng.next_anchor[:b].clone()
     graph = ar_graph = None
     per_step_launches = None
     if not args.no_graph:
         l_cap = capi.dflash_launch_count(ctx)
-        graph = capture_step_graph(eng, sid)
+        graph = capture_step_graph(eng, sid, tree=tree, topk=w.topk, budget=w.tree_budget)
         per_step_launches = capi.dflash_launch_count(ctx) - l_cap
         for _ in range(2):
             graph.replay()
@@ -271,7 +287,7 @@ def run_ours(args, w: wl.Workload) -> None:
             graph.replay()
     else:
         for _ in range(args.steps):
-            eng.step(sid, eng.next_anchor[:b])
+            one_step(eng.next_anchor[:b])
     ev1.record(stream)
     barrier()
     clocks = sampler.stop()
@@ -296,7 +312,7 @@ def run_ours(args, w: wl.Workload) -> None:
     # live per-kernel timing over a second pass of the same steps
     capi.dflash_profile(ctx, True)
     for _ in range(args.prof_steps):
-        eng.step(sid, anchors)
+        one_step(anchors)
         anchors = eng.next_anchor[:b].clone()
     capi.dflash_profile(ctx, False)
     prof = {}
@@ -342,7 +358,7 @@ def run_ours(args, w: wl.Workload) -> None:
     # end to end through the C ABI with host buffers
     h_anchor = torch.empty(b, dtype=torch.int32, pin_memory=True)
     h_anchor.copy_(anchors.cpu())
-    h_emit = torch.empty(b, B, dtype=torch.int32, pin_memory=True)
+    h_emit = torch.empty(b, max(B, nmax), dtype=torch.int32, pin_memory=True)
     h_acc = torch.empty(b, dtype=torch.int32, pin_memory=True)
     d_anchor = torch.empty(b, dtype=torch.int32, device="cuda")
     barrier()
@@ -350,10 +366,10 @@ def run_ours(args, w: wl.Workload) -> None:
     e2e_tokens = 0
     for _ in range(args.e2e_steps):
         d_anchor.copy_(h_anchor, non_blocking=True)
-        out = eng.step(sid, d_anchor)
-        h_emit.copy_(out.emitted, non_blocking=True)
-        h_acc.copy_(out.accept_len, non_blocking=True)
-        h_anchor.copy_(out.next_anchor, non_blocking=True)
+        em, acc, nxt = one_step(d_anchor)
+        h_emit.copy_(em, non_blocking=True)
+        h_acc.copy_(acc, non_blocking=True)
+        h_anchor.copy_(nxt, non_blocking=True)
         stream.synchronize()
         e2e_tokens += int(h_acc.sum().item()) + b
     e2e_s = time.perf_counter() - t0
@@ -399,7 +415,7 @@ def run_ours(args, w: wl.Workload) -> None:
         "kernel_ms_per_step": {k: v["ms_per_step"] for k, v in prof.items()},
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": 4 * b,
-                "d2h_bytes_per_step": 4 * b * B + 8 * b},
+                "d2h_bytes_per_step": 4 * b * max(B, nmax) + 8 * b},
         "cpu_baseline": cpu,
     }
     print(json.dumps(line))
@@ -416,7 +432,8 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="qwen3_8b_b1",
-                    choices=["qwen3_8b_b1", "qwen3_8b_b32", "qwen3_8b_slice_b1", "tiny_f32_e2e",
+                    choices=["qwen3_8b_b1", "qwen3_8b_b32", "llama31_8b_ddtree_b4", "qwen3_8b_slice_b1",
+                             "tiny_f32_e2e",
                              "mini_bf16_e2e"])
     ap.add_argument("--prof-steps", type=int, default=10)
     ap.add_argument("--ar-steps", type=int, default=50)
