@@ -433,6 +433,7 @@ def main() -> None:
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="qwen3_8b_b1",
                     choices=["qwen3_8b_b1", "qwen3_8b_b32", "llama31_8b_ddtree_b4", "qwen3_8b_slice_b1",
+                             "qwen3_8b_slice_b32",
                              "tiny_f32_e2e",
                              "mini_bf16_e2e"])
     ap.add_argument("--prof-steps", type=int, default=10)

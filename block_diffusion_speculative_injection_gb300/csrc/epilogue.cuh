@@ -198,16 +198,13 @@ __device__ void run_epilogue_cluster(const EpiArgs& e, int n0, int m0, int BN, c
   const int rank = (int)cluster_ctarank();
   const int cn = min(BN, e.M - m0);
   const uint32_t local = smem_u32(part);
-  uint32_t peer[16];
-#pragma unroll
-  for (int r = 0; r < 16; ++r)
-    if (r < csize) peer[r] = map_peer(local, (uint32_t)r);
+  // partial of split s (gate h = 0 / up h = 1 for SwiGLU) at tile row u, column c
   auto val = [&](int u, int c, int h) {
-    const uint32_t off = (uint32_t)((u * 128 + c) * 4);
+    const uint32_t addr = local + (uint32_t)((u * 128 + c) * 4);
     float v = 0.f;
 #pragma unroll
     for (int s = 0; s < 8; ++s)
-      if (s < S) v += ld_peer_f32(peer[two ? h + 2 * s : s] + off);
+      if (s < S) v += ld_peer_f32(map_peer(addr, (uint32_t)(two ? h + 2 * s : s)));
     return v;
   };
   const int first = rank * (int)blockDim.x + (int)threadIdx.x;

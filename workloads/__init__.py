@@ -140,6 +140,7 @@ WORKLOADS: Dict[str, Workload] = {
         Workload("mini_bf16_e2e", MINI_BF16, 16, 3, (40, 160), 48),
         Workload("mini_bf16_ddtree", MINI_BF16, 16, 2, (96, 130), 40, tree_budget=64, topk=8),
         Workload("qwen3_8b_slice_b1", QWEN3_8B_SLICE, 16, 1, (2048, 2048), 256),
+        Workload("qwen3_8b_slice_b32", QWEN3_8B_SLICE, 16, 32, (512, 1024), 128),
     )
 }
 
