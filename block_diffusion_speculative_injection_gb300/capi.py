@@ -89,11 +89,15 @@ def header_functions():
     return sorted(set(re.findall(r"\b((?:dflash|dtree)_[a-z_]+)\s*\(", src)))
 
 
-def load(path: str = LIB_PATH) -> ctypes.CDLL:
-    """Loads libdflash.so (raises if it has not been built)."""
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Loads libdflash.so (raises if it has not been built).  DFLASH_LIB_PATH
+    names another build of the same library (e.g. one compiled with
+    different tuning flags)."""
     global _lib
     if _lib is not None:
         return _lib
+    if path is None:
+        path = os.environ.get("DFLASH_LIB_PATH", LIB_PATH)
     if not os.path.exists(path):
         raise FileNotFoundError(f"{path} is missing: build it with __graft_entry__.build()")
     lib = ctypes.CDLL(path)

@@ -90,11 +90,13 @@ __global__ void __launch_bounds__(128, 1)
     tma_prefetch_desc(&xmap);
     // Weights are never written by an earlier kernel: fill the first stages'
     // weight tiles before waiting on the preceding kernel (programmatic
-    // dependent launch), then add the activation tiles.
+    // dependent launch), then add the activation tiles.  Weights are read
+    // once per pass: their lines are first in line for eviction from L2.
+    const uint64_t wpol = l2_policy_evict_first();
     const int pre = min(S, nkb);
     for (int i = 0; i < pre; ++i) {
       mbar_arrive_expect_tx(&full[i], a_bytes + b_bytes);
-      tma_load_2d(a_s + i * a_bytes, &wmaps.m[seg], (kb0 + i) * 64, wrow0, &full[i]);
+      tma_load_2d_hint(a_s + i * a_bytes, &wmaps.m[seg], (kb0 + i) * 64, wrow0, &full[i], wpol);
     }
     pdl_wait();
     for (int i = 0; i < pre; ++i)
@@ -106,7 +108,7 @@ __global__ void __launch_bounds__(128, 1)
       if (!mbar_wait(&empty[s], ph ^ 1u, p.status)) break;
       mbar_arrive_expect_tx(&full[s], a_bytes + b_bytes);
       const int kx = (kb0 + i) * 64;
-      tma_load_2d(a_s + s * a_bytes, &wmaps.m[seg], kx, wrow0, &full[s]);
+      tma_load_2d_hint(a_s + s * a_bytes, &wmaps.m[seg], kx, wrow0, &full[s], wpol);
       tma_load_2d(b_s + s * b_bytes, &xmap, kx, m0, &full[s]);
       ++issued;
     }
@@ -308,6 +310,8 @@ static dflash_status get_tmap(dflash_ctx* ctx, const void* ptr, int64_t rows, in
   return DFLASH_OK;
 }
 
+static size_t tc_smem_bytes(int BN, int stages);
+
 static int tc_stages(int BN) {
   const int per = 128 * 64 * 2 + BN * 64 * 2;
   int budget = (BN <= 32) ? 110 * 1024 : 200 * 1024;  // small tiles: 2 CTAs per SM
@@ -319,6 +323,53 @@ static int tc_stages(int BN) {
 
 static size_t tc_smem_bytes(int BN, int stages) {
   return 1024 + (size_t)stages * (128 * 64 * 2 + BN * 64 * 2) + (2 * stages + 1) * 8 + 16;
+}
+
+// tile shape and K split of one bf16 GEMM launch
+struct TcPlan {
+  int BN, m_tiles, n_tiles, stages, n_kb, splits, kb_per;
+};
+
+static cudaError_t ensure_tc_smem() {
+  static bool done = false;
+  if (done) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       210 * 1024);
+  if (e == cudaSuccess) done = true;
+  return e;
+}
+
+static TcPlan plan_tc(dflash_ctx* ctx, int M, int N, int K, int kind, int max_splits) {
+  TcPlan t;
+  t.m_tiles = (M + 255) / 256;
+  int BN = (M + t.m_tiles - 1) / t.m_tiles;
+  BN = ((BN + 15) / 16) * 16;
+  t.BN = BN < 16 ? 16 : BN;
+  t.stages = tc_stages(t.BN);
+  t.n_tiles = (N + 127) / 128;
+  t.n_kb = K / 64;
+  const int ctas = t.n_tiles * t.m_tiles;
+  // K splits: as many as fit in ONE wave of resident CTAs (a partial second
+  // wave would double the latency of these short, bandwidth-bound launches)
+  const int per_sm = (t.BN <= 32) ? 2 : 1;
+  const int slots = per_sm * ctx->sm_count;
+  int splits = ctas >= slots ? 1 : slots / ctas;
+  // the K splits of a tile form one thread-block cluster (portable size <= 8;
+  // a SwiGLU cluster also holds the matching up tile)
+  const int max_cluster_splits = kind == kEpiSwiGLU ? 4 : 8;
+  if (splits > max_cluster_splits) splits = max_cluster_splits;
+  if (splits > max_splits) splits = max_splits;
+  if (splits > t.n_kb / 4) splits = t.n_kb / 4;
+  if (splits < 1 || kind == kEpiSlab) splits = 1;
+  // ... and every cluster of the launch resident at once: clusters that wait
+  // for a second wave double the launch time.  A cluster sits inside one GPC,
+  // so fewer than slots / size clusters fit; on GB300 (152 SMs, 2 CTAs per
+  // SM) between 0.875 and 0.97 of that number were resident for cluster
+  // sizes 2..8, so the plan counts on 7/8 of it.
+  while (splits > 1 && (int64_t)ctas * splits * 8 > (int64_t)slots * 7) --splits;
+  t.kb_per = (t.n_kb + splits - 1) / splits;
+  t.splits = (t.n_kb + t.kb_per - 1) / t.kb_per;
+  return t;
 }
 
 dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs& segs,
@@ -375,26 +426,11 @@ dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs&
       set_error(ctx, "GEMM segment %d has %d rows (not a multiple of 128)", i, segs.rows[i]);
       return DFLASH_E_UNSUPPORTED;
     }
-  const int m_tiles = (M + 255) / 256;
-  int BN = (M + m_tiles - 1) / m_tiles;
-  BN = ((BN + 15) / 16) * 16;
-  if (BN < 16) BN = 16;
-  const int stages = tc_stages(BN);
-  const int n_tiles = (N + 127) / 128;
-  const int n_kb = K / 64;
-  const int ctas = n_tiles * m_tiles;
-  // K splits: as many as fit in ONE wave of resident CTAs (a partial second
-  // wave would double the latency of these short, bandwidth-bound launches)
-  const int per_sm = (BN <= 32) ? 2 : 1;
-  const int slots = per_sm * ctx->sm_count;
-  int splits = ctas >= slots ? 1 : slots / ctas;
-  // the K splits of a tile form one thread-block cluster (portable size <= 8;
-  // a SwiGLU cluster also holds the matching up tile)
-  const int max_cluster_splits = epi_in.kind == kEpiSwiGLU ? 4 : 8;
-  if (splits > max_cluster_splits) splits = max_cluster_splits;
-  if (splits > max_splits) splits = max_splits;
-  if (splits > n_kb / 4) splits = n_kb / 4;
-  if (splits < 1 || epi_in.kind == kEpiSlab) splits = 1;
+  const TcPlan plan = plan_tc(ctx, M, N, K, epi_in.kind, max_splits);
+  const int m_tiles = plan.m_tiles, BN = plan.BN, stages = plan.stages, n_tiles = plan.n_tiles;
+  const int n_kb = plan.n_kb;
+  const int kb_per = plan.kb_per;
+  int splits = plan.splits;
   if (epi_in.kind == kEpiSlab && (size_t)M * N > ctx->ws_elems) {
     set_error(ctx, "GEMM output %dx%d exceeds workspace", M, N);
     return DFLASH_E_CAPACITY;
@@ -403,8 +439,6 @@ dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs&
     set_error(ctx, "SwiGLU GEMM needs gate and up segments of F %% 128 == 0 rows");
     return DFLASH_E_UNSUPPORTED;
   }
-  const int kb_per = (n_kb + splits - 1) / splits;
-  splits = (n_kb + kb_per - 1) / kb_per;
 
   TmapSet maps;
   memset(&maps, 0, sizeof(maps));
@@ -438,12 +472,7 @@ dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs&
   p.epi.slab = out;
   p.epi.status = ctx->dev_status;
 
-  static bool attr_set = false;
-  if (!attr_set) {
-    DF_CUDA_TRY(ctx, cudaFuncSetAttribute(gemm_tc_kernel,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, 210 * 1024));
-    attr_set = true;
-  }
+  DF_CUDA_TRY(ctx, ensure_tc_smem());
   dim3 grid(n_tiles, m_tiles, splits);
   const size_t smem_bytes = tc_smem_bytes(BN, stages);
   const dim3 cluster(epi_in.kind == kEpiSwiGLU ? 2 : 1, 1, splits);
