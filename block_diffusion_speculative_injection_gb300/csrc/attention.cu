@@ -121,8 +121,18 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const AttnK p) {
   if (j0 >= blk) return;
   const int jmax = min(j0 + POS, blk);  // exclusive
   int key_end = (p.mask == kMaskCausal) ? ctx_len + jmax : ctx_len + blk;
-  const int k_begin = split * p.keys_per_split;
-  const int k_stop = min(key_end, k_begin + p.keys_per_split);
+  // causal and draft passes: this sequence's keys in equal whole-tile
+  // shares over the splits (the launch is sized for the longest context;
+  // shorter ones must not leave the later splits idle).  Tree verify keeps
+  // the plan's fixed share, which measured faster there.
+  const int kps =
+      p.mask == kMaskTree
+          ? p.keys_per_split
+          : min(p.keys_per_split,
+                max(kTileKeys, (key_end + p.n_splits * kTileKeys - 1) / (p.n_splits * kTileKeys) *
+                                   kTileKeys));
+  const int k_begin = split * kps;
+  const int k_stop = min(key_end, k_begin + kps);
 
   // this thread's two query rows (within the CTA tile) and their block index
   const int r0 = warp * 16 + (lane >> 2), r1 = r0 + 8;
