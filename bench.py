@@ -425,6 +425,72 @@ def run_ours(args, w: wl.Workload) -> None:
 KERNEL_REV = "gemm-v3"
 
 
+def run_attn_op(args) -> None:
+    """Block attention op (dflash_block_attention) over the grid of context
+    lengths x batches: Q [b,16,32,128], K/V [b,8,ctx+16,128] bf16, block
+    visible without mask.  Each point: W warm-up calls, then K calls timed
+    one by one with CUDA events on the launching stream, a 256 MB buffer
+    written between calls so that every call starts with a cold L2; the
+    median is reported against the measured HBM peak."""
+    import torch
+
+    from block_diffusion_speculative_injection_gb300 import capi
+    from block_diffusion_speculative_injection_gb300.engine import device_operand
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    H, HKV, HD = wl.ATTN_OP_HEADS
+    BLK = 16
+    hbm, _, src = peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    sampler = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    points = []
+    sampler.start()
+    for ctx in wl.ATTN_OP_CTX:
+        for b in wl.ATTN_OP_BATCH:
+            q = device_operand("q", b * BLK * H).view(b, BLK, H, HD)
+            k = device_operand("k", b * HKV * (ctx + BLK)).view(b, HKV, ctx + BLK, HD)
+            v = device_operand("v", b * HKV * (ctx + BLK)).view(b, HKV, ctx + BLK, HD)
+            out = torch.empty_like(q)
+            need = capi.dflash_block_attention_workspace(b, H, HKV, ctx, BLK)
+            ws = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
+            for _ in range(args.warmup):
+                capi.dflash_block_attention(b, H, HKV, ctx, BLK, 0, q, k, v, out, ws)
+            times = []
+            for _ in range(args.steps):
+                flush.fill_(1)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                capi.dflash_block_attention(b, H, HKV, ctx, BLK, 0, q, k, v, out, ws)
+                e1.record(stream)
+                e1.synchronize()
+                times.append(e0.elapsed_time(e1) * 1e3)
+            us = statistics.median(times)
+            nbytes = b * (4096 * ctx + 327680)  # ctx + block K/V, Q and O per sequence
+            gbs = nbytes / (us * 1e-6) / 1e9
+            points.append({"ctx": ctx, "batch": b, "us": us, "bytes": nbytes, "gbs": gbs,
+                           "frac": gbs / hbm, "roofline_us": nbytes / (hbm * 1e9) * 1e6})
+            del q, k, v, out, ws
+    clocks = sampler.stop()
+    head = next(pt for pt in points if pt["ctx"] == max(wl.ATTN_OP_CTX) and pt["batch"] == max(wl.ATTN_OP_BATCH))
+    line = {
+        "metric": "block attention op: achieved HBM bandwidth (Q [b,16,32,128] over ctx+16 keys, GQA 4:1)",
+        "value": head["gbs"], "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": head["us"] / 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) operands)",
+        "config": {"workload": "attn_op", "points": f"ctx {list(wl.ATTN_OP_CTX)} x batch {list(wl.ATTN_OP_BATCH)}",
+                   "headline_point": {"ctx": head["ctx"], "batch": head["batch"]},
+                   "l2": "256 MB buffer written before every timed call"},
+        "roofline": {"bound": "hbm", "kernel": "attn_mma_kernel (+ attn_combine_kernel)", "achieved": head["gbs"],
+                     "peak": hbm, "unit": "GB/s", "frac": head["gbs"] / hbm, "traffic": None,
+                     "peak_source": src},
+        "points": points,
+        "clocks": clocks,
+    }
+    print(json.dumps(line))
+
+
 def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -433,7 +499,7 @@ def main() -> None:
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="qwen3_8b_b1",
                     choices=["qwen3_8b_b1", "qwen3_8b_b32", "llama31_8b_ddtree_b4", "qwen3_8b_slice_b1",
-                             "qwen3_8b_slice_b32",
+                             "qwen3_8b_slice_b32", "attn_op",
                              "tiny_f32_e2e",
                              "mini_bf16_e2e"])
     ap.add_argument("--prof-steps", type=int, default=10)
@@ -445,6 +511,11 @@ def main() -> None:
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
+    if args.workload == "attn_op":
+        if args.impl == "reference":
+            raise SystemExit("the attention op has no reference arm; its oracle check is in tests/")
+        run_attn_op(args)
+        return
     w = wl.WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)

@@ -453,23 +453,36 @@ __global__ void attn_simt_f32_kernel(const AttnK p) {
   for (int i = 0; i < per; ++i) og[lane + 32 * i] = acc[i] / l;
 }
 
-// number of KV splits and keys per split for a launch of `ctas` CTAs
+// number of KV splits and keys per split for a launch of `ctas` CTAs.  The
+// split count minimises the estimated makespan: waves of resident CTAs (2 per
+// SM) x (key tiles per split + a fixed cost of about two tiles for the Q
+// load, the partial write and the combine), so that a launch never ends with
+// a nearly empty extra wave of full-length splits.
 static void plan_splits(int sm_count, int ctas, int64_t max_keys, size_t part_cap, int rows_heads,
-                        int* n_splits, int* keys_per_split) {
-  const int64_t key_tiles = (max_keys + kTileKeys - 1) / kTileKeys;
-  int splits = (2 * sm_count + ctas - 1) / ctas;
-  // at least 4 key tiles (256 keys) per split, at most kMaxSplits splits
-  if (splits > (key_tiles + 3) / 4) splits = (int)((key_tiles + 3) / 4);
-  if (splits > kMaxSplits) splits = kMaxSplits;
-  if (splits < 1) splits = 1;
-  while (splits > 1 && (size_t)splits * rows_heads > part_cap) --splits;
-  *keys_per_split = 1 << 30;
-  if (splits > 1) {
-    const int64_t tiles_per = (key_tiles + splits - 1) / splits;
-    *keys_per_split = (int)(tiles_per * kTileKeys);
-    splits = (int)((key_tiles + tiles_per - 1) / tiles_per);
+                        int* n_splits, int* keys_per_split, int min_splits = 1) {
+  const int64_t key_tiles = std::max<int64_t>(1, (max_keys + kTileKeys - 1) / kTileKeys);
+  const int64_t slots = 2 * (int64_t)sm_count;
+  int best = 1;
+  int64_t best_cost = INT64_MAX;
+  const int64_t s_max = std::min<int64_t>(kMaxSplits, key_tiles);
+  for (int64_t sp = std::min<int64_t>(min_splits, s_max); sp <= s_max; ++sp) {
+    if (sp > 1 && (size_t)sp * rows_heads > part_cap) break;
+    const int64_t tiles_per = (key_tiles + sp - 1) / sp;
+    if (sp > 1 && (key_tiles + tiles_per - 1) / tiles_per < sp) continue;  // same as a smaller split
+    const int64_t waves = (ctas * sp + slots - 1) / slots;
+    const int64_t cost = waves * (tiles_per + 2) + (sp > 1 ? 1 : 0);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = (int)sp;
+    }
   }
-  *n_splits = splits;
+  *keys_per_split = 1 << 30;
+  if (best > 1) {
+    const int64_t tiles_per = (key_tiles + best - 1) / best;
+    *keys_per_split = (int)(tiles_per * kTileKeys);
+    best = (int)((key_tiles + tiles_per - 1) / tiles_per);
+  }
+  *n_splits = best;
 }
 
 static int device_sms() {
@@ -533,9 +546,11 @@ dflash_status attention(dflash_ctx* ctx, const AttnArgs& a, cudaStream_t st) {
   const int POS = 64 / p.G;
   const int q_tiles = (a.q_stride + POS - 1) / POS;
   const int ctas = q_tiles * c.n_kv_heads * a.batch;
+  // a batch's sequences differ in length: with one split the longest ones
+  // set the time while the rest idle, so batched passes take two or more
   int splits = 1;
   plan_splits(ctx->sm_count, ctas, a.max_keys_ub, ctx->part_rows_cap, p.rows_total * p.H, &splits,
-              &p.keys_per_split);
+              &p.keys_per_split, a.batch > 1 ? 2 : 1);
   p.n_splits = splits;
   DF_CUDA_TRY(ctx, ensure_attn_smem());
   dim3 grid(q_tiles, c.n_kv_heads, a.batch * splits);
