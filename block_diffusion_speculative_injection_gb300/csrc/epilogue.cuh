@@ -1,8 +1,9 @@
-// Fused GEMM epilogues.  A GEMM writes fp32 partial tiles ("slabs", one per
-// K split); the CTA that finishes a tile (or a tile pair, for SwiGLU) last
-// sums the slabs in split order -- so the result does not depend on which
-// CTA finishes last -- and applies the operation that follows the
-// projection in the pass:
+// Fused GEMM epilogues.  The K splits of a tile are summed in split order
+// (so the result does not depend on timing) -- from the partial tiles in
+// the shared memory of a thread-block cluster (bf16 tensor-core GEMM,
+// run_epilogue_cluster) or from fp32 slabs in global memory (fp32 SIMT
+// GEMM, run_epilogue) -- and the operation that follows the projection in
+// the pass is applied:
 //   QKV    RoPE on Q and K at the row's position; Q -> q_out, K/V -> cache
 //   SWIGLU act = SiLU(gate) * up            (tile pair: gate tile, up tile)
 //   RESID  residual += projection (+ bf16 capture of an injected layer)
@@ -189,17 +190,28 @@ __device__ void run_epilogue(const EpiArgs& e, int n0, int m0, int BN) {
 // and applies the epilogue operation.  meta[u] = (position, sequence, slot)
 // of tile row u (QKV / INJECT).
 // ---------------------------------------------------------------------------
+#ifndef DFLASH_EPI_UNROLL
+#define DFLASH_EPI_UNROLL 1
+#endif
+
 template <typename T>
 __device__ void run_epilogue_cluster(const EpiArgs& e, int n0, int m0, int BN, const float* part,
                                      const int32_t* meta) {
+  // Every thread takes kU work items per round and issues all of their
+  // loads (global operands, then partials) before using any.
+  constexpr int kU = DFLASH_EPI_UNROLL;
   const int S = e.splits;
   const bool two = e.kind == kEpiSwiGLU;
   const int csize = two ? 2 * S : S;
   const int rank = (int)cluster_ctarank();
   const int cn = min(BN, e.M - m0);
   const uint32_t local = smem_u32(part);
-  // partial of split s (gate h = 0 / up h = 1 for SwiGLU) at tile row u, column c
+  // sum over the splits of the partial (gate h = 0 / up h = 1 for SwiGLU) at
+  // tile row u, column c, in split order through distributed shared memory;
+  // a cluster of one CTA reads its own tile with ordinary shared loads
+  const bool alone = S == 1 && !two;
   auto val = [&](int u, int c, int h) {
+    if (alone) return part[u * 128 + c];
     const uint32_t addr = local + (uint32_t)((u * 128 + c) * 4);
     float v = 0.f;
 #pragma unroll
@@ -212,27 +224,67 @@ __device__ void run_epilogue_cluster(const EpiArgs& e, int n0, int m0, int BN, c
   switch (e.kind) {
     case kEpiResid: {
       T* cap = static_cast<T*>(e.capture);
-      for (int i = first; i < cn * 128; i += step) {
-        const int u = i >> 7, c = i & 127, t = m0 + u, n = n0 + c;
-        const float r = e.resid[(size_t)t * e.N + n] + val(u, c, 0);
-        e.resid[(size_t)t * e.N + n] = r;
-        if (cap) st_f(cap + ((size_t)t * e.n_inject + e.cap_slot) * e.N + n, r);
-        if (e.trace) e.trace[(size_t)t * e.N + n] = r;
+      const int total = cn * 128;
+      for (int i0 = first; i0 < total; i0 += kU * step) {
+        float r[kU], v[kU];
+#pragma unroll
+        for (int k = 0; k < kU; ++k) {
+          const int i = i0 + k * step;
+          r[k] = i < total ? e.resid[(size_t)(m0 + (i >> 7)) * e.N + n0 + (i & 127)] : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < kU; ++k) {
+          const int i = i0 + k * step;
+          v[k] = i < total ? val(i >> 7, i & 127, 0) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < kU; ++k) {
+          const int i = i0 + k * step;
+          if (i >= total) continue;
+          const int t = m0 + (i >> 7), n = n0 + (i & 127);
+          const float x = r[k] + v[k];
+          e.resid[(size_t)t * e.N + n] = x;
+          if (cap) st_f(cap + ((size_t)t * e.n_inject + e.cap_slot) * e.N + n, x);
+          if (e.trace) e.trace[(size_t)t * e.N + n] = x;
+        }
       }
       break;
     }
     case kEpiStore: {
-      for (int i = first; i < cn * 128; i += step) {
-        const int u = i >> 7, c = i & 127;
-        st_f(static_cast<T*>(e.out) + (size_t)(m0 + u) * e.N + n0 + c, val(u, c, 0));
+      const int total = cn * 128;
+      for (int i0 = first; i0 < total; i0 += kU * step) {
+        float v[kU];
+#pragma unroll
+        for (int k = 0; k < kU; ++k) {
+          const int i = i0 + k * step;
+          v[k] = i < total ? val(i >> 7, i & 127, 0) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < kU; ++k) {
+          const int i = i0 + k * step;
+          if (i < total)
+            st_f(static_cast<T*>(e.out) + (size_t)(m0 + (i >> 7)) * e.N + n0 + (i & 127), v[k]);
+        }
       }
       break;
     }
     case kEpiSwiGLU: {
-      for (int i = first; i < cn * 128; i += step) {
-        const int u = i >> 7, c = i & 127;
-        const float g = val(u, c, 0), up = val(u, c, 1);
-        st_f(static_cast<T*>(e.act) + (size_t)(m0 + u) * e.F + n0 + c, g / (1.f + __expf(-g)) * up);
+      const int total = cn * 128;
+      for (int i0 = first; i0 < total; i0 += kU * step) {
+        float g[kU], up[kU];
+#pragma unroll
+        for (int k = 0; k < kU; ++k) {
+          const int i = i0 + k * step;
+          g[k] = i < total ? val(i >> 7, i & 127, 0) : 0.f;
+          up[k] = i < total ? val(i >> 7, i & 127, 1) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < kU; ++k) {
+          const int i = i0 + k * step;
+          if (i < total)
+            st_f(static_cast<T*>(e.act) + (size_t)(m0 + (i >> 7)) * e.F + n0 + (i & 127),
+                 g[k] / (1.f + __expf(-g[k])) * up[k]);
+        }
       }
       break;
     }
@@ -258,23 +310,47 @@ __device__ void run_epilogue_cluster(const EpiArgs& e, int n0, int m0, int BN, c
       else base = static_cast<T*>(is_v ? e.vc : e.kc) +
                   (inject ? (size_t)(e.layer0 + layer) * e.layer_elems : 0);
       const int per = is_v ? 128 : 64;
-      for (int i = first; i < cn * per; i += step) {
-        const int u = i / per, c = i % per, t = m0 + u;
-        const int pos = meta[u * 3], seq = meta[u * 3 + 1], slot = meta[u * 3 + 2];
-        if (pos < 0 || seq < 0) continue;
-        if (inject && (seq >= e.max_batch || pos >= e.max_ctx)) {
-          set_dev_status(e.status, kDevCheck);
-          continue;
+      const int total = cn * per;
+      for (int i0 = first; i0 < total; i0 += kU * step) {
+        float lo[kU], hi[kU], cs[kU], sn[kU];
+#pragma unroll
+        for (int k = 0; k < kU; ++k) {
+          const int i = i0 + k * step;
+          cs[k] = 1.f;
+          sn[k] = 0.f;
+          if (i < total && !is_v) {
+            const int pos = meta[(i / per) * 3];
+            if (pos >= 0 && pos < e.max_ctx) {  // the tables hold max_ctx positions
+              cs[k] = e.rcos[(size_t)pos * 64 + i % per];
+              sn[k] = e.rsin[(size_t)pos * 64 + i % per];
+            }
+          }
         }
-        T* dst = is_q ? base + ((size_t)t * e.H + head) * 128
-                      : base + (((size_t)seq * e.Hkv + head) * e.max_ctx + slot) * 128;
-        if (is_v) {
-          st_f(dst + c, val(u, c, 0));
-        } else {
-          const float lo = val(u, c, 0), hi = val(u, c + 64, 0);
-          const float cs = e.rcos[(size_t)pos * 64 + c], sn = e.rsin[(size_t)pos * 64 + c];
-          st_f(dst + c, lo * cs - hi * sn);
-          st_f(dst + c + 64, hi * cs + lo * sn);
+#pragma unroll
+        for (int k = 0; k < kU; ++k) {
+          const int i = i0 + k * step;
+          lo[k] = i < total ? val(i / per, i % per, 0) : 0.f;
+          hi[k] = (i < total && !is_v) ? val(i / per, i % per + 64, 0) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < kU; ++k) {
+          const int i = i0 + k * step;
+          if (i >= total) continue;
+          const int u = i / per, c = i % per, t = m0 + u;
+          const int pos = meta[u * 3], seq = meta[u * 3 + 1], slot = meta[u * 3 + 2];
+          if (pos < 0 || seq < 0) continue;
+          if (inject && (seq >= e.max_batch || pos >= e.max_ctx)) {
+            set_dev_status(e.status, kDevCheck);
+            continue;
+          }
+          T* dst = is_q ? base + ((size_t)t * e.H + head) * 128
+                        : base + (((size_t)seq * e.Hkv + head) * e.max_ctx + slot) * 128;
+          if (is_v) {
+            st_f(dst + c, lo[k]);
+          } else {
+            st_f(dst + c, lo[k] * cs[k] - hi[k] * sn[k]);
+            st_f(dst + c + 64, hi[k] * cs[k] + lo[k] * sn[k]);
+          }
         }
       }
       break;
