@@ -72,6 +72,11 @@ _SIGS = {
     "dflash_block_attention": ([_I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, ctypes.c_int64, _P], _I),
     "dflash_block_attention_workspace": ([_I, _I, _I, _I, _I], ctypes.c_int64),
     "dflash_block_attention_noalloc": ([_I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P], _I),
+    "dflash_sample_workspace": ([_I, _I], ctypes.c_int64),
+    "dflash_sample_rows": ([_I, _I, _P, _P, _P, _P, ctypes.c_int64, _P], _I),
+    "dflash_spec_accept_workspace": ([_I, _I, _I], ctypes.c_int64),
+    "dflash_spec_accept_sampled": ([_I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int64, _P],
+                                   _I),
     "dflash_profile": ([_P, _I], _I),
     "dflash_debug_trace": ([_P, _P, ctypes.c_int64], _I),
     "dflash_profile_read": ([_P, _I, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double),
@@ -253,6 +258,35 @@ def dflash_block_attention_noalloc(batch, n_heads, n_kv_heads, ctx_len, block, c
                                                _ptr(q), _ptr(k), _ptr(v), _ptr(out), _stream(stream))
     if st != 0:
         raise DFlashError(st, "dflash_block_attention_noalloc")
+
+
+def dflash_sample_workspace(rows, vocab) -> int:
+    return int(load().dflash_sample_workspace(rows, vocab))
+
+
+def dflash_sample_rows(rows, vocab, logits, u, tokens, workspace, stream=None) -> None:
+    """One temperature-1 draw per row of fp32 logits [rows][vocab] (uniforms u [rows])."""
+    nbytes = workspace.numel() * workspace.element_size()
+    st = load().dflash_sample_rows(rows, vocab, _ptr(logits), _ptr(u), _ptr(tokens), _ptr(workspace),
+                                   nbytes, _stream(stream))
+    if st != 0:
+        raise DFlashError(st, "dflash_sample_rows")
+
+
+def dflash_spec_accept_workspace(batch, block, vocab) -> int:
+    return int(load().dflash_spec_accept_workspace(batch, block, vocab))
+
+
+def dflash_spec_accept_sampled(batch, block, vocab, draft_logits, target_logits, tokens, u_accept,
+                               u_resample, accept_len, emitted, workspace, stream=None) -> None:
+    """Temperature-1 acceptance of one block per sequence (speculative rejection rule)."""
+    nbytes = workspace.numel() * workspace.element_size()
+    st = load().dflash_spec_accept_sampled(batch, block, vocab, _ptr(draft_logits), _ptr(target_logits),
+                                           _ptr(tokens), _ptr(u_accept), _ptr(u_resample),
+                                           _ptr(accept_len), _ptr(emitted), _ptr(workspace), nbytes,
+                                           _stream(stream))
+    if st != 0:
+        raise DFlashError(st, "dflash_spec_accept_sampled")
 
 
 def dflash_debug_trace(ctx, dst=None) -> None:

@@ -308,6 +308,58 @@ DFLASH_API dflash_status dflash_block_attention_noalloc(int32_t batch, int32_t n
                                                         const void *v_dev, void *out_dev,
                                                         dflash_stream_t stream);
 
+/* ---- temperature-1 drafting and acceptance ------------------------------------
+ * The pages run DFlash at temperature 1 ("DFlash benchmark results" report: an
+ * average 4.03x) and say the drafter fills the block with sampled tokens and
+ * the target accepts a draft token that matches its argmax "or sits within an
+ * acceptance criterion" ("DFlash speculative decoding" glossary, section
+ * "DFlash: architecture and workflow", stages 2 and 3); the criterion is not
+ * stated.  These calls implement the standard speculative rejection rule,
+ * which keeps the output distributed exactly as sampling the target:
+ *   d_j ~ p_j = softmax(drafter logits of slot j);
+ *   d_j passes when u_j * p_j(d_j) < q_{j-1}(d_j), q_i = softmax(target logits
+ *   of block row i); at the first failure one token is drawn from
+ *   max(0, q_{j-1} - p_j) normalised; if all B-1 pass, from q_{B-1}.
+ * Every draw takes the smallest token id whose cumulative weight, summed in id
+ * order, exceeds u times the total weight.  Uniforms are inputs (u in [0, 1)).
+ * Logits are fp32 row-major; -inf entries have zero weight (a row with no
+ * finite entry has no mass and draws -1).  Sums run in a
+ * fixed order, so equal inputs give equal outputs; a decision within fp32
+ * rounding of a tie may differ from an exact evaluation.
+ * Vocabulary up to 524,288 ids.  Workspaces are caller device memory, 256-byte
+ * aligned, of at least the size the matching *_workspace call returns (which
+ * returns -1 for unsupported sizes); nothing in them needs to start at zero.
+ * All calls only enqueue work on `stream`. */
+
+/* One draw per row from softmax(logits[row]) with uniform u[row]:
+ * logits [rows][vocab] fp32, u [rows], tokens [rows] int32 (outputs).
+ * rows 1..65535.  Returns DFLASH_E_INVALID_ARG on bad sizes, null pointers or
+ * a short / misaligned workspace, DFLASH_E_CUDA if a launch fails. */
+DFLASH_API int64_t dflash_sample_workspace(int32_t rows, int32_t vocab);
+DFLASH_API dflash_status dflash_sample_rows(int32_t rows, int32_t vocab, const float *logits_dev,
+                                            const float *u_dev, int32_t *tokens_dev,
+                                            void *workspace_dev, int64_t workspace_bytes,
+                                            dflash_stream_t stream);
+
+/* One acceptance step for `batch` sequences of block size `block` (1..32,
+ * batch * block <= 65535):
+ *   draft_logits [batch][block][vocab]: row j = the drafter's slot j (row 0
+ *     unused); target_logits [batch][block][vocab]: row i = the target's
+ *     logits at block row i (predicting position P + i + 1);
+ *   tokens [batch][block]: slot 0 the anchor, slot j = d_j;
+ *   u_accept [batch][block] (entry j tests d_j; entry 0 unused);
+ *   u_resample [batch]: the uniform of the final draw.
+ * Outputs: accept_len [batch] = a (accepted draft tokens, 0..block-1) and
+ * emitted [batch] = the token drawn after them (residual or bonus).  A draft
+ * token outside [0, vocab) fails its test.  A residual without mass (q and p
+ * equal up to rounding) draws from q instead.  Errors as dflash_sample_rows. */
+DFLASH_API int64_t dflash_spec_accept_workspace(int32_t batch, int32_t block, int32_t vocab);
+DFLASH_API dflash_status dflash_spec_accept_sampled(
+    int32_t batch, int32_t block, int32_t vocab, const float *draft_logits_dev,
+    const float *target_logits_dev, const int32_t *tokens_dev, const float *u_accept_dev,
+    const float *u_resample_dev, int32_t *accept_len_dev, int32_t *emitted_dev,
+    void *workspace_dev, int64_t workspace_bytes, dflash_stream_t stream);
+
 /* ---- per-kernel timing ------------------------------------------------------
  * enable != 0 starts recording a CUDA event pair around every kernel launch of
  * this context (clearing earlier records); 0 stops recording. */

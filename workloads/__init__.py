@@ -321,5 +321,31 @@ def attn_operand_rows(which: str, n_rows: int, width: int = 128, seed: int = ATT
     return pool_rows(value_pool(seed, 1.0, "bf16"), off, width)
 
 
+SAMPLING_SEED = 4
+
+
+def sampling_inputs(batch: int, block: int, vocab: int, seed: int = SAMPLING_SEED,
+                    spread: float = 3.0, agreement: float = 0.8):
+    """Seeded fp32 logits and uniforms for the temperature-1 acceptance op.
+
+    A shared N(0, spread) score per (sequence, slot, token) plus independent
+    noise for the drafter and the target (the target's row i is paired with
+    the drafter's slot i + 1, the position both predict), so the two
+    distributions agree to a tunable degree.  Returns (draft_logits,
+    target_logits [batch, block, vocab] float32, u_draft, u_accept
+    [batch, block], u_resample [batch]).
+    """
+    rng = np.random.Generator(np.random.PCG64([seed, batch, block, vocab]))
+    base = rng.normal(0.0, spread, (batch, block + 1, vocab))
+    noise = np.sqrt(max(0.0, 1.0 - agreement ** 2)) * spread
+    draft = agreement * base[:, :block] + rng.normal(0.0, noise, (batch, block, vocab))
+    target = agreement * base[:, 1:] + rng.normal(0.0, noise, (batch, block, vocab))
+    u_draft = rng.random((batch, block))
+    u_accept = rng.random((batch, block))
+    u_res = rng.random(batch)
+    return (draft.astype(np.float32), target.astype(np.float32), u_draft.astype(np.float32),
+            u_accept.astype(np.float32), u_res.astype(np.float32))
+
+
 def replace(w: Workload, **kw) -> Workload:
     return dataclasses.replace(w, **kw)
