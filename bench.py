@@ -491,6 +491,78 @@ def run_attn_op(args) -> None:
     print(json.dumps(line))
 
 
+def run_spec_sample_op(args) -> None:
+    """Temperature-1 acceptance op (dflash_spec_accept_sampled) and the draft
+    draws (dflash_sample_rows) on seeded fp32 logits of the Qwen3-8B
+    vocabulary, block 16, batch 1 and 32.  Each timed call reads both
+    [batch, 16, V] logit arrays once (per-chunk stats) and the two rows of
+    each sequence's final draw once more; the inputs exceed L2 at batch 32,
+    and a 256 MB buffer is written before every timed call."""
+    import torch
+
+    from block_diffusion_speculative_injection_gb300 import capi
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    V, B = wl.QWEN3_8B.vocab, 16
+    hbm, _, src = peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    sampler = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    sampler.start()
+    points = []
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        ts = []
+        for _ in range(args.steps):
+            flush.fill_(1)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3)
+        return statistics.median(ts)
+
+    for batch in (1, 32):
+        dl, tl, ud, ua, ur = wl.sampling_inputs(batch, B, V)
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+        dlg, tlg, uag, urg = t(dl), t(tl), t(ua), t(ur)
+        tokens = torch.zeros(batch, B, dtype=torch.int32, device="cuda")
+        acc = torch.zeros(batch, dtype=torch.int32, device="cuda")
+        em = torch.zeros(batch, dtype=torch.int32, device="cuda")
+        ws = torch.empty(capi.dflash_spec_accept_workspace(batch, B, V), dtype=torch.uint8,
+                         device="cuda")
+        rows = batch * B
+        uds = t(ud.reshape(-1))
+        wsd = torch.empty(capi.dflash_sample_workspace(rows, V), dtype=torch.uint8, device="cuda")
+        us_draw = timed(lambda: capi.dflash_sample_rows(rows, V, dlg, uds, tokens, wsd))
+        us_acc = timed(lambda: capi.dflash_spec_accept_sampled(batch, B, V, dlg, tlg, tokens, uag, urg,
+                                                               acc, em, ws))
+        b_draw = rows * V * 4 + batch * B * 4096 * 4      # one pass + one chunk re-read per row
+        b_acc = 2 * rows * V * 4 + 2 * batch * V * 4      # both arrays + the final draw's two rows
+        points.append({"batch": batch, "op": "sample_rows", "us": us_draw, "bytes": b_draw,
+                       "gbs": b_draw / us_draw / 1e3, "frac": b_draw / us_draw / 1e3 / hbm})
+        points.append({"batch": batch, "op": "spec_accept_sampled", "us": us_acc, "bytes": b_acc,
+                       "gbs": b_acc / us_acc / 1e3, "frac": b_acc / us_acc / 1e3 / hbm})
+        del dlg, tlg, ws, wsd
+    clocks = sampler.stop()
+    head = next(p for p in points if p["batch"] == 32 and p["op"] == "spec_accept_sampled")
+    print(json.dumps({
+        "metric": "temperature-1 acceptance op: achieved HBM bandwidth (block 16, vocab 151936)",
+        "value": head["gbs"], "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": head["us"] / 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded logits and uniforms)",
+        "config": {"workload": "spec_sample", "batch": [1, 32], "block": B, "vocab": V,
+                   "l2": "256 MB buffer written before every timed call"},
+        "roofline": {"bound": "hbm", "kernel": "samp_stats_kernel (+ accept, final draw)",
+                     "achieved": head["gbs"], "peak": hbm, "unit": "GB/s", "frac": head["frac"],
+                     "traffic": None, "peak_source": src},
+        "points": points, "clocks": clocks}))
+
+
 def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -499,7 +571,7 @@ def main() -> None:
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="qwen3_8b_b1",
                     choices=["qwen3_8b_b1", "qwen3_8b_b32", "llama31_8b_ddtree_b4", "qwen3_8b_slice_b1",
-                             "qwen3_8b_slice_b32", "attn_op",
+                             "qwen3_8b_slice_b32", "attn_op", "spec_sample",
                              "tiny_f32_e2e",
                              "mini_bf16_e2e"])
     ap.add_argument("--prof-steps", type=int, default=10)
@@ -511,10 +583,10 @@ def main() -> None:
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
-    if args.workload == "attn_op":
+    if args.workload in ("attn_op", "spec_sample"):
         if args.impl == "reference":
-            raise SystemExit("the attention op has no reference arm; its oracle check is in tests/")
-        run_attn_op(args)
+            raise SystemExit("op workloads have no reference arm; their oracle checks are in tests/")
+        (run_attn_op if args.workload == "attn_op" else run_spec_sample_op)(args)
         return
     w = wl.WORKLOADS[args.workload]
     if args.impl == "reference":

@@ -78,12 +78,22 @@ __global__ void __launch_bounds__(kSampThreads) samp_stats_kernel(const float* _
   const int k = blockIdx.x, row = blockIdx.y;
   const float* x = logits + (size_t)row * V;
   const int x0 = k * kChunk, x1 = min(V, x0 + kChunk);
-  MS v = {-INFINITY, 0.f};
-  for (int i = x0 + (int)threadIdx.x; i < x1; i += kSampThreads) {
-    const float xi = x[i];
-    if (xi == -INFINITY) continue;
-    v = ms_merge(v, MS{xi, 1.f});
+  // this thread's ids x0 + e * kSampThreads + tid: all loads first, then the
+  // max, then one exponential per id, summed in e order
+  float xs[kPerThread];
+  float m = -INFINITY;
+#pragma unroll
+  for (int e = 0; e < kPerThread; ++e) {
+    const int i = x0 + e * kSampThreads + (int)threadIdx.x;
+    xs[e] = i < x1 ? x[i] : -INFINITY;
+    m = fmaxf(m, xs[e]);
   }
+  float sum = 0.f;
+  if (m != -INFINITY) {
+#pragma unroll
+    for (int e = 0; e < kPerThread; ++e) sum += expf(xs[e] - m);
+  }
+  const MS v = {m, sum};
   const MS r = block_merge(v);
   if (threadIdx.x == 0) stats[(size_t)row * n_chunks + k] = make_float2(r.m, r.s);
 }
