@@ -190,101 +190,223 @@ __device__ void run_epilogue(const EpiArgs& e, int n0, int m0, int BN) {
 // and applies the epilogue operation.  meta[u] = (position, sequence, slot)
 // of tile row u (QKV / INJECT).
 // ---------------------------------------------------------------------------
-#ifndef DFLASH_EPI_UNROLL
-#define DFLASH_EPI_UNROLL 1
-#endif
-
+// Epilogue straight from tensor memory, for a tile without K splits: the
+// thread of TMEM lane f holds feature n0 + f for 16 token rows per
+// tcgen05.ld; it loads every operand of those 16 rows before using any.
+// QKV / INJECT rotate the pairs (f, f + 64) of a head, which sit in warps w
+// and w ^ 2: each 16-row chunk goes through `xbuf` ([16][128] fp32, shared,
+// followed by 3 x 256 ints of row metadata: 11 KB of the idle stage memory).
 template <typename T>
-__device__ void run_epilogue_cluster(const EpiArgs& e, int n0, int m0, int BN, const float* part,
-                                     const int32_t* meta) {
-  // Every thread takes kU work items per round and issues all of their
-  // loads (global operands, then partials) before using any.
-  constexpr int kU = DFLASH_EPI_UNROLL;
-  const int S = e.splits;
-  const bool two = e.kind == kEpiSwiGLU;
-  const int csize = two ? 2 * S : S;
-  const int rank = (int)cluster_ctarank();
-  const int cn = min(BN, e.M - m0);
-  const uint32_t local = smem_u32(part);
-  // sum over the splits of the partial (gate h = 0 / up h = 1 for SwiGLU) at
-  // tile row u, column c, in split order through distributed shared memory;
-  // a cluster of one CTA reads its own tile with ordinary shared loads
-  const bool alone = S == 1 && !two;
-  auto val = [&](int u, int c, int h) {
-    if (alone) return part[u * 128 + c];
-    const uint32_t addr = local + (uint32_t)((u * 128 + c) * 4);
-    float v = 0.f;
-#pragma unroll
-    for (int s = 0; s < 8; ++s)
-      if (s < S) v += ld_peer_f32(map_peer(addr, (uint32_t)(two ? h + 2 * s : s)));
-    return v;
-  };
-  const int first = rank * (int)blockDim.x + (int)threadIdx.x;
-  const int step = csize * (int)blockDim.x;
+__device__ void run_epilogue_direct(const EpiArgs& e, uint32_t tmem, int n0, int m0, int BN,
+                                    float* xbuf) {
+  const int warp = (int)threadIdx.x >> 5, lane = (int)threadIdx.x & 31;
+  const int f = warp * 32 + lane;
+  const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+  const int M = e.M;
   switch (e.kind) {
     case kEpiResid: {
-      T* cap = static_cast<T*>(e.capture);
-      const int total = cn * 128;
-      for (int i0 = first; i0 < total; i0 += kU * step) {
-        float r[kU], v[kU];
+      float* const resid = e.resid;
+      float* const trace = e.trace;
+      T* const cap = static_cast<T*>(e.capture);
+      const int N = e.N, n_inj = e.n_inject, cap_slot = e.cap_slot, n = n0 + f;
+      for (int c = 0; c < BN; c += 16) {
+        float v[16], r[16];
+        tmem_ld16(taddr + (uint32_t)c, v);
 #pragma unroll
-        for (int k = 0; k < kU; ++k) {
-          const int i = i0 + k * step;
-          r[k] = i < total ? e.resid[(size_t)(m0 + (i >> 7)) * e.N + n0 + (i & 127)] : 0.f;
-        }
+        for (int i = 0; i < 16; ++i) r[i] = (m0 + c + i < M) ? resid[(size_t)(m0 + c + i) * N + n] : 0.f;
 #pragma unroll
-        for (int k = 0; k < kU; ++k) {
-          const int i = i0 + k * step;
-          v[k] = i < total ? val(i >> 7, i & 127, 0) : 0.f;
-        }
-#pragma unroll
-        for (int k = 0; k < kU; ++k) {
-          const int i = i0 + k * step;
-          if (i >= total) continue;
-          const int t = m0 + (i >> 7), n = n0 + (i & 127);
-          const float x = r[k] + v[k];
-          e.resid[(size_t)t * e.N + n] = x;
-          if (cap) st_f(cap + ((size_t)t * e.n_inject + e.cap_slot) * e.N + n, x);
-          if (e.trace) e.trace[(size_t)t * e.N + n] = x;
-        }
-      }
-      break;
-    }
-    case kEpiStore: {
-      const int total = cn * 128;
-      for (int i0 = first; i0 < total; i0 += kU * step) {
-        float v[kU];
-#pragma unroll
-        for (int k = 0; k < kU; ++k) {
-          const int i = i0 + k * step;
-          v[k] = i < total ? val(i >> 7, i & 127, 0) : 0.f;
-        }
-#pragma unroll
-        for (int k = 0; k < kU; ++k) {
-          const int i = i0 + k * step;
-          if (i < total)
-            st_f(static_cast<T*>(e.out) + (size_t)(m0 + (i >> 7)) * e.N + n0 + (i & 127), v[k]);
+        for (int i = 0; i < 16; ++i) {
+          const int t = m0 + c + i;
+          if (t >= M) continue;
+          const float x = r[i] + v[i];
+          resid[(size_t)t * N + n] = x;
+          if (cap) st_f(cap + ((size_t)t * n_inj + cap_slot) * N + n, x);
+          if (trace) trace[(size_t)t * N + n] = x;
         }
       }
       break;
     }
     case kEpiSwiGLU: {
-      const int total = cn * 128;
-      for (int i0 = first; i0 < total; i0 += kU * step) {
-        float g[kU], up[kU];
+      // lanes 0..63: gate of features n0 + f; lanes 64..127: up of n0 + f - 64
+      T* const act = static_cast<T*>(e.act);
+      const int F = e.F;
+      for (int c = 0; c < BN; c += 16) {
+        float v[16];
+        tmem_ld16(taddr + (uint32_t)c, v);
 #pragma unroll
-        for (int k = 0; k < kU; ++k) {
-          const int i = i0 + k * step;
-          g[k] = i < total ? val(i >> 7, i & 127, 0) : 0.f;
-          up[k] = i < total ? val(i >> 7, i & 127, 1) : 0.f;
+        for (int i = 0; i < 16; ++i) xbuf[i * 128 + f] = v[i];
+        __syncthreads();
+        if (f < 64) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int t = m0 + c + i;
+            if (t >= M) continue;
+            const float g = v[i], up = xbuf[i * 128 + f + 64];
+            st_f(act + (size_t)t * F + n0 + f, g / (1.f + __expf(-g)) * up);
+          }
+        }
+        __syncthreads();  // xbuf is rewritten by the next chunk
+      }
+      break;
+    }
+    case kEpiStore: {
+      T* const out = static_cast<T*>(e.out);
+      const int N = e.N, n = n0 + f;
+      for (int c = 0; c < BN; c += 16) {
+        float v[16];
+        tmem_ld16(taddr + (uint32_t)c, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (m0 + c + i < M) st_f(out + (size_t)(m0 + c + i) * N + n, v[i]);
+      }
+      break;
+    }
+    case kEpiQKV:
+    case kEpiInject: {
+      const bool inject = e.kind == kEpiInject;
+      const int H = e.H, Hkv = e.Hkv, max_ctx = e.max_ctx, max_batch = e.max_batch;
+      const int kvd = Hkv * 128;
+      int head, layer = 0;
+      bool is_q = false, is_v = false;
+      if (!inject) {
+        head = n0 / 128;
+        if (head < H) is_q = true;
+        else if (head < H + Hkv) head -= H;
+        else { head -= H + Hkv; is_v = true; }
+      } else {
+        layer = n0 / (2 * kvd);
+        const int o = n0 % (2 * kvd);
+        is_v = o >= kvd;
+        head = (is_v ? o - kvd : o) / 128;
+      }
+      T* base;
+      if (is_q) base = static_cast<T*>(e.q_out);
+      else base = static_cast<T*>(is_v ? e.vc : e.kc) +
+                  (inject ? (size_t)(e.layer0 + layer) * e.layer_elems : 0);
+      const int32_t* const row_pos = e.row_pos;
+      const int32_t* const row_seq = e.row_seq;
+      const int32_t* const row_slot = e.row_slot;
+      const float* const rcos = e.rcos;
+      const float* const rsin = e.rsin;
+      const int j = f & 63;
+      const bool low = f < 64;
+      // the tile's row metadata, read from global memory once, kept in the
+      // (idle) stage memory after xbuf
+      int* const s_pos = reinterpret_cast<int*>(xbuf + 16 * 128);
+      int* const s_seq = s_pos + 256;
+      int* const s_slot = s_seq + 256;
+      for (int u = (int)threadIdx.x; u < BN; u += (int)blockDim.x) {
+        const int t = m0 + u;
+        const int ps = t < M ? row_pos[t] : -1;
+        s_pos[u] = ps;
+        s_seq[u] = t < M ? row_seq[t] : -1;
+        s_slot[u] = t < M ? (inject ? ps : row_slot[t]) : 0;
+      }
+      __syncthreads();
+      // cos/sin of a chunk's rows, loaded one chunk ahead so that their
+      // latency overlaps the previous chunk's exchange and stores
+      float cs[16], sn[16], cs_n[16], sn_n[16];
+      auto load_rope = [&](int c, float* cn, float* snn) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int ps = c + i < BN ? s_pos[c + i] : -1;
+          const bool ok = ps >= 0 && ps < max_ctx;  // the tables hold max_ctx positions
+          cn[i] = ok ? rcos[(size_t)ps * 64 + j] : 1.f;
+          snn[i] = ok ? rsin[(size_t)ps * 64 + j] : 0.f;
+        }
+      };
+      if (!is_v) load_rope(0, cs_n, sn_n);
+      for (int c = 0; c < BN; c += 16) {
+        float v[16];
+        int pos[16], seq[16], slot[16];
+        tmem_ld16(taddr + (uint32_t)c, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          pos[i] = s_pos[c + i];
+          seq[i] = s_seq[c + i];
+          slot[i] = s_slot[c + i];
+        }
+        if (!is_v) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            cs[i] = cs_n[i];
+            sn[i] = sn_n[i];
+          }
+          if (c + 16 < BN) load_rope(c + 16, cs_n, sn_n);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) xbuf[i * 128 + f] = v[i];
+          __syncthreads();
+        }
+        float other[16];
+        if (!is_v) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) other[i] = xbuf[i * 128 + (f ^ 64)];
         }
 #pragma unroll
-        for (int k = 0; k < kU; ++k) {
-          const int i = i0 + k * step;
-          if (i < total)
-            st_f(static_cast<T*>(e.act) + (size_t)(m0 + (i >> 7)) * e.F + n0 + (i & 127),
-                 g[k] / (1.f + __expf(-g[k])) * up[k]);
+        for (int i = 0; i < 16; ++i) {
+          const int t = m0 + c + i;
+          if (t >= M || pos[i] < 0 || seq[i] < 0) continue;
+          if (inject && (seq[i] >= max_batch || pos[i] >= max_ctx)) {
+            set_dev_status(e.status, kDevCheck);
+            continue;
+          }
+          T* dst = is_q ? base + ((size_t)t * H + head) * 128
+                        : base + (((size_t)seq[i] * Hkv + head) * max_ctx + slot[i]) * 128;
+          float y = v[i];
+          if (!is_v) {
+            const float lo = low ? v[i] : other[i], hi = low ? other[i] : v[i];
+            y = low ? lo * cs[i] - hi * sn[i] : hi * cs[i] + lo * sn[i];
+          }
+          st_f(dst + f, y);
         }
+        if (!is_v) __syncthreads();  // xbuf is rewritten by the next chunk
+      }
+      break;
+    }
+    default:
+      break;
+  }
+}
+
+// Epilogue of a tile whose K splits form a thread-block cluster (residual,
+// store, QKV and injection projections): each CTA has its fp32 partial tile
+// in its own shared memory as part[token][feature]; after a cluster barrier,
+// CTA `rank` takes every S-th work item of the tile, sums the partials of all
+// splits in split order through distributed shared memory, and applies the
+// epilogue operation.  meta[u] = (position, sequence, slot) of tile row u.
+template <typename T>
+__device__ void run_epilogue_cluster(const EpiArgs& e, int n0, int m0, int BN, const float* part,
+                                     const int32_t* meta) {
+  const int S = e.splits;
+  const int rank = (int)cluster_ctarank();
+  const int cn = min(BN, e.M - m0);
+  const uint32_t local = smem_u32(part);
+  auto val = [&](int u, int c) {
+    const uint32_t addr = local + (uint32_t)((u * 128 + c) * 4);
+    float v = 0.f;
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+      if (s < S) v += ld_peer_f32(map_peer(addr, (uint32_t)s));
+    return v;
+  };
+  const int first = rank * (int)blockDim.x + (int)threadIdx.x;
+  const int step = S * (int)blockDim.x;
+  switch (e.kind) {
+    case kEpiResid: {
+      T* cap = static_cast<T*>(e.capture);
+      for (int i = first; i < cn * 128; i += step) {
+        const int u = i >> 7, c = i & 127, t = m0 + u, n = n0 + c;
+        const float r = e.resid[(size_t)t * e.N + n] + val(u, c);
+        e.resid[(size_t)t * e.N + n] = r;
+        if (cap) st_f(cap + ((size_t)t * e.n_inject + e.cap_slot) * e.N + n, r);
+        if (e.trace) e.trace[(size_t)t * e.N + n] = r;
+      }
+      break;
+    }
+    case kEpiStore: {
+      for (int i = first; i < cn * 128; i += step) {
+        const int u = i >> 7, c = i & 127;
+        st_f(static_cast<T*>(e.out) + (size_t)(m0 + u) * e.N + n0 + c, val(u, c));
       }
       break;
     }
@@ -310,47 +432,23 @@ __device__ void run_epilogue_cluster(const EpiArgs& e, int n0, int m0, int BN, c
       else base = static_cast<T*>(is_v ? e.vc : e.kc) +
                   (inject ? (size_t)(e.layer0 + layer) * e.layer_elems : 0);
       const int per = is_v ? 128 : 64;
-      const int total = cn * per;
-      for (int i0 = first; i0 < total; i0 += kU * step) {
-        float lo[kU], hi[kU], cs[kU], sn[kU];
-#pragma unroll
-        for (int k = 0; k < kU; ++k) {
-          const int i = i0 + k * step;
-          cs[k] = 1.f;
-          sn[k] = 0.f;
-          if (i < total && !is_v) {
-            const int pos = meta[(i / per) * 3];
-            if (pos >= 0 && pos < e.max_ctx) {  // the tables hold max_ctx positions
-              cs[k] = e.rcos[(size_t)pos * 64 + i % per];
-              sn[k] = e.rsin[(size_t)pos * 64 + i % per];
-            }
-          }
+      for (int i = first; i < cn * per; i += step) {
+        const int u = i / per, c = i % per, t = m0 + u;
+        const int pos = meta[u * 3], seq = meta[u * 3 + 1], slot = meta[u * 3 + 2];
+        if (pos < 0 || seq < 0) continue;
+        if (inject && (seq >= e.max_batch || pos >= e.max_ctx)) {
+          set_dev_status(e.status, kDevCheck);
+          continue;
         }
-#pragma unroll
-        for (int k = 0; k < kU; ++k) {
-          const int i = i0 + k * step;
-          lo[k] = i < total ? val(i / per, i % per, 0) : 0.f;
-          hi[k] = (i < total && !is_v) ? val(i / per, i % per + 64, 0) : 0.f;
-        }
-#pragma unroll
-        for (int k = 0; k < kU; ++k) {
-          const int i = i0 + k * step;
-          if (i >= total) continue;
-          const int u = i / per, c = i % per, t = m0 + u;
-          const int pos = meta[u * 3], seq = meta[u * 3 + 1], slot = meta[u * 3 + 2];
-          if (pos < 0 || seq < 0) continue;
-          if (inject && (seq >= e.max_batch || pos >= e.max_ctx)) {
-            set_dev_status(e.status, kDevCheck);
-            continue;
-          }
-          T* dst = is_q ? base + ((size_t)t * e.H + head) * 128
-                        : base + (((size_t)seq * e.Hkv + head) * e.max_ctx + slot) * 128;
-          if (is_v) {
-            st_f(dst + c, lo[k]);
-          } else {
-            st_f(dst + c, lo[k] * cs[k] - hi[k] * sn[k]);
-            st_f(dst + c + 64, hi[k] * cs[k] + lo[k] * sn[k]);
-          }
+        T* dst = is_q ? base + ((size_t)t * e.H + head) * 128
+                      : base + (((size_t)seq * e.Hkv + head) * e.max_ctx + slot) * 128;
+        if (is_v) {
+          st_f(dst + c, val(u, c));
+        } else {
+          const float lo = val(u, c), hi = val(u, c + 64);
+          const float cs = e.rcos[(size_t)pos * 64 + c], sn = e.rsin[(size_t)pos * 64 + c];
+          st_f(dst + c, lo * cs - hi * sn);
+          st_f(dst + c + 64, hi * cs + lo * sn);
         }
       }
       break;

@@ -52,18 +52,18 @@ __global__ void __launch_bounds__(128, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // SwiGLU clusters pair a gate tile with its up tile: x = 2c + h
-  const int half_tiles = p.epi.F / 128;
-  const int tile_n = p.epi.kind == kEpiSwiGLU
-                         ? ((blockIdx.x & 1) ? (int)(blockIdx.x >> 1) + half_tiles : (int)(blockIdx.x >> 1))
-                         : (int)blockIdx.x;
-  const int n0 = tile_n * 128, m0 = blockIdx.y * BN;
+  // SwiGLU: CTA x takes features f0 = 64 x of both the gate and the up
+  // segment; its 128-row weight tile is gate rows f0..f0+63 over up rows
+  // f0..f0+63 (two 64-row TMA boxes), so SiLU(gate) * up forms in one CTA
+  const bool swiglu = p.epi.kind == kEpiSwiGLU;
+  const int n0 = swiglu ? (int)blockIdx.x * 64 : (int)blockIdx.x * 128, m0 = blockIdx.y * BN;
   const int kb0 = blockIdx.z * p.kb_per_split;
   const int kb1 = min(p.n_kb, kb0 + p.kb_per_split);
   const int nkb = kb1 - kb0;
   int seg = 0;
-  while (seg + 1 < p.n_seg && p.seg_begin[seg + 1] <= n0) ++seg;
-  const int wrow0 = n0 - p.seg_begin[seg];
+  if (!swiglu)
+    while (seg + 1 < p.n_seg && p.seg_begin[seg + 1] <= n0) ++seg;
+  const int wrow0 = swiglu ? n0 : n0 - p.seg_begin[seg];
   const uint32_t tmem_cols = BN <= 32 ? 32u : (BN <= 64 ? 64u : (BN <= 128 ? 128u : 256u));
 
   if (threadIdx.x == 0) {
@@ -87,6 +87,7 @@ __global__ void __launch_bounds__(128, 1)
    if (lane == 0) {
     // TMA producer
     tma_prefetch_desc(&wmaps.m[seg]);
+    if (swiglu) tma_prefetch_desc(&wmaps.m[1]);
     tma_prefetch_desc(&xmap);
     // Weights are never written by an earlier kernel: fill the first stages'
     // weight tiles before waiting on the preceding kernel (programmatic
@@ -96,7 +97,13 @@ __global__ void __launch_bounds__(128, 1)
     const int pre = min(S, nkb);
     for (int i = 0; i < pre; ++i) {
       mbar_arrive_expect_tx(&full[i], a_bytes + b_bytes);
-      tma_load_2d_hint(a_s + i * a_bytes, &wmaps.m[seg], (kb0 + i) * 64, wrow0, &full[i], wpol);
+      if (swiglu) {
+        tma_load_2d_hint(a_s + i * a_bytes, &wmaps.m[0], (kb0 + i) * 64, wrow0, &full[i], wpol);
+        tma_load_2d_hint(a_s + i * a_bytes + a_bytes / 2, &wmaps.m[1], (kb0 + i) * 64, wrow0,
+                         &full[i], wpol);
+      } else {
+        tma_load_2d_hint(a_s + i * a_bytes, &wmaps.m[seg], (kb0 + i) * 64, wrow0, &full[i], wpol);
+      }
     }
     pdl_wait();
     for (int i = 0; i < pre; ++i)
@@ -108,7 +115,12 @@ __global__ void __launch_bounds__(128, 1)
       if (!mbar_wait(&empty[s], ph ^ 1u, p.status)) break;
       mbar_arrive_expect_tx(&full[s], a_bytes + b_bytes);
       const int kx = (kb0 + i) * 64;
-      tma_load_2d_hint(a_s + s * a_bytes, &wmaps.m[seg], kx, wrow0, &full[s], wpol);
+      if (swiglu) {
+        tma_load_2d_hint(a_s + s * a_bytes, &wmaps.m[0], kx, wrow0, &full[s], wpol);
+        tma_load_2d_hint(a_s + s * a_bytes + a_bytes / 2, &wmaps.m[1], kx, wrow0, &full[s], wpol);
+      } else {
+        tma_load_2d_hint(a_s + s * a_bytes, &wmaps.m[seg], kx, wrow0, &full[s], wpol);
+      }
       tma_load_2d(b_s + s * b_bytes, &xmap, kx, m0, &full[s]);
       ++issued;
     }
@@ -161,6 +173,13 @@ __global__ void __launch_bounds__(128, 1)
     if (warp == 1) tmem_dealloc(tmem, tmem_cols);
     return;
   }
+  if (p.epi.splits == 1) {  // no K split: straight from TMEM
+    run_epilogue_direct<bf16>(p.epi, tmem, n0, m0, BN, reinterpret_cast<float*>(smem));
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, tmem_cols);
+    return;
+  }
 
   // fused epilogue over the cluster of K splits: partial tile -> own smem
   // (the pipeline buffers are idle now), then a cluster-wide reduction
@@ -188,8 +207,7 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, tmem_cols);
   cluster_sync();
-  const int n0_epi = p.epi.kind == kEpiSwiGLU ? (int)(blockIdx.x >> 1) * 128 : n0;
-  run_epilogue_cluster<bf16>(p.epi, n0_epi, m0, BN, part, s_meta);
+  run_epilogue_cluster<bf16>(p.epi, n0, m0, BN, part, s_meta);
   cluster_sync();  // peers may still be reading this CTA's partial tile
 }
 
@@ -354,9 +372,13 @@ static TcPlan plan_tc(dflash_ctx* ctx, int M, int N, int K, int kind, int max_sp
   const int per_sm = (t.BN <= 32) ? 2 : 1;
   const int slots = per_sm * ctx->sm_count;
   int splits = ctas >= slots ? 1 : slots / ctas;
+  // wide token tiles (one CTA per SM) take the whole K range: their epilogue
+  // then runs straight from tensor memory instead of reducing through the
+  // cluster, which costs more than the parallelism splits add
+  if (t.BN > 32) splits = 1;
   // the K splits of a tile form one thread-block cluster (portable size <= 8;
   // a SwiGLU cluster also holds the matching up tile)
-  const int max_cluster_splits = kind == kEpiSwiGLU ? 4 : 8;
+  const int max_cluster_splits = kind == kEpiSwiGLU ? 1 : 8;  // SwiGLU: direct epilogue only
   if (splits > max_cluster_splits) splits = max_cluster_splits;
   if (splits > max_splits) splits = max_splits;
   if (splits > t.n_kb / 4) splits = t.n_kb / 4;
@@ -435,8 +457,9 @@ dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs&
     set_error(ctx, "GEMM output %dx%d exceeds workspace", M, N);
     return DFLASH_E_CAPACITY;
   }
-  if (epi_in.kind == kEpiSwiGLU && (N % 256 != 0 || epi_in.F * 2 != N)) {
-    set_error(ctx, "SwiGLU GEMM needs gate and up segments of F %% 128 == 0 rows");
+  if (epi_in.kind == kEpiSwiGLU &&
+      (segs.n != 2 || segs.rows[0] != epi_in.F || segs.rows[1] != epi_in.F || epi_in.F % 64 != 0)) {
+    set_error(ctx, "SwiGLU GEMM needs gate and up segments of F %% 64 == 0 rows each");
     return DFLASH_E_UNSUPPORTED;
   }
 
@@ -447,7 +470,8 @@ dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs&
   p.seg_begin[0] = 0;
   for (int i = 0; i < segs.n; ++i) {
     const CUtensorMap* m = nullptr;
-    DF_TRY(get_tmap(ctx, segs.w[i], segs.rows[i], K, 128, &m));
+    // SwiGLU: 64-row boxes (gate rows over up rows in one 128-row tile)
+    DF_TRY(get_tmap(ctx, segs.w[i], segs.rows[i], K, epi_in.kind == kEpiSwiGLU ? 64 : 128, &m));
     maps.m[i] = *m;
     p.seg_begin[i + 1] = p.seg_begin[i] + segs.rows[i];
   }
@@ -475,7 +499,7 @@ dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs&
   DF_CUDA_TRY(ctx, ensure_tc_smem());
   dim3 grid(n_tiles, m_tiles, splits);
   const size_t smem_bytes = tc_smem_bytes(BN, stages);
-  const dim3 cluster(epi_in.kind == kEpiSwiGLU ? 2 : 1, 1, splits);
+  const dim3 cluster(1, 1, splits);
   DF_CUDA_TRY(ctx, launch_k_cluster(ctx->pdl, cluster, gemm_tc_kernel, grid, dim3(128), smem_bytes,
                                     st, maps, *xm, p));
   DF_LAUNCHED(ctx);
