@@ -422,7 +422,7 @@ def run_ours(args, w: wl.Workload) -> None:
     eng.close()
 
 
-KERNEL_REV = "gemm-v3"
+KERNEL_REV = "gemm-v4"
 
 
 def run_attn_op(args) -> None:
