@@ -389,19 +389,25 @@ __global__ void attn_combine_kernel(const AttnK p) {
   const int S = p.n_splits;
   const size_t stride = (size_t)p.rows_total * p.H;  // (row, head) units between splits
   const size_t base = (size_t)row * p.H + h;
-  for (int s = d; s < S; s += blockDim.x) sw[s] = p.part_ml[(base + s * stride) * 2];
-  __syncthreads();
-  if (d == 0) {
-    float m = -INFINITY;
-    for (int s = 0; s < S; ++s) m = fmaxf(m, sw[s]);
-    if (m == -INFINITY) m = 0.f;
+  // split weights in warp 0: lane s takes splits s, s + 32, ...; max and
+  // weighted sum by butterflies in a fixed order
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    float mx = -INFINITY;
+    for (int s = lane; s < S; s += 32) mx = fmaxf(mx, p.part_ml[(base + s * stride) * 2]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (mx == -INFINITY) mx = 0.f;
     float l = 0.f;
-    for (int s = 0; s < S; ++s) {
-      const float w = exp2f(sw[s] - m);
+    for (int s = lane; s < S; s += 32) {
+      const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + (base + s * stride) * 2);
+      const float w = exp2f(ml.x - mx);
       sw[s] = w;
-      l += w * p.part_ml[(base + s * stride) * 2 + 1];
+      l += w * ml.y;
     }
-    s_inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+    if (lane == 0) s_inv = l > 0.f ? 1.f / l : 0.f;
   }
   __syncthreads();
   float acc = 0.f;
