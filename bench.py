@@ -529,20 +529,20 @@ def run_spec_sample_op(args) -> None:
     for batch in (1, 32):
         dl, tl, ud, ua, ur = wl.sampling_inputs(batch, B, V)
         t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
-        dlg, tlg, uag, urg = t(dl), t(tl), t(ua), t(ur)
+        dlg, tlg, uag, urg = t(dl[:, 1:]), t(tl), t(ua), t(ur)  # drafter slots 1..B-1
         tokens = torch.zeros(batch, B, dtype=torch.int32, device="cuda")
         acc = torch.zeros(batch, dtype=torch.int32, device="cuda")
         em = torch.zeros(batch, dtype=torch.int32, device="cuda")
         ws = torch.empty(capi.dflash_spec_accept_workspace(batch, B, V), dtype=torch.uint8,
                          device="cuda")
-        rows = batch * B
-        uds = t(ud.reshape(-1))
+        rows = batch * (B - 1)
+        uds = t(ud[:, 1:].reshape(-1))
         wsd = torch.empty(capi.dflash_sample_workspace(rows, V), dtype=torch.uint8, device="cuda")
         us_draw = timed(lambda: capi.dflash_sample_rows(rows, V, dlg, uds, tokens, wsd))
         us_acc = timed(lambda: capi.dflash_spec_accept_sampled(batch, B, V, dlg, tlg, tokens, uag, urg,
                                                                acc, em, ws))
-        b_draw = rows * V * 4 + batch * B * 4096 * 4      # one pass + one chunk re-read per row
-        b_acc = 2 * rows * V * 4 + 2 * batch * V * 4      # both arrays + the final draw's two rows
+        b_draw = rows * V * 4 + rows * 4096 * 4           # one pass + one chunk re-read per row
+        b_acc = (rows + batch * B) * V * 4 + 2 * batch * V * 4  # both arrays + the final draw's rows
         points.append({"batch": batch, "op": "sample_rows", "us": us_draw, "bytes": b_draw,
                        "gbs": b_draw / us_draw / 1e3, "frac": b_draw / us_draw / 1e3 / hbm})
         points.append({"batch": batch, "op": "spec_accept_sampled", "us": us_acc, "bytes": b_acc,

@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(PKG, "libdflash.so")
 HEADER = os.path.join(os.path.dirname(PKG), "include", "dflash.h")
 
 DFLASH_F32, DFLASH_BF16, DFLASH_I32 = 0, 1, 2
-DFLASH_ACCEPT_GREEDY, DFLASH_ACCEPT_ALL = 0, 1
+DFLASH_ACCEPT_GREEDY, DFLASH_ACCEPT_ALL, DFLASH_ACCEPT_GIVEN = 0, 1, 2
 DFLASH_VERIFY_LAST_ONLY = 1
 
 STATUS = {0: "OK", 1: "INVALID_ARG", 2: "CAPACITY", 3: "OOM", 4: "CUDA", 5: "DEVICE_CHECK",

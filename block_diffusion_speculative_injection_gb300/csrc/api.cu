@@ -578,7 +578,7 @@ dflash_status dflash_accept_commit(dflash_ctx* ctx, int32_t batch, const int32_t
   if (!ctx) return DFLASH_E_INVALID_ARG;
   if (!argmax_dev || !accept_len_dev || !next_anchor_dev || !emitted_dev)
     return fail(ctx, DFLASH_E_INVALID_ARG, "null pointer argument");
-  if (mode != DFLASH_ACCEPT_GREEDY && mode != DFLASH_ACCEPT_ALL)
+  if (mode != DFLASH_ACCEPT_GREEDY && mode != DFLASH_ACCEPT_ALL && mode != DFLASH_ACCEPT_GIVEN)
     return fail(ctx, DFLASH_E_INVALID_ARG, "unknown accept mode %d", mode);
   if (ctx->last_kind == kPassNone)
     return fail(ctx, DFLASH_E_STATE, "accept_commit without a preceding verify");
@@ -593,8 +593,8 @@ dflash_status dflash_accept_commit(dflash_ctx* ctx, int32_t batch, const int32_t
                               next_anchor_dev, emitted_dev, st));
   } else {
     if (tree) return fail(ctx, DFLASH_E_INVALID_ARG, "last pass was linear, tree given");
-    if (mode == DFLASH_ACCEPT_GREEDY && !block_dev)
-      return fail(ctx, DFLASH_E_INVALID_ARG, "greedy accept needs the block tokens");
+    if (mode != DFLASH_ACCEPT_ALL && !block_dev)
+      return fail(ctx, DFLASH_E_INVALID_ARG, "block accept needs the block tokens");
     DF_TRY(launch_accept_linear(ctx, batch, seq_ids_dev, block_dev, argmax_dev, ctx->last_q, mode,
                                 accept_len_dev, next_anchor_dev, emitted_dev, st));
   }

@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(32)
   float lse_t = 0.f, lse_d = 0.f;
   if (j >= 1 && j < B) {
     const int d = tokens[b * B + j];
-    const size_t drow = (size_t)b * B + j, trow = (size_t)b * B + j - 1;
+    const size_t drow = (size_t)b * (B - 1) + j - 1, trow = (size_t)b * B + j - 1;
     lse_d = row_lse(dstats + drow * n_chunks, n_chunks);
     lse_t = row_lse(tstats + trow * n_chunks, n_chunks);
     if (d >= 0 && d < V) {
@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(32)
       accept_len[b] = jf - 1;
       s.mode = 1;
       s.trow = b * B + jf - 1;
-      s.drow = b * B + jf;
+      s.drow = b * (B - 1) + jf - 1;
       s.lse_t = lt;
       s.lse_d = ld;
     } else {  // all passed: bonus from q_{B-1}
@@ -387,7 +387,7 @@ int64_t dflash_spec_accept_workspace(int32_t batch, int32_t block, int32_t vocab
   const int64_t nc = sample_chunks(vocab);
   const int64_t stats = align256((int64_t)batch * block * nc * (int64_t)sizeof(float2));
   return 2 * stats + align256((int64_t)batch * (int64_t)sizeof(SeqDraw)) +
-         align256((int64_t)batch * nc * (int64_t)sizeof(float));
+         align256((int64_t)batch * nc * (int64_t)sizeof(float));  // draft stats fit in `stats`
 }
 
 dflash_status dflash_spec_accept_sampled(int32_t batch, int32_t block, int32_t vocab,
@@ -397,8 +397,8 @@ dflash_status dflash_spec_accept_sampled(int32_t batch, int32_t block, int32_t v
                                          int32_t* emitted, void* workspace,
                                          int64_t workspace_bytes, dflash_stream_t stream) {
   const int64_t need = dflash_spec_accept_workspace(batch, block, vocab);
-  if (need < 0 || !draft_logits || !target_logits || !tokens || !u_accept || !u_resample ||
-      !accept_len || !emitted || !workspace)
+  if (need < 0 || (block > 1 && !draft_logits) || !target_logits || !tokens || !u_accept ||
+      !u_resample || !accept_len || !emitted || !workspace)
     return DFLASH_E_INVALID_ARG;
   if (workspace_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
     return DFLASH_E_INVALID_ARG;
@@ -412,8 +412,9 @@ dflash_status dflash_spec_accept_sampled(int32_t batch, int32_t block, int32_t v
   float* mass = reinterpret_cast<float*>(w + 2 * stats_bytes +
                                          align256((int64_t)batch * (int64_t)sizeof(SeqDraw)));
   cudaStream_t st = (cudaStream_t)stream;
-  if (launch_k(true, samp_stats_kernel, dim3(nc, rows), dim3(kSampThreads), 0, st, draft_logits,
-               vocab, nc, dstats) != cudaSuccess ||
+  if ((block > 1 &&
+       launch_k(true, samp_stats_kernel, dim3(nc, batch * (block - 1)), dim3(kSampThreads), 0, st,
+                draft_logits, vocab, nc, dstats) != cudaSuccess) ||
       launch_k(true, samp_stats_kernel, dim3(nc, rows), dim3(kSampThreads), 0, st, target_logits,
                vocab, nc, tstats) != cudaSuccess ||
       launch_k(true, samp_accept_kernel, dim3(batch), dim3(32), 0, st, draft_logits,

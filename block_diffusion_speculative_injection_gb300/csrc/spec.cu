@@ -49,9 +49,14 @@ __global__ void accept_linear_kernel(int batch, int q, int mode, const int32_t* 
     emitted[base] = y;
     for (int j = 1; j < q; ++j) emitted[base + j] = -1;
   } else {
-    int a = 0;
-    while (a < n - 1 && block[base + 1 + a] == argmax[base + a]) ++a;
-    const int y = argmax[base + a];
+    int a = 0, y;
+    if (mode == DFLASH_ACCEPT_GIVEN) {  // decided by the caller's sampling step
+      a = min(max(accept_len[b], 0), n - 1);
+      y = next_anchor[b];
+    } else {
+      while (a < n - 1 && block[base + 1 + a] == argmax[base + a]) ++a;
+      y = argmax[base + a];
+    }
     for (int j = 0; j < a; ++j) emitted[base + j] = block[base + 1 + j];
     emitted[base + a] = y;
     for (int j = a + 1; j < q; ++j) emitted[base + j] = -1;

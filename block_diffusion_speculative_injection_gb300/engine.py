@@ -209,6 +209,48 @@ class DFlashEngine:
             return out, dlog.view(b, max(B - 1, 1), -1), vlog.view(b, B, -1), margin.view(b, B)
         return out
 
+    # -- one temperature-1 DFlash step -----------------------------------------
+    def sample_step(self, seq_ids: torch.Tensor, anchors: torch.Tensor, u_draft: torch.Tensor,
+                    u_accept: torch.Tensor, u_resample: torch.Tensor):
+        """Draft block -> draft tokens drawn from the drafter's softmax (u_draft
+        [b][B-1]) -> verify -> speculative rejection test (u_accept [b][B],
+        u_resample [b]) -> commit the accepted prefix and the drawn token ->
+        injection.  Every step runs in the library's kernels; this method only
+        moves device buffers between the calls."""
+        b = seq_ids.numel()
+        B = self.B
+        V = self.shape.vocab
+        if not hasattr(self, "_samp"):
+            rows = self.max_batch * max(B - 1, 1)
+            self._samp = {
+                "dlog": torch.empty(rows * V, dtype=torch.float32, device=self.device),
+                "vlog": torch.empty(self.max_batch * B * V, dtype=torch.float32, device=self.device),
+                "draws": torch.empty(rows, dtype=torch.int32, device=self.device),
+                "ws_draw": torch.empty(max(capi.dflash_sample_workspace(rows, V), 256), dtype=torch.uint8,
+                                       device=self.device),
+                "ws_acc": torch.empty(capi.dflash_spec_accept_workspace(self.max_batch, B, V),
+                                      dtype=torch.uint8, device=self.device),
+            }
+        m = self._samp
+        block = self.block[: b * B]
+        dlog = m["dlog"][: b * max(B - 1, 1) * V]
+        capi.dflash_draft_block(self.ctx, b, seq_ids, anchors, block, 0, None, None, dlog)
+        if B > 1:
+            draws = m["draws"][: b * (B - 1)]
+            capi.dflash_sample_rows(b * (B - 1), V, dlog, u_draft.contiguous(), draws, m["ws_draw"])
+            block.view(b, B)[:, 1:].copy_(draws.view(b, B - 1))
+        vlog = m["vlog"][: b * B * V]
+        argmax = self.argmax[: b * B]
+        capi.dflash_verify(self.ctx, b, seq_ids, block, B, None, 0, argmax, None, vlog)
+        acc, nxt = self.accept_len[:b], self.next_anchor[:b]
+        capi.dflash_spec_accept_sampled(b, B, V, dlog, vlog, block, u_accept.contiguous(),
+                                        u_resample.contiguous(), acc, nxt, m["ws_acc"])
+        emitted = self.emitted[: b * B]
+        capi.dflash_accept_commit(self.ctx, b, seq_ids, block, block, None, capi.DFLASH_ACCEPT_GIVEN,
+                                  acc, nxt, emitted)
+        capi.dflash_inject_kv(self.ctx)
+        return StepOut(block.view(b, B), argmax.view(b, B), acc, nxt, emitted.view(b, B))
+
     def ar_step(self, seq_ids: torch.Tensor, anchors: torch.Tensor):
         """Plain greedy decoding step: verify the anchor alone, commit it."""
         b = seq_ids.numel()

@@ -104,7 +104,9 @@ typedef struct {
 /* Accept modes of dflash_accept_commit. */
 enum {
   DFLASH_ACCEPT_GREEDY = 0,  /* longest matching prefix + bonus (block) or tree walk */
-  DFLASH_ACCEPT_ALL = 1      /* commit every row of the pass (prompt prefill) */
+  DFLASH_ACCEPT_ALL = 1,     /* commit every row of the pass (prompt prefill) */
+  DFLASH_ACCEPT_GIVEN = 2    /* accept length and emitted token decided by the caller
+                                (temperature-1 acceptance, dflash_spec_accept_sampled) */
 };
 
 /* Flags of dflash_verify. */
@@ -180,6 +182,11 @@ DFLASH_API dflash_status dflash_draft_block(dflash_ctx *ctx, int32_t batch, cons
  *   argmax at the last node.
  * ALL (prefill): every row j < q_len is committed; accept_len[b] = q_len;
  *   next_anchor[b] = emitted[b][0] = argmax of the last row.
+ * GIVEN, linear block only: accept_len_dev[b] and next_anchor_dev[b] are
+ *   READ as a (clamped to 0..q_len-1) and the token emitted after d_1..d_a
+ *   (e.g. dflash_spec_accept_sampled's outputs) and left unchanged;
+ *   emitted[b] = d_1..d_a, that token; argmax_dev is not read (may be the
+ *   block itself); the committed length grows by a + 1 as in GREEDY.
  * In every mode the committed rows are queued for dflash_inject_kv.
  *   block_dev  [batch][q] (linear) -- the verified tokens; ignored for trees
  *   argmax_dev [batch][q] from the verify call
@@ -343,9 +350,10 @@ DFLASH_API dflash_status dflash_sample_rows(int32_t rows, int32_t vocab, const f
 
 /* One acceptance step for `batch` sequences of block size `block` (1..32,
  * batch * block <= 65535):
- *   draft_logits [batch][block][vocab]: row j = the drafter's slot j (row 0
- *     unused); target_logits [batch][block][vocab]: row i = the target's
- *     logits at block row i (predicting position P + i + 1);
+ *   draft_logits [batch][block-1][vocab]: row j-1 = the drafter's slot j (the
+ *     layout dflash_draft_block returns; unused when block == 1);
+ *     target_logits [batch][block][vocab]: row i = the target's logits at
+ *     block row i (predicting position P + i + 1);
  *   tokens [batch][block]: slot 0 the anchor, slot j = d_j;
  *   u_accept [batch][block] (entry j tests d_j; entry 0 unused);
  *   u_resample [batch]: the uniform of the final draw.

@@ -84,7 +84,7 @@ def _run_accept(batch, block, V, agreement):
     em = torch.full((batch,), -7, dtype=torch.int32, device="cuda")
     ws = torch.empty(capi.dflash_spec_accept_workspace(batch, block, V), dtype=torch.uint8,
                      device="cuda")
-    capi.dflash_spec_accept_sampled(batch, block, V, t(dl), t(tl), t(tokens), t(ua), t(ur), acc, em, ws)
+    capi.dflash_spec_accept_sampled(batch, block, V, t(dl[:, 1:]), t(tl), t(tokens), t(ua), t(ur), acc, em, ws)
     torch.cuda.synchronize()
     return dl, tl, tokens, ua, ur, acc.cpu().numpy(), em.cpu().numpy()
 
@@ -142,7 +142,7 @@ def test_spec_accept_identical_distributions_accept_all():
     acc = torch.zeros(batch, dtype=torch.int32, device="cuda")
     em = torch.zeros(batch, dtype=torch.int32, device="cuda")
     ws = torch.empty(capi.dflash_spec_accept_workspace(batch, block, V), dtype=torch.uint8, device="cuda")
-    capi.dflash_spec_accept_sampled(batch, block, V, t(dl), t(tl), t(tokens), t(ua), t(ur), acc, em, ws)
+    capi.dflash_spec_accept_sampled(batch, block, V, t(dl[:, 1:]), t(tl), t(tokens), t(ua), t(ur), acc, em, ws)
     torch.cuda.synchronize()
     assert (acc.cpu().numpy() == block - 1).all()
 

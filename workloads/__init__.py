@@ -347,5 +347,15 @@ def sampling_inputs(batch: int, block: int, vocab: int, seed: int = SAMPLING_SEE
             u_accept.astype(np.float32), u_res.astype(np.float32))
 
 
+def step_uniforms(step: int, batch: int, block: int, seed: int = SAMPLING_SEED):
+    """Seeded uniforms of one temperature-1 step: (u_draft [batch, block-1],
+    u_accept [batch, block], u_resample [batch]), float32 in [0, 1)."""
+    rng = np.random.Generator(np.random.PCG64([seed, 7, step]))
+    u_draft = rng.random((batch, max(block - 1, 0))).astype(np.float32)
+    u_accept = rng.random((batch, block)).astype(np.float32)
+    u_res = rng.random(batch).astype(np.float32)
+    return u_draft, u_accept, u_res
+
+
 def replace(w: Workload, **kw) -> Workload:
     return dataclasses.replace(w, **kw)
