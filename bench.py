@@ -563,6 +563,75 @@ def run_spec_sample_op(args) -> None:
         "points": points, "clocks": clocks}))
 
 
+def run_concurrency(args) -> None:
+    """Concurrency sweep of the DFlash step on the Qwen3-8B shape (block 16,
+    2048-token random prompts): for b = 1, 2, 4, 8, 16, 32 sequences, the
+    step time and the plain AR step time (both CUDA-graph replays, CUDA
+    events on the launching stream), verified tokens/s, and the projected
+    speedup S = C_AR * E[L] / C_DF with E[L] from the pages -- the quantity
+    whose decay with concurrency the pages report."""
+    import torch
+
+    from block_diffusion_speculative_injection_gb300 import capi
+    from block_diffusion_speculative_injection_gb300.engine import DFlashEngine, capture_step_graph
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    w = wl.WORKLOADS["qwen3_8b_b1"]
+    B, P = w.block_size, wl.prompt_lengths(w)[0]
+    batches = (1, 2, 4, 8, 16, 32)
+    nb = max(batches)
+    prompts = [wl.prompt_tokens(w, s, P) for s in range(nb)]
+    steps_total = len(batches) * (args.warmup + args.steps) * 2 + 8
+    eng = DFlashEngine(w.shape, B, nb, P + B * steps_total + 64, max_rows=max(P, nb * B), seed=w.seed)
+    eng.prefill(prompts)
+    stream = torch.cuda.current_stream()
+    sampler = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    sampler.start()
+    points = []
+    for b in batches:
+        sid = eng.seq_ids(b)
+        for _ in range(2):
+            eng.step(sid, eng.next_anchor[:b].clone())
+        g = capture_step_graph(eng, sid)
+        ag = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(ag):
+            eng.ar_step(sid, eng.next_anchor[:b])
+
+        def timed(graph):
+            for _ in range(args.warmup):
+                graph.replay()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(args.steps):
+                graph.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / args.steps
+
+        step_ms = timed(g)
+        ar_ms = timed(ag)
+        points.append({"batch": b, "step_ms": step_ms, "ar_step_ms": ar_ms,
+                       "tokens_per_s_tau1": b / (step_ms / 1e3),
+                       "ar_tokens_per_s": b / (ar_ms / 1e3),
+                       "projected_speedup": ar_ms * PAGES_ACCEPT_LEN / step_ms})
+        del g, ag
+    clocks = sampler.stop()
+    eng.close()
+    head = points[-1]
+    print(json.dumps({
+        "metric": "DFlash step over concurrency (Qwen3-8B shape, B=16, prompt 2048): projected speedup at b=32",
+        "value": head["projected_speedup"], "unit": "x", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["step_ms"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded random-init weights, uniform random prompt tokens)",
+        "config": {"workload": "concurrency", "batches": list(batches), "block": B, "prompt_len": P,
+                   "expected_accept_len": PAGES_ACCEPT_LEN,
+                   "l2": "no flush: every step streams ~19 GB of weights"},
+        "points": points, "clocks": clocks}))
+
+
 def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -571,7 +640,7 @@ def main() -> None:
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="qwen3_8b_b1",
                     choices=["qwen3_8b_b1", "qwen3_8b_b32", "llama31_8b_ddtree_b4", "qwen3_8b_slice_b1",
-                             "qwen3_8b_slice_b32", "attn_op", "spec_sample",
+                             "qwen3_8b_slice_b32", "attn_op", "spec_sample", "concurrency",
                              "tiny_f32_e2e",
                              "mini_bf16_e2e"])
     ap.add_argument("--prof-steps", type=int, default=10)
@@ -583,10 +652,11 @@ def main() -> None:
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
-    if args.workload in ("attn_op", "spec_sample"):
+    if args.workload in ("attn_op", "spec_sample", "concurrency"):
         if args.impl == "reference":
-            raise SystemExit("op workloads have no reference arm; their oracle checks are in tests/")
-        (run_attn_op if args.workload == "attn_op" else run_spec_sample_op)(args)
+            raise SystemExit("op and sweep workloads have no reference arm; their oracle checks are in tests/")
+        {"attn_op": run_attn_op, "spec_sample": run_spec_sample_op,
+         "concurrency": run_concurrency}[args.workload](args)
         return
     w = wl.WORKLOADS[args.workload]
     if args.impl == "reference":

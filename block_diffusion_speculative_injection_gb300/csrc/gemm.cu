@@ -372,10 +372,13 @@ static TcPlan plan_tc(dflash_ctx* ctx, int M, int N, int K, int kind, int max_sp
   const int per_sm = (t.BN <= 32) ? 2 : 1;
   const int slots = per_sm * ctx->sm_count;
   int splits = ctas >= slots ? 1 : slots / ctas;
-  // wide token tiles (one CTA per SM) take the whole K range: their epilogue
-  // then runs straight from tensor memory instead of reducing through the
-  // cluster, which costs more than the parallelism splits add
-  if (t.BN > 32) splits = 1;
+  // Tiles wider than 128 token rows take the whole K range when the unsplit
+  // grid already covers a third of the SMs: their epilogue then runs
+  // straight from tensor memory, while a cluster reduction of such a wide
+  // tile costs more than the parallelism it adds.  Measured on the
+  // concurrency sweep (b = 4, 8, 16, 32 at block 16): splitting pays up to
+  // 128 rows, and above that only for grids of a few dozen CTAs.
+  if (t.BN > 128 && 3 * ctas >= ctx->sm_count) splits = 1;
   // the K splits of a tile form one thread-block cluster (portable size <= 8;
   // a SwiGLU cluster also holds the matching up tile)
   const int max_cluster_splits = kind == kEpiSwiGLU ? 1 : 8;  // SwiGLU: direct epilogue only
