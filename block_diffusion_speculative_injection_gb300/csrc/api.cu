@@ -382,8 +382,6 @@ dflash_status dflash_create(const dflash_config* cfg, dflash_ctx** out) {
   alloc((void**)&ctx->inj_seq, sizeof(int32_t) * R);
   alloc((void**)&ctx->inj_pos, sizeof(int32_t) * R);
   alloc((void**)&ctx->path, sizeof(int32_t) * c.max_batch * 34);
-  ctx->n_tile_counters = 1 << 16;
-  alloc((void**)&ctx->tile_counters, sizeof(int32_t) * ctx->n_tile_counters);
   alloc((void**)&ctx->rope_cos, sizeof(float) * ctx->rope_len * (c.head_dim / 2));
   alloc((void**)&ctx->rope_sin, sizeof(float) * ctx->rope_len * (c.head_dim / 2));
   DraftMeta dm{nullptr, nullptr, nullptr};
@@ -404,7 +402,6 @@ dflash_status dflash_create(const dflash_config* cfg, dflash_ctx** out) {
              cudaMemset(ctx->dvc, 0, cache_layer_bytes * c.n_draft_layers) == cudaSuccess &&
              cudaMemset(ctx->seq_len, 0, sizeof(int32_t) * c.max_batch) == cudaSuccess &&
              cudaMemset(ctx->gen_count, 0, sizeof(int32_t) * c.max_batch) == cudaSuccess &&
-             cudaMemset(ctx->tile_counters, 0, sizeof(int32_t) * ctx->n_tile_counters) == cudaSuccess &&
              cudaMemset(ctx->dev_status, 0, sizeof(int32_t) * 4) == cudaSuccess &&
              cudaMemset(ctx->inj_seq, 0xFF, sizeof(int32_t) * R) == cudaSuccess &&
              cudaMemset(ctx->capture, 0, R * c.n_inject * d * es) == cudaSuccess &&
@@ -437,8 +434,7 @@ void dflash_destroy(dflash_ctx* ctx) {
                   ctx->ao,      ctx->act,        ctx->fb,      ctx->lm_in,   ctx->ws,
                   ctx->part_o,  ctx->part_ml,    ctx->vk_part, ctx->vv_part, ctx->pass_seq,
                   ctx->row_pos, ctx->row_slot,   ctx->row_seq, ctx->lm_rows, ctx->inj_seq,
-                  ctx->inj_pos, ctx->path,       ctx->rope_cos, ctx->rope_sin,
-                  ctx->tile_counters};
+                  ctx->inj_pos, ctx->path,       ctx->rope_cos, ctx->rope_sin};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   for (cudaEvent_t e : ctx->prof_ev) cudaEventDestroy(e);

@@ -120,8 +120,6 @@ struct dflash_ctx {
   int last_batch = 0, last_q = 0;
   int pending_rows = 0;  // rows of the injection queue (capture rows)
 
-  int32_t* tile_counters = nullptr;  // GEMM split-K completion tickets (self-resetting)
-  size_t n_tile_counters = 0;
 
   float* trace = nullptr;  // debug: residual after every target layer [L][max_rows][d]
   bool pdl = true;  // programmatic dependent launch between this context's kernels
