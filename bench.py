@@ -186,6 +186,20 @@ def cpu_cores() -> int:
         return os.cpu_count() or 1
 
 
+def reduce_over_ranks(ms: float, emitted: int, world: int):
+    """Whole-job timing of N independent replicas: the slowest rank's timed
+    region and the tokens all ranks emitted (rank-local values when N = 1)."""
+    if world <= 1:
+        return ms, emitted
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    n = torch.tensor([emitted], dtype=torch.float64)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(n.item())
+
+
 def run_reference(args, w: wl.Workload) -> None:
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -296,15 +310,7 @@ def run_ours(args, w: wl.Workload) -> None:
     ms = ev0.elapsed_time(ev1)
     anchors = eng.next_anchor[:b].clone()
     emitted = int((gen - g0)[:b].sum().item())
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-        n = torch.tensor([emitted], dtype=torch.float64)
-        dist.all_reduce(n, op=dist.ReduceOp.SUM)
-        emitted_all = int(n.item())
-    else:
-        emitted_all = emitted
+    ms, emitted_all = reduce_over_ranks(ms, emitted, world)
     value = emitted_all / (ms / 1e3)
     step_ms = ms / args.steps
     tau = emitted / (args.steps * b)
