@@ -72,6 +72,7 @@ _SIGS = {
     "dflash_block_attention": ([_I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, ctypes.c_int64, _P], _I),
     "dflash_block_attention_workspace": ([_I, _I, _I, _I, _I], ctypes.c_int64),
     "dflash_block_attention_noalloc": ([_I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P], _I),
+    "dflash_debug_wait_timeout": ([_P, _P], _I),
     "dflash_sample_workspace": ([_I, _I], ctypes.c_int64),
     "dflash_sample_rows": ([_I, _I, _P, _P, _P, _P, ctypes.c_int64, _P], _I),
     "dflash_spec_accept_workspace": ([_I, _I, _I], ctypes.c_int64),
@@ -258,6 +259,13 @@ def dflash_block_attention_noalloc(batch, n_heads, n_kv_heads, ctx_len, block, c
                                                _ptr(q), _ptr(k), _ptr(v), _ptr(out), _stream(stream))
     if st != 0:
         raise DFlashError(st, "dflash_block_attention_noalloc")
+
+
+def dflash_debug_wait_timeout(ctx, stream=None) -> None:
+    """Runs a bounded wait that expires (about 2 s) and records a timeout."""
+    st = load().dflash_debug_wait_timeout(ctx, _stream(stream))
+    if st != 0:
+        raise DFlashError(st, "dflash_debug_wait_timeout")
 
 
 def dflash_sample_workspace(rows, vocab) -> int:

@@ -88,10 +88,12 @@ __global__ void __launch_bounds__(kSampThreads) samp_stats_kernel(const float* _
     xs[e] = i < x1 ? x[i] : -INFINITY;
     m = fmaxf(m, xs[e]);
   }
+  // exp(x - m) = 2^((x - m) log2 e)
+  constexpr float kLog2e = 1.4426950408889634f;
   float sum = 0.f;
   if (m != -INFINITY) {
 #pragma unroll
-    for (int e = 0; e < kPerThread; ++e) sum += expf(xs[e] - m);
+    for (int e = 0; e < kPerThread; ++e) sum += exp2f((xs[e] - m) * kLog2e);
   }
   const MS v = {m, sum};
   const MS r = block_merge(v);

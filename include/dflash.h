@@ -368,6 +368,15 @@ DFLASH_API dflash_status dflash_spec_accept_sampled(
     const float *u_resample_dev, int32_t *accept_len_dev, int32_t *emitted_dev,
     void *workspace_dev, int64_t workspace_bytes, dflash_stream_t stream);
 
+/* ---- failure-path diagnostic --------------------------------------------------
+ * Enqueues one kernel that waits, with the same bounded wait every pipelined
+ * kernel of the library uses, on a barrier that nothing completes.  The wait
+ * gives up after about 2 seconds and records a timeout in the context's
+ * sticky status word, so the next dflash_check returns DFLASH_E_TIMEOUT
+ * (and clears it); the context stays usable.  The pages have no counterpart:
+ * this exists to test the library's failure handling. */
+DFLASH_API dflash_status dflash_debug_wait_timeout(dflash_ctx *ctx, dflash_stream_t stream);
+
 /* ---- per-kernel timing ------------------------------------------------------
  * enable != 0 starts recording a CUDA event pair around every kernel launch of
  * this context (clearing earlier records); 0 stops recording. */

@@ -129,3 +129,22 @@ def test_capacity_overflow_sets_device_status(engine_mod):
     assert e.value.status == 2
     assert eng.argmax[:32].cpu().tolist() == [-1] * 32
     eng.close()
+
+
+def test_expired_device_wait_is_reported_and_context_survives(engine_mod):
+    """A bounded device wait that runs out (a barrier nothing completes)
+    records DFLASH_E_TIMEOUT in the sticky status; the context then runs a
+    normal step and checks clean."""
+    from block_diffusion_speculative_injection_gb300 import capi
+    w = wl.WORKLOADS["tiny_f32_e2e"]
+    eng = engine_mod.DFlashEngine(w.shape, w.block_size, 1, 256, max_rows=128)
+    anchors = eng.prefill([wl.prompts(w)[0]])
+    capi.dflash_check(eng.ctx)
+    capi.dflash_debug_wait_timeout(eng.ctx)
+    with pytest.raises(capi.DFlashError) as e:
+        capi.dflash_check(eng.ctx)
+    assert e.value.status == 6  # DFLASH_E_TIMEOUT
+    out = eng.step(eng.seq_ids(1), anchors)
+    capi.dflash_check(eng.ctx)
+    assert int(out.accept_len[0]) >= 0
+    eng.close()
