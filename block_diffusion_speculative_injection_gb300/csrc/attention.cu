@@ -320,17 +320,27 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const AttnK p) {
       split_bf16(s[2 * c][2], s[2 * c][3], a[1], alo[1]);
       split_bf16(s[2 * c + 1][0], s[2 * c + 1][1], a[2], alo[2]);
       split_bf16(s[2 * c + 1][2], s[2 * c + 1][3], a[3], alo[3]);
+      // two column pairs at a time: the four high-part MMAs, then the four
+      // residual MMAs into the same accumulators, four MMAs apart
 #pragma unroll
-      for (int np = 0; np < 8; ++np) {
+      for (int np = 0; np < 8; np += 2) {
         const int mi = lane >> 3;
         const int r = c * 16 + (mi & 1) * 8 + (lane & 7);
-        const int cc = 2 * np + (mi >> 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(smem_u32(vs + swz(r, cc)), b0, b1, b2, b3);
-        mma_bf16(o[2 * np], a, b0, b1);
-        mma_bf16(o[2 * np + 1], a, b2, b3);
-        mma_bf16(o[2 * np], alo, b0, b1);
-        mma_bf16(o[2 * np + 1], alo, b2, b3);
+        uint32_t b[2][4];
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          ldsm_x4_t(smem_u32(vs + swz(r, 2 * (np + h) + (mi >> 1))), b[h][0], b[h][1], b[h][2],
+                    b[h][3]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          mma_bf16(o[2 * (np + h)], a, b[h][0], b[h][1]);
+          mma_bf16(o[2 * (np + h) + 1], a, b[h][2], b[h][3]);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          mma_bf16(o[2 * (np + h)], alo, b[h][0], b[h][1]);
+          mma_bf16(o[2 * (np + h) + 1], alo, b[h][2], b[h][3]);
+        }
       }
     }
     __syncthreads();
