@@ -82,6 +82,9 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // let the next kernel launch now: its CTAs take free slots and wait for
+  // this grid's completion before they read anything it writes
+  pdl_trigger();
 
   if (warp == 0) {
    if (lane == 0) {
@@ -153,7 +156,6 @@ __global__ void __launch_bounds__(128, 1)
   // epilogue: TMEM lane = weight row (output feature), column = token row.
   // Every thread orders itself after the preceding kernel before writing.
   pdl_wait();
-  pdl_trigger();
   mbar_wait_sleep(accum, 0, p.status);
   __syncwarp();
   tc_fence_after();
