@@ -190,6 +190,51 @@ def test_zero_branch_weights_leave_residual_unchanged(tiny_w, tiny_prompt):
     np.testing.assert_allclose(logits, ref, rtol=1e-12, atol=1e-12)
 
 
+@pytest.mark.parametrize("name", ["tiny_f32_e2e", "mini_bf16_e2e"])  # MHA, and GQA 8 / 2
+def test_attention_branch_with_zero_scores_is_a_causal_mean(name):
+    """W_q = W_k = 0 makes every score 0, so each query head takes the plain
+    mean of the V rows it may see (rows 0..i); with the FFN switched off
+    (W_down = 0) layer 0 must give x + W_o . mean(V), V = W_v . RMSNorm(x),
+    query head h reading KV head h // (H / H_kv).  Pins the pre-norm, the GQA
+    mapping, the output projection and the residual add of the attention
+    branch against a formula without softmax or RoPE."""
+    s = wl.WORKLOADS[name].shape
+    prompt = wl.prompts(wl.WORKLOADS[name])[0]
+    over = {"layers.0.wq": np.zeros((s.q_dim, s.d_model), np.float32),
+            "layers.0.wk": np.zeros((s.n_kv_heads * s.head_dim, s.d_model), np.float32),
+            "layers.0.w_down": np.zeros((s.d_model, s.ffn_dim), np.float32)}
+    w = Weights(wl.SyntheticWeights(s).with_override(over))
+    t = 6
+    _, cap, _ = _prefill_logits(w, s, prompt[:t])
+    x = w["tok_emb"][prompt[:t]]
+    h = nm.rmsnorm(x, np.ones(s.d_model), s.rms_eps)
+    v = (h @ w["layers.0.wv"].T).reshape(t, s.n_kv_heads, s.head_dim)
+    mean = np.cumsum(v, axis=0) / np.arange(1, t + 1)[:, None, None]
+    group = s.n_heads // s.n_kv_heads
+    o = np.repeat(mean, group, axis=1).reshape(t, s.q_dim)
+    want = x + o @ w["layers.0.wo"].T
+    np.testing.assert_allclose(cap[:, 0], want, rtol=1e-10, atol=1e-12)
+
+
+def test_ffn_branch_alone_is_swiglu_of_the_normed_residual(tiny_w, tiny_prompt):
+    """W_o = 0 switches the attention branch off: layer 0 must give
+    x + W_down . (SiLU(W_gate . n) * (W_up . n)), n = RMSNorm(x), with SiLU
+    from scipy.  Pins the FFN's norm placement, the SwiGLU order (SiLU on the
+    gate, not the up projection) and the residual add."""
+    from scipy.special import expit
+    s = TINY.shape
+    w = Weights(wl.SyntheticWeights(s).with_override(
+        {"layers.0.wo": np.zeros((s.d_model, s.q_dim), np.float32)}))
+    t = 5
+    _, cap, _ = _prefill_logits(w, s, tiny_prompt[:t])
+    x = w["tok_emb"][tiny_prompt[:t]]
+    n = nm.rmsnorm(x, np.ones(s.d_model), s.rms_eps)
+    g = n @ w["layers.0.w_gate"].T
+    u = n @ w["layers.0.w_up"].T
+    want = x + ((g * expit(g)) * u) @ w["layers.0.w_down"].T
+    np.testing.assert_allclose(cap[:, 0], want, rtol=1e-10, atol=1e-12)
+
+
 def test_causal_prefix_unchanged_by_later_tokens(tiny_w, tiny_prompt):
     s = TINY.shape
     p = tiny_prompt[:12].copy()
