@@ -106,8 +106,8 @@ constexpr int kHd = 128;
 constexpr int kAttnSmem = 3 * 64 * 256 * 2 - 64 * 256;  // Q + 2 x (K, V) = 80 KB
 
 __global__ void __launch_bounds__(128) attn_mma_kernel(const AttnK p) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   extern __shared__ __align__(128) uint8_t sm[];
   uint8_t* qs = sm;                   // 64 x 256 B
   uint8_t* ks0 = sm + 64 * 256;       // 2 stages x (K 16 KB, V 16 KB)
@@ -384,54 +384,103 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const AttnK p) {
 
 constexpr int kMaxSplits = 256;
 
-// merge split partials: one CTA (128 threads = head_dim) per (row, head); all
-// partial loads are issued independently
-__global__ void attn_combine_kernel(const AttnK p) {
-  pdl_wait();
+// merge split partials: one warp per (row, head), lane l holds head dims
+// 4l..4l+3.  Up to kB splits, every load of the merge (row metadata, each
+// split's (m, l) and partial output) is issued before any is used, so the
+// kernel costs one memory round trip after its predecessor ends; more
+// splits go in batches of kB.  The sums run in split order either way.
+template <int kB>
+__global__ void __launch_bounds__(128) attn_combine_kernel(const AttnK p) {
   pdl_trigger();
-  __shared__ float sw[kMaxSplits];
-  __shared__ float s_inv;
-  const int row = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
+  pdl_wait();
+  __shared__ float sw[4][kMaxSplits];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x, h = blockIdx.y * 4 + warp;
+  if (h >= p.H) return;
   const int b = row / p.q_stride, j = row % p.q_stride;
   int seq_, ctx_, blk_;
   seq_meta(p, b, seq_, ctx_, blk_);
-  if (j >= blk_) return;
   const int S = p.n_splits;
   const size_t stride = (size_t)p.rows_total * p.H;  // (row, head) units between splits
   const size_t base = (size_t)row * p.H + h;
-  // split weights in warp 0: lane s takes splits s, s + 32, ...; max and
-  // weighted sum by butterflies in a fixed order
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
+  // partials of rows past the sequence's block were not written this pass:
+  // they are read (in bounds) and then dropped with the row
+  const float4* po = reinterpret_cast<const float4*>(p.part_o + base * kHd) + lane;
+  const size_t ostride = stride * (kHd / 4);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  auto fma4 = [](float4& a, float w, const float4& o) {
+    a.x += w * o.x;
+    a.y += w * o.y;
+    a.z += w * o.z;
+    a.w += w * o.w;
+  };
+  float l = 0.f;
+  if (S <= kB) {
+    const float2 ml = lane < S
+                          ? *reinterpret_cast<const float2*>(p.part_ml + (base + lane * stride) * 2)
+                          : make_float2(-INFINITY, 0.f);
+    float4 o[kB];
+#pragma unroll
+    for (int s = 0; s < kB; ++s)
+      if (s < S) o[s] = po[s * ostride];
+    float mx = ml.x;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (mx == -INFINITY) mx = 0.f;
+    const float w = lane < S ? exp2f(ml.x - mx) : 0.f;
+    l = w * ml.y;
+#pragma unroll
+    for (int s = 0; s < kB; ++s)
+      if (s < S) fma4(acc, __shfl_sync(0xffffffffu, w, s), o[s]);
+  } else {
+    // lane l takes splits l, l + 32, ...: maximum, then weights (kept in
+    // shared memory for the output sum) and the weighted sum of l
     float mx = -INFINITY;
     for (int s = lane; s < S; s += 32) mx = fmaxf(mx, p.part_ml[(base + s * stride) * 2]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
     if (mx == -INFINITY) mx = 0.f;
-    float l = 0.f;
     for (int s = lane; s < S; s += 32) {
       const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + (base + s * stride) * 2);
       const float w = exp2f(ml.x - mx);
-      sw[s] = w;
+      sw[warp][s] = w;
       l += w * ml.y;
     }
+    __syncwarp();
+    for (int s0 = 0; s0 < S; s0 += kB) {
+      float4 o[kB];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-    if (lane == 0) s_inv = l > 0.f ? 1.f / l : 0.f;
+      for (int s = 0; s < kB; ++s)
+        if (s0 + s < S) o[s] = po[(s0 + s) * ostride];
+#pragma unroll
+      for (int s = 0; s < kB; ++s)
+        if (s0 + s < S) fma4(acc, sw[warp][s0 + s], o[s]);
+    }
   }
-  __syncthreads();
-  float acc = 0.f;
-#pragma unroll 8
-  for (int s = 0; s < S; ++s) acc += sw[s] * p.part_o[(base + s * stride) * kHd + d];
-  static_cast<bf16*>(p.out)[base * kHd + d] = __float2bfloat16_rn(acc * s_inv);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+  if (j >= blk_) return;
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+  const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+  uint2 pk;
+  pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+  pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(static_cast<bf16*>(p.out) + base * kHd + lane * 4) = pk;
+}
+
+// few splits: a small batch keeps the registers (and so the resident warps
+// that hide the loads) of the common batched case
+static void (*combine_for(int splits))(const AttnK) {
+  return splits <= 8 ? attn_combine_kernel<8> : attn_combine_kernel<32>;
 }
 
 // ---------------------------------------------------------------------------
 // fp32 storage: one warp per (row, query head), keys visited in order
 // ---------------------------------------------------------------------------
 __global__ void attn_simt_f32_kernel(const AttnK p) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (wid >= p.rows_total * p.H) return;
   const int row = wid / p.H, h = wid % p.H;
@@ -573,8 +622,8 @@ dflash_status attention(dflash_ctx* ctx, const AttnArgs& a, cudaStream_t st) {
   DF_CUDA_TRY(ctx, launch_k(ctx->pdl, attn_mma_kernel, dim3(grid), dim3(128), kAttnSmem, st, p));
   DF_LAUNCHED(ctx);
   if (splits > 1) {
-    dim3 g2(p.rows_total, c.n_heads);
-    DF_CUDA_TRY(ctx, launch_k(ctx->pdl, attn_combine_kernel, dim3(g2), dim3(kHd), 0, st, p));
+    dim3 g2(p.rows_total, (c.n_heads + 3) / 4);
+    DF_CUDA_TRY(ctx, launch_k(ctx->pdl, combine_for(splits), dim3(g2), dim3(128), 0, st, p));
     DF_LAUNCHED(ctx);
   }
   return DFLASH_OK;
@@ -604,6 +653,10 @@ dflash_status block_attention(int batch, int H, int Hkv, int hd, int ctx_len, in
                               void* workspace, int64_t workspace_bytes, cudaStream_t st) {
   if (!op_shape_ok(batch, H, Hkv, hd, ctx_len, block)) return DFLASH_E_INVALID_ARG;
   if (!q || !k || !v || !out) return DFLASH_E_INVALID_ARG;
+  // 16-byte copies of Q/K/V rows and partials, 8-byte stores of the output
+  auto a16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; };
+  if (!a16(q) || !a16(k) || !a16(v) || !a16(out) || (workspace && !a16(workspace)))
+    return DFLASH_E_INVALID_ARG;
   AttnK p;
   memset(&p, 0, sizeof(p));
   p.q = q;
@@ -640,8 +693,8 @@ dflash_status block_attention(int batch, int H, int Hkv, int hd, int ctx_len, in
   if (launch_k(true, attn_mma_kernel, dim3(grid), dim3(128), kAttnSmem, st, p) != cudaSuccess)
     return DFLASH_E_CUDA;
   if (splits > 1) {
-    dim3 g2(p.rows_total, H);
-    if (launch_k(true, attn_combine_kernel, dim3(g2), dim3(kHd), 0, st, p) != cudaSuccess)
+    dim3 g2(p.rows_total, (H + 3) / 4);
+    if (launch_k(true, combine_for(splits), dim3(g2), dim3(128), 0, st, p) != cudaSuccess)
       return DFLASH_E_CUDA;
   }
   return DFLASH_OK;

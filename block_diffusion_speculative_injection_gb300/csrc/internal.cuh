@@ -267,8 +267,13 @@ __device__ __forceinline__ void st_f<bf16>(bf16* p, float v) { *p = __float2bflo
 // ---------------------------------------------------------------------------
 // programmatic dependent launch: a kernel may start while its predecessor
 // drains; it must call pdl_wait() before touching any memory an earlier
-// kernel writes or reads-then-rewrites.  Both are no-ops without the launch
-// attribute.
+// kernel writes or reads-then-rewrites.  Kernels signal their dependents
+// (pdl_trigger) before they wait, so a launch can be resident two or three
+// kernels ahead of the one that is running; what it does before its wait
+// (the GEMM's weight prefetch) reads only memory no kernel writes.  A kernel
+// is released only once every CTA of its predecessor has started, so the
+// CTAs that wait never hold back one that is still to be scheduled.  Both
+// are no-ops without the launch attribute.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {

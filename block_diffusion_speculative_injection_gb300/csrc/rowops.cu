@@ -25,8 +25,8 @@ struct PassSetupArgs {
 };
 
 __global__ void pass_setup_kernel(PassSetupArgs a) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   __shared__ int s_blk[1024];
   __shared__ int s_ctx[1024];
   for (int b = threadIdx.x; b < a.batch; b += blockDim.x) {
@@ -142,8 +142,8 @@ __global__ void embed_kernel(const int32_t* __restrict__ tokens, const T* __rest
                              const T* __restrict__ mask_emb, const int32_t* __restrict__ row_pos,
                              float* __restrict__ resid, int d, int vocab, int draft_block,
                              int block, int32_t* status) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x;
   float* out = resid + (size_t)r * d;
   const T* src = nullptr;
@@ -204,8 +204,8 @@ template <typename T>
 __global__ void __launch_bounds__(kNormThreads)
     norm_kernel(const float* __restrict__ resid, const int32_t* __restrict__ rows_in, int d,
                 const T* __restrict__ gain, T* __restrict__ out, float eps) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   __shared__ float red[32];
   const int i_out = blockIdx.x;
   const int r = rows_in ? rows_in[i_out] : i_out;
@@ -252,8 +252,8 @@ template <typename T, int VPT>
 __global__ void __launch_bounds__(kNormThreads)
     norm_vec_kernel(const float* __restrict__ resid, const int32_t* __restrict__ rows_in, int d,
                     const T* __restrict__ gain, T* __restrict__ out, float eps) {
-  pdl_wait();
   pdl_trigger();
+  pdl_wait();
   __shared__ float red[32];
   const int i_out = blockIdx.x;
   const int r = rows_in ? rows_in[i_out] : i_out;

@@ -276,8 +276,9 @@ DFLASH_API void dflash_destroy(dflash_ctx *ctx);
  * workspace_dev holds split-KV partials (fp32); pass at least
  * dflash_block_attention_workspace(...) bytes, or NULL / 0 to run without
  * splitting the context (slower at small batch, same result up to rounding).
+ * Every pointer must be 16-byte aligned.
  * Returns DFLASH_E_INVALID_ARG for unsupported shapes (block 1..64,
- * n_heads / n_kv_heads must divide 64). */
+ * n_heads / n_kv_heads must divide 64) and for misaligned pointers. */
 DFLASH_API dflash_status dflash_block_attention(int32_t batch, int32_t n_heads, int32_t n_kv_heads,
                                                 int32_t ctx_len, int32_t block, int32_t causal,
                                                 const void *q_dev, const void *k_dev,

@@ -80,3 +80,33 @@ def test_block_attention_full_grid_sampled(b, ctx):
     got = np.stack([out[bb, j, h] for (bb, j, h) in picks])
     np.testing.assert_allclose(got, ref, atol=2e-2, rtol=1e-2)
     assert np.isfinite(out).all()
+
+
+def test_full_grid_covers_every_combine_regime():
+    """The split merge has three code paths: up to 8 splits, up to 32 (all
+    loads in flight at once) and more (batches of 32).  The sampled grid
+    above must reach each of them."""
+    from block_diffusion_speculative_injection_gb300 import capi
+    seen = set()
+    for b in wl.ATTN_OP_BATCH:
+        for ctx in wl.ATTN_OP_CTX:
+            need = capi.dflash_block_attention_workspace(b, H, HKV, ctx, BLK)
+            splits = need // (b * BLK * H * (HD + 2) * 4) if need > 0 else 1
+            if splits > 1:
+                seen.add(0 if splits <= 8 else (1 if splits <= 32 else 2))
+    assert seen == {0, 1, 2}, seen
+
+
+def test_misaligned_pointers_are_refused():
+    from block_diffusion_speculative_injection_gb300 import capi
+    b, ctx = 1, 100
+    q = torch.zeros(b * BLK * H * HD + 8, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(b * HKV * (ctx + BLK) * HD, dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros_like(k)
+    out = torch.zeros(b * BLK * H * HD + 8, dtype=torch.bfloat16, device="cuda")
+    for qq, oo in ((q[1:], out[:-8]), (q[:-8], out[1:]), (q[4:], out[:-8])):
+        with pytest.raises(capi.DFlashError) as e:
+            capi.dflash_block_attention(b, H, HKV, ctx, BLK, 0, qq, k, v, oo)
+        assert e.value.status == 1
+    capi.dflash_block_attention(b, H, HKV, ctx, BLK, 0, q[8:], k, v, out[8:])  # 16-byte offsets pass
+    torch.cuda.synchronize()
