@@ -180,28 +180,32 @@ __device__ void run_epilogue(const EpiArgs& e, int n0, int m0, int BN) {
 }
 
 // ---------------------------------------------------------------------------
-// Cluster variant for the tensor-core GEMM (bf16, head_dim 128, N % 128 == 0).
-// The thread-block cluster holds the K splits of one 128-feature output tile
-// (SwiGLU: of a gate tile and the matching up tile, interleaved by rank:
-// rank = h + 2*split with h = 0 gate, 1 up).  Each CTA has its fp32 partial
-// tile in its own shared memory as part[token][feature]; after a cluster
-// barrier, CTA `rank` takes every csize-th work item of the tile, sums the
-// partials of all splits through distributed shared memory in split order,
-// and applies the epilogue operation.  meta[u] = (position, sequence, slot)
-// of tile row u (QKV / INJECT).
-// ---------------------------------------------------------------------------
-// Epilogue straight from tensor memory, for a tile without K splits: the
+// Epilogue straight from tensor memory, for a tile without K splits.  The
 // thread of TMEM lane f holds feature n0 + f for 16 token rows per
-// tcgen05.ld; it loads every operand of those 16 rows before using any.
-// QKV / INJECT rotate the pairs (f, f + 64) of a head, which sit in warps w
-// and w ^ 2: each 16-row chunk goes through `xbuf` ([16][128] fp32, shared,
-// followed by 3 x 256 ints of row metadata: 11 KB of the idle stage memory).
+// tcgen05.ld.  A warp may only read the TMEM lane quarter warp % 4, so a
+// CTA of 8 warps runs two groups of 4 warps over alternate 16-row chunks
+// (one group: all chunks); each group has its own named barrier and its own
+// exchange buffer.  QKV / INJECT rotate the pairs (f, f + 64) of a head and
+// SwiGLU multiplies gate row f by up row f + 64: those partners sit in warps
+// w and w ^ 2 and trade through the group's [16][128] fp32 buffer.  Row
+// metadata (destination offset, RoPE table offset) is worked out once per
+// row before the chunks.  All of it lives in the idle stage memory: two
+// 8 KB buffers, then 256 x 8 + 256 x 4 bytes.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void group_bar_sync(int grp) {
+  if (grp == 0) asm volatile("bar.sync 1, 128;" ::: "memory");
+  else asm volatile("bar.sync 2, 128;" ::: "memory");
+}
+
 template <typename T>
 __device__ void run_epilogue_direct(const EpiArgs& e, uint32_t tmem, int n0, int m0, int BN,
                                     float* xbuf) {
   const int warp = (int)threadIdx.x >> 5, lane = (int)threadIdx.x & 31;
-  const int f = warp * 32 + lane;
-  const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+  const int quarter = warp & 3, grp = warp >> 2, ngrp = (int)blockDim.x >> 7;
+  const int f = quarter * 32 + lane;
+  const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
+  const int c0 = grp * 16, cstep = ngrp * 16;
+  float* const xb = xbuf + grp * 16 * 128;
   const int M = e.M;
   switch (e.kind) {
     case kEpiResid: {
@@ -209,11 +213,18 @@ __device__ void run_epilogue_direct(const EpiArgs& e, uint32_t tmem, int n0, int
       float* const trace = e.trace;
       T* const cap = static_cast<T*>(e.capture);
       const int N = e.N, n_inj = e.n_inject, cap_slot = e.cap_slot, n = n0 + f;
-      for (int c = 0; c < BN; c += 16) {
-        float v[16], r[16];
-        tmem_ld16(taddr + (uint32_t)c, v);
+      // the residual rows of the next chunk load while this one is stored
+      auto load_r = [&](int c, float* r) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) r[i] = (m0 + c + i < M) ? resid[(size_t)(m0 + c + i) * N + n] : 0.f;
+        for (int i = 0; i < 16; ++i)
+          r[i] = (m0 + c + i < M) ? resid[(size_t)(m0 + c + i) * N + n] : 0.f;
+      };
+      float r[16], rn[16];
+      if (c0 < BN) load_r(c0, r);
+      for (int c = c0; c < BN; c += cstep) {
+        float v[16];
+        tmem_ld16(taddr + (uint32_t)c, v);
+        if (c + cstep < BN) load_r(c + cstep, rn);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int t = m0 + c + i;
@@ -223,6 +234,8 @@ __device__ void run_epilogue_direct(const EpiArgs& e, uint32_t tmem, int n0, int
           if (cap) st_f(cap + ((size_t)t * n_inj + cap_slot) * N + n, x);
           if (trace) trace[(size_t)t * N + n] = x;
         }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) r[i] = rn[i];
       }
       break;
     }
@@ -230,29 +243,34 @@ __device__ void run_epilogue_direct(const EpiArgs& e, uint32_t tmem, int n0, int
       // lanes 0..63: gate of features n0 + f; lanes 64..127: up of n0 + f - 64
       T* const act = static_cast<T*>(e.act);
       const int F = e.F;
-      for (int c = 0; c < BN; c += 16) {
+      for (int c = c0; c < BN; c += cstep) {
         float v[16];
         tmem_ld16(taddr + (uint32_t)c, v);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) xbuf[i * 128 + f] = v[i];
-        __syncthreads();
+        for (int i = 0; i < 16; ++i) xb[i * 128 + f] = v[i];
+        group_bar_sync(grp);
         if (f < 64) {
+          float up[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) up[i] = xb[i * 128 + f + 64];
+          group_bar_sync(grp);  // xb may be rewritten by the next chunk
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int t = m0 + c + i;
             if (t >= M) continue;
-            const float g = v[i], up = xbuf[i * 128 + f + 64];
-            st_f(act + (size_t)t * F + n0 + f, g / (1.f + __expf(-g)) * up);
+            const float g = v[i];
+            st_f(act + (size_t)t * F + n0 + f, g / (1.f + __expf(-g)) * up[i]);
           }
+        } else {
+          group_bar_sync(grp);
         }
-        __syncthreads();  // xbuf is rewritten by the next chunk
       }
       break;
     }
     case kEpiStore: {
       T* const out = static_cast<T*>(e.out);
       const int N = e.N, n = n0 + f;
-      for (int c = 0; c < BN; c += 16) {
+      for (int c = c0; c < BN; c += cstep) {
         float v[16];
         tmem_ld16(taddr + (uint32_t)c, v);
 #pragma unroll
@@ -283,83 +301,79 @@ __device__ void run_epilogue_direct(const EpiArgs& e, uint32_t tmem, int n0, int
       if (is_q) base = static_cast<T*>(e.q_out);
       else base = static_cast<T*>(is_v ? e.vc : e.kc) +
                   (inject ? (size_t)(e.layer0 + layer) * e.layer_elems : 0);
-      const int32_t* const row_pos = e.row_pos;
-      const int32_t* const row_seq = e.row_seq;
-      const int32_t* const row_slot = e.row_slot;
+      // per tile row: element offset of its 128-wide destination row (-1:
+      // nothing to write) and of its cos/sin table row (-1: no rotation)
+      long long* const s_dst = reinterpret_cast<long long*>(xbuf + 2 * 16 * 128);
+      int* const s_rope = reinterpret_cast<int*>(s_dst + 256);
+      for (int u = (int)threadIdx.x; u < BN; u += (int)blockDim.x) {
+        const int t = m0 + u;
+        long long dst = -1;
+        int rope = -1;
+        if (t < M) {
+          const int pos = e.row_pos[t], seq = e.row_seq[t];
+          if (pos >= 0 && seq >= 0) {
+            if (inject && (seq >= max_batch || pos >= max_ctx)) {
+              set_dev_status(e.status, kDevCheck);
+            } else {
+              const int slot = inject ? pos : e.row_slot[t];
+              dst = is_q ? ((long long)t * H + head) * 128
+                         : (((long long)seq * Hkv + head) * max_ctx + slot) * 128;
+              if (pos < max_ctx) rope = pos * 64;  // the tables hold max_ctx positions
+            }
+          }
+        }
+        s_dst[u] = dst;
+        s_rope[u] = rope;
+      }
+      __syncthreads();
       const float* const rcos = e.rcos;
       const float* const rsin = e.rsin;
       const int j = f & 63;
       const bool low = f < 64;
-      // the tile's row metadata, read from global memory once, kept in the
-      // (idle) stage memory after xbuf
-      int* const s_pos = reinterpret_cast<int*>(xbuf + 16 * 128);
-      int* const s_seq = s_pos + 256;
-      int* const s_slot = s_seq + 256;
-      for (int u = (int)threadIdx.x; u < BN; u += (int)blockDim.x) {
-        const int t = m0 + u;
-        const int ps = t < M ? row_pos[t] : -1;
-        s_pos[u] = ps;
-        s_seq[u] = t < M ? row_seq[t] : -1;
-        s_slot[u] = t < M ? (inject ? ps : row_slot[t]) : 0;
-      }
-      __syncthreads();
       // cos/sin of a chunk's rows, loaded one chunk ahead so that their
       // latency overlaps the previous chunk's exchange and stores
       float cs[16], sn[16], cs_n[16], sn_n[16];
       auto load_rope = [&](int c, float* cn, float* snn) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const int ps = c + i < BN ? s_pos[c + i] : -1;
-          const bool ok = ps >= 0 && ps < max_ctx;  // the tables hold max_ctx positions
-          cn[i] = ok ? rcos[(size_t)ps * 64 + j] : 1.f;
-          snn[i] = ok ? rsin[(size_t)ps * 64 + j] : 0.f;
+          const int ro = s_rope[c + i];
+          cn[i] = ro >= 0 ? rcos[ro + j] : 1.f;
+          snn[i] = ro >= 0 ? rsin[ro + j] : 0.f;
         }
       };
-      if (!is_v) load_rope(0, cs_n, sn_n);
-      for (int c = 0; c < BN; c += 16) {
+      if (!is_v && c0 < BN) load_rope(c0, cs_n, sn_n);
+      for (int c = c0; c < BN; c += cstep) {
         float v[16];
-        int pos[16], seq[16], slot[16];
         tmem_ld16(taddr + (uint32_t)c, v);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          pos[i] = s_pos[c + i];
-          seq[i] = s_seq[c + i];
-          slot[i] = s_slot[c + i];
-        }
+        float y[16];
         if (!is_v) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             cs[i] = cs_n[i];
             sn[i] = sn_n[i];
           }
-          if (c + 16 < BN) load_rope(c + 16, cs_n, sn_n);
+          if (c + cstep < BN) load_rope(c + cstep, cs_n, sn_n);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) xbuf[i * 128 + f] = v[i];
-          __syncthreads();
-        }
-        float other[16];
-        if (!is_v) {
+          for (int i = 0; i < 16; ++i) xb[i * 128 + f] = v[i];
+          group_bar_sync(grp);
+          float other[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) other[i] = xbuf[i * 128 + (f ^ 64)];
+          for (int i = 0; i < 16; ++i) other[i] = xb[i * 128 + (f ^ 64)];
+          group_bar_sync(grp);  // xb may be rewritten by the next chunk
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float lo = low ? v[i] : other[i], hi = low ? other[i] : v[i];
+            y[i] = low ? lo * cs[i] - hi * sn[i] : hi * cs[i] + lo * sn[i];
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) y[i] = v[i];
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const int t = m0 + c + i;
-          if (t >= M || pos[i] < 0 || seq[i] < 0) continue;
-          if (inject && (seq[i] >= max_batch || pos[i] >= max_ctx)) {
-            set_dev_status(e.status, kDevCheck);
-            continue;
-          }
-          T* dst = is_q ? base + ((size_t)t * H + head) * 128
-                        : base + (((size_t)seq[i] * Hkv + head) * max_ctx + slot[i]) * 128;
-          float y = v[i];
-          if (!is_v) {
-            const float lo = low ? v[i] : other[i], hi = low ? other[i] : v[i];
-            y = low ? lo * cs[i] - hi * sn[i] : hi * cs[i] + lo * sn[i];
-          }
-          st_f(dst + f, y);
+          const long long off = s_dst[c + i];
+          if (off >= 0) st_f(base + off + f, y[i]);
         }
-        if (!is_v) __syncthreads();  // xbuf is rewritten by the next chunk
       }
       break;
     }

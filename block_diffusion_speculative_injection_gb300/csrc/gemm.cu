@@ -35,7 +35,7 @@ struct TcParams {
   EpiArgs epi;
 };
 
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(256, 1)
     gemm_tc_kernel(const __grid_constant__ TmapSet wmaps, const __grid_constant__ CUtensorMap xmap,
                    const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -159,11 +159,14 @@ __global__ void __launch_bounds__(128, 1)
   mbar_wait_sleep(accum, 0, p.status);
   __syncwarp();
   tc_fence_after();
+  // a warp reads TMEM lane quarter warp % 4; with 8 warps the two groups of
+  // 4 take alternate 16-row chunks
+  const int quarter = warp & 3, c_first = (warp >> 2) * 16, c_step = ((int)blockDim.x >> 7) * 16;
   if (p.epi.kind == kEpiSlab) {  // plain fp32 result (lm_head logits), no K split
-    const int feat = n0 + warp * 32 + lane;
-    for (int c = 0; c < BN; c += 16) {
+    const int feat = n0 + quarter * 32 + lane;
+    for (int c = c_first; c < BN; c += c_step) {
       float v[16];
-      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, v);
+      tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c, v);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int t = m0 + c + i;
@@ -187,11 +190,11 @@ __global__ void __launch_bounds__(128, 1)
   // (the pipeline buffers are idle now), then a cluster-wide reduction
   __shared__ int32_t s_meta[256 * 3];
   float* part = reinterpret_cast<float*>(smem);
-  for (int c = 0; c < BN; c += 16) {
+  for (int c = c_first; c < BN; c += c_step) {
     float v[16];
-    tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, v);
+    tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c, v);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) part[(c + i) * 128 + warp * 32 + lane] = v[i];
+    for (int i = 0; i < 16; ++i) part[(c + i) * 128 + quarter * 32 + lane] = v[i];
   }
   for (int u = threadIdx.x; u < BN; u += blockDim.x) {
     const int t = m0 + u;
@@ -505,7 +508,10 @@ dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs&
   dim3 grid(n_tiles, m_tiles, splits);
   const size_t smem_bytes = tc_smem_bytes(BN, stages);
   const dim3 cluster(1, 1, splits);
-  DF_CUDA_TRY(ctx, launch_k_cluster(ctx->pdl, cluster, gemm_tc_kernel, grid, dim3(128), smem_bytes,
+  // tiles of more than 32 token rows hold an SM alone (shared memory): a
+  // second group of 4 warps then shares the epilogue at no occupancy cost
+  const dim3 block(BN > 32 ? 256 : 128);
+  DF_CUDA_TRY(ctx, launch_k_cluster(ctx->pdl, cluster, gemm_tc_kernel, grid, block, smem_bytes,
                                     st, maps, *xm, p));
   DF_LAUNCHED(ctx);
   *splits_used = splits;
