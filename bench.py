@@ -428,7 +428,7 @@ def run_ours(args, w: wl.Workload) -> None:
     eng.close()
 
 
-KERNEL_REV = "gemm-v4"
+KERNEL_REV = "gemm-v5"
 
 
 def run_attn_op(args) -> None:
