@@ -59,6 +59,7 @@ _SIGS = {
     "dflash_reset_seq": ([_P, _I, _P], _I),
     "dflash_verify": ([_P, _I, _P, _P, _I, _P, _I, _P, _P, _P, _P], _I),
     "dflash_draft_block": ([_P, _I, _P, _P, _P, _I, _P, _P, _P, _P], _I),
+    "dflash_set_block_size": ([_P, _I], _I),
     "dflash_accept_commit": ([_P, _I, _P, _P, _P, ctypes.POINTER(DTree), _I, _P, _P, _P, _P], _I),
     "dflash_inject_kv": ([_P, _I, _P, _P, _P, _P], _I),
     "dtree_build": ([_P, _I, _P, _P, _P, _I, _I, ctypes.POINTER(DTree), _P], _I),
@@ -165,6 +166,10 @@ def dflash_verify(ctx, batch, seq_ids, tokens, q, q_lens, flags, argmax, margin=
                   stream=None) -> None:
     _check(ctx, load().dflash_verify(ctx, batch, _ptr(seq_ids), _ptr(tokens), q, _ptr(q_lens), flags,
                                      _ptr(argmax), _ptr(margin), _ptr(logits), _stream(stream)))
+
+
+def dflash_set_block_size(ctx, block: int) -> None:
+    _check(ctx, load().dflash_set_block_size(ctx, block))
 
 
 def dflash_draft_block(ctx, batch, seq_ids, anchor, block, topk=0, topk_ids=None, topk_logp=None,

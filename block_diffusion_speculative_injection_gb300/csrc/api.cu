@@ -310,6 +310,7 @@ dflash_status dflash_create(const dflash_config* cfg, dflash_ctx** out) {
   }
   dflash_ctx* ctx = new dflash_ctx();
   ctx->cfg = *cfg;
+  ctx->active_block = cfg->block_size;
   const dflash_config& c = ctx->cfg;
   ctx->esize = c.dtype == DFLASH_BF16 ? 2 : 4;
   // programmatic dependent launch between kernels (DFLASH_NO_PDL=1 turns it off)
@@ -511,6 +512,15 @@ dflash_status dflash_verify(dflash_ctx* ctx, int32_t batch, const int32_t* seq_i
   return DFLASH_OK;
 }
 
+dflash_status dflash_set_block_size(dflash_ctx* ctx, int32_t block) {
+  if (!ctx) return DFLASH_E_INVALID_ARG;
+  if (block < 1 || block > ctx->cfg.block_size)
+    return fail(ctx, DFLASH_E_INVALID_ARG, "block %d outside 1..%d (the configured block size)",
+                block, ctx->cfg.block_size);
+  ctx->active_block = block;
+  return DFLASH_OK;
+}
+
 dflash_status dflash_draft_block(dflash_ctx* ctx, int32_t batch, const int32_t* seq_ids_dev,
                                  const int32_t* anchor_dev, int32_t* block_dev, int32_t topk,
                                  int32_t* topk_ids_dev, float* topk_logp_dev, float* logits_dev,
@@ -526,7 +536,7 @@ dflash_status dflash_draft_block(dflash_ctx* ctx, int32_t batch, const int32_t* 
   if (topk > c.vocab) return fail(ctx, DFLASH_E_INVALID_ARG, "topk exceeds vocab");
   DF_TRY(resolve_weights(ctx));
   cudaStream_t st = (cudaStream_t)stream;
-  const int B = c.block_size;
+  const int B = ctx->active_block;
   const DraftMeta& dm = g_draft_meta[ctx];
   DF_TRY(launch_pass_setup_full(ctx, batch, seq_ids_dev, B, nullptr, nullptr, nullptr, kPassDraft,
                                 0, anchor_dev, block_dev, dm.seq, dm.ctx, dm.blk, st));
@@ -667,9 +677,9 @@ dflash_status dtree_build(dflash_ctx* ctx, int32_t batch, const int32_t* anchor_
     return fail(ctx, DFLASH_E_CAPACITY, "tree max_nodes exceeds max_tree_nodes");
   if (tree->anc_words != (tree->max_nodes + 63) / 64)
     return fail(ctx, DFLASH_E_INVALID_ARG, "anc_words must be ceil(max_nodes/64)");
-  if (c.block_size < 2) return fail(ctx, DFLASH_E_INVALID_ARG, "tree needs block_size >= 2");
+  if (ctx->active_block < 2) return fail(ctx, DFLASH_E_INVALID_ARG, "tree needs block size >= 2");
   return launch_tree_build(ctx, batch, anchor_dev, topk_ids_dev, topk_logp_dev, topk,
-                           c.block_size - 1, budget, tree, (cudaStream_t)stream);
+                           ctx->active_block - 1, budget, tree, (cudaStream_t)stream);
 }
 
 dflash_status dtree_verify(dflash_ctx* ctx, int32_t batch, const int32_t* seq_ids_dev,

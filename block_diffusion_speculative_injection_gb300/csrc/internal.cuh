@@ -72,6 +72,7 @@ struct dflash_ctx {
   const void *tok_emb = nullptr, *lm_head = nullptr, *final_norm = nullptr;
   const void *fuse = nullptr, *mask_emb = nullptr, *draft_final_norm = nullptr;
   bool resolved = false;
+  int active_block = 0;  // block size of the next draft passes (<= cfg.block_size)
 
   // per-sequence state
   int32_t* seq_len = nullptr;        // [max_batch] committed length

@@ -18,6 +18,7 @@ import torch
 import workloads as wl
 
 from . import capi
+from .adaptive import AdaptiveBlock
 
 
 def config_for(shape: wl.ModelShape, block_size: int, max_batch: int, max_ctx: int,
@@ -82,6 +83,7 @@ class DFlashEngine:
         capi.load()
         self.shape = shape
         self.B = block_size
+        self.B_max = block_size
         self.max_batch = max_batch
         self.max_tree_nodes = max_tree_nodes
         self.device = device
@@ -133,6 +135,11 @@ class DFlashEngine:
             self.close()
         except Exception:
             pass
+
+    def set_block_size(self, block: int) -> None:
+        """Block size of the following steps (1..the configured block size)."""
+        capi.dflash_set_block_size(self.ctx, block)
+        self.B = block
 
     # -- sequence setup ----------------------------------------------------
     def seq_ids(self, batch: int) -> torch.Tensor:
@@ -221,14 +228,15 @@ class DFlashEngine:
         B = self.B
         V = self.shape.vocab
         if not hasattr(self, "_samp"):
-            rows = self.max_batch * max(B - 1, 1)
+            rows = self.max_batch * max(self.B_max - 1, 1)
             self._samp = {
                 "dlog": torch.empty(rows * V, dtype=torch.float32, device=self.device),
-                "vlog": torch.empty(self.max_batch * B * V, dtype=torch.float32, device=self.device),
+                "vlog": torch.empty(self.max_batch * self.B_max * V, dtype=torch.float32,
+                                    device=self.device),
                 "draws": torch.empty(rows, dtype=torch.int32, device=self.device),
                 "ws_draw": torch.empty(max(capi.dflash_sample_workspace(rows, V), 256), dtype=torch.uint8,
                                        device=self.device),
-                "ws_acc": torch.empty(capi.dflash_spec_accept_workspace(self.max_batch, B, V),
+                "ws_acc": torch.empty(capi.dflash_spec_accept_workspace(self.max_batch, self.B_max, V),
                                       dtype=torch.uint8, device=self.device),
             }
         m = self._samp
@@ -299,12 +307,25 @@ class DFlashEngine:
 
     # -- whole generations ---------------------------------------------------
     def generate(self, prompts: Sequence[np.ndarray], n_new: int, mode: str = "dflash",
-                 topk: int = 8, budget: int = 64) -> List[List[int]]:
+                 topk: int = 8, budget: int = 64, block_schedule=None) -> List[List[int]]:
+        """Greedy generation.  mode "dflash" / "ddtree" / "ar"; "adaptive" is
+        "dflash" with the block size of every step chosen by AdaptiveBlock
+        from the previous steps' accepted lengths.  block_schedule (a list
+        of block sizes, cycled) fixes the block size of each dflash step
+        instead."""
         b = len(prompts)
         sid = self.seq_ids(b)
         anchors = self.prefill(prompts)
         outs = [[int(t)] for t in anchors.tolist()]
+        policy = AdaptiveBlock(self.B_max) if mode == "adaptive" else None
+        n_step = 0
         while min(len(o) for o in outs) < n_new:
+            if mode in ("dflash", "adaptive") and (policy is not None or block_schedule is not None):
+                nb = policy.next_block() if policy is not None else \
+                    block_schedule[n_step % len(block_schedule)]
+                if nb != self.B:
+                    self.set_block_size(nb)
+            n_step += 1
             if mode == "ar":
                 anchors = self.ar_step(sid, anchors).clone()
                 for s, t in enumerate(anchors.tolist()):
@@ -315,9 +336,13 @@ class DFlashEngine:
                 em = r["emitted"]
             else:
                 em = self.step(sid, anchors).emitted
+                if policy is not None:
+                    policy.update(self.accept_len[:b].tolist())
             anchors = self.next_anchor[:b].clone()
             for s, row in enumerate(em.tolist()):
                 outs[s].extend(int(t) for t in row if t >= 0)
+        if self.B != self.B_max:
+            self.set_block_size(self.B_max)
         return [o[:n_new] for o in outs]
 
 

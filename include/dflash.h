@@ -154,9 +154,22 @@ DFLASH_API dflash_status dflash_verify(dflash_ctx *ctx, int32_t batch, const int
                             int32_t flags, int32_t *argmax_dev, float *margin_dev,
                             float *logits_dev, dflash_stream_t stream);
 
+/* Block size B of the draft passes that follow (and of the draft slots
+ * dtree_build reads), 1 <= block <= config.block_size.  The pages train the
+ * drafter with a large block that carries over to smaller inference blocks
+ * (Deep Research Report, "Key points": training innovations) and name
+ * adaptive block sizes as a direction (its "Discussion and open problems");
+ * this call lets a caller pick B per step.  dflash_verify takes its q
+ * explicitly (pass q = B).  Host state only: it applies to calls made after
+ * it, enqueues nothing, and a CUDA graph captured with one B replays that B.
+ * The context starts at config.block_size.  DFLASH_E_INVALID_ARG outside
+ * 1..config.block_size. */
+DFLASH_API dflash_status dflash_set_block_size(dflash_ctx *ctx, int32_t block);
+
 /* One block-diffusion draft pass (stage 2).  Slot j of the block of slot
  * seq_ids[b] sits at position P_b + j; slot 0 embeds anchor_dev[b], slots
- * 1..B-1 the mask embedding.  Every block position attends to the injected
+ * 1..B-1 the mask embedding (B: the block size set by dflash_set_block_size,
+ * initially config.block_size).  Every block position attends to the injected
  * draft context 0..P_b-1 and to all B block positions (no mask).
  *   block_dev   [batch][B] int32 out: [anchor, d_1 .. d_{B-1}] where d_j is
  *               the argmax of the shared lm_head at slot j (ties: lowest id)

@@ -148,3 +148,35 @@ def test_expired_device_wait_is_reported_and_context_survives(engine_mod):
     capi.dflash_check(eng.ctx)
     assert int(out.accept_len[0]) >= 0
     eng.close()
+
+
+def test_block_size_per_step_is_lossless(engine_mod):
+    """Greedy output does not depend on the block size of each step: a fixed
+    schedule of block sizes and the adaptive policy both emit the oracle's
+    greedy AR tokens."""
+    from oracle.decode import greedy_ar
+    w = wl.WORKLOADS["tiny_f32_e2e"]
+    prompt = wl.prompts(w)[0]
+    eng = engine_mod.DFlashEngine(w.shape, w.block_size, 1, 256, max_rows=128)
+    sched = [w.block_size, 5, 1, 9, 2, w.block_size, 3]
+    got = eng.generate([prompt], w.new_tokens, block_schedule=sched)[0]
+    assert eng.B == w.block_size  # restored after the run
+    adaptive = eng.generate([prompt], w.new_tokens, mode="adaptive")[0]
+    W = Weights(wl.SyntheticWeights(w.shape))
+    ref = greedy_ar(W, w.shape, Precision("exact"), prompt, w.new_tokens)
+    assert got == ref
+    assert adaptive == ref
+    eng.close()
+
+
+def test_set_block_size_bounds(engine_mod):
+    from block_diffusion_speculative_injection_gb300 import capi
+    w = wl.WORKLOADS["tiny_f32_e2e"]
+    eng = engine_mod.DFlashEngine(w.shape, w.block_size, 1, 256, max_rows=128)
+    for bad in (0, -1, w.block_size + 1):
+        with pytest.raises(capi.DFlashError) as e:
+            capi.dflash_set_block_size(eng.ctx, bad)
+        assert e.value.status == 1
+    capi.dflash_set_block_size(eng.ctx, 1)
+    capi.dflash_set_block_size(eng.ctx, w.block_size)
+    eng.close()
