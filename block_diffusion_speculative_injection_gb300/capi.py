@@ -79,6 +79,8 @@ _SIGS = {
     "dflash_spec_accept_workspace": ([_I, _I, _I], ctypes.c_int64),
     "dflash_spec_accept_sampled": ([_I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int64, _P],
                                    _I),
+    "dflash_plan_gemm": ([_I, _I, _I, _I, _I, _I, _P], _I),
+    "dflash_plan_attention": ([_I, _I, _I, _I, _I, ctypes.c_int64, _I, _P], _I),
     "dflash_profile": ([_P, _I], _I),
     "dflash_debug_trace": ([_P, _P, ctypes.c_int64], _I),
     "dflash_profile_read": ([_P, _I, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double),
@@ -239,6 +241,27 @@ def dflash_block_attention(batch, n_heads, n_kv_heads, ctx_len, block, causal, q
 
 def dflash_block_attention_workspace(batch, n_heads, n_kv_heads, ctx_len, block) -> int:
     return int(load().dflash_block_attention_workspace(batch, n_heads, n_kv_heads, ctx_len, block))
+
+
+def dflash_plan_gemm(sm_count, M, N, K, kind, max_splits=8) -> dict:
+    """Launch plan of the tensor-core GEMM (host arithmetic; no GPU needed)."""
+    out = (ctypes.c_int32 * 7)()
+    st = load().dflash_plan_gemm(sm_count, M, N, K, kind, max_splits, ctypes.addressof(out))
+    if st != 0:
+        raise DFlashError(st, "dflash_plan_gemm")
+    keys = ("BN", "m_tiles", "n_tiles", "stages", "splits", "threads", "smem_bytes")
+    return dict(zip(keys, list(out)))
+
+
+def dflash_plan_attention(sm_count, batch, n_heads, n_kv_heads, q_per_seq, max_keys,
+                          min_splits=1) -> dict:
+    """Split-KV plan of the bf16 attention (host arithmetic; no GPU needed)."""
+    out = (ctypes.c_int32 * 3)()
+    st = load().dflash_plan_attention(sm_count, batch, n_heads, n_kv_heads, q_per_seq, max_keys,
+                                      min_splits, ctypes.addressof(out))
+    if st != 0:
+        raise DFlashError(st, "dflash_plan_attention")
+    return dict(zip(("splits", "keys_per_split", "ctas"), list(out)))
 
 
 def dflash_profile(ctx, enable: bool) -> None:

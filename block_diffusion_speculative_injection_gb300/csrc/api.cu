@@ -738,6 +738,18 @@ dflash_status dflash_block_attention(int32_t batch, int32_t n_heads, int32_t n_k
                          (cudaStream_t)stream);
 }
 
+dflash_status dflash_plan_gemm(int32_t sm_count, int32_t M, int32_t N, int32_t K, int32_t kind,
+                              int32_t max_splits, int32_t* plan_out) {
+  return plan_gemm(sm_count, M, N, K, kind, max_splits, plan_out);
+}
+
+dflash_status dflash_plan_attention(int32_t sm_count, int32_t batch, int32_t n_heads,
+                                   int32_t n_kv_heads, int32_t q_per_seq, int64_t max_keys,
+                                   int32_t min_splits, int32_t* plan_out) {
+  return plan_attention(sm_count, batch, n_heads, n_kv_heads, q_per_seq, max_keys, min_splits,
+                        plan_out);
+}
+
 int64_t dflash_block_attention_workspace(int32_t batch, int32_t n_heads, int32_t n_kv_heads,
                                          int32_t ctx_len, int32_t block) {
   return block_attention_workspace(batch, n_heads, n_kv_heads, 128, ctx_len, block);

@@ -550,6 +550,24 @@ static void plan_splits(int sm_count, int ctas, int64_t max_keys, size_t part_ca
   *n_splits = best;
 }
 
+dflash_status plan_attention(int sm_count, int batch, int H, int Hkv, int q_per_seq,
+                             int64_t max_keys, int min_splits, int32_t* out) {
+  if (!out || sm_count < 1 || batch < 1 || H < 1 || Hkv < 1 || H % Hkv != 0 ||
+      64 % (H / Hkv) != 0 || q_per_seq < 1 || max_keys < 1 || max_keys >= (1 << 30) ||
+      min_splits < 1)
+    return DFLASH_E_INVALID_ARG;
+  const int POS = 64 / (H / Hkv);
+  const int64_t ctas = (int64_t)((q_per_seq + POS - 1) / POS) * Hkv * batch;
+  if (ctas * kMaxSplits >= (1 << 30)) return DFLASH_E_INVALID_ARG;
+  int splits = 1, kps = 0;
+  plan_splits(sm_count, (int)ctas, max_keys, (size_t)1 << 40, batch * q_per_seq * H, &splits, &kps,
+              min_splits);
+  out[0] = splits;
+  out[1] = splits > 1 ? kps : (int32_t)max_keys;
+  out[2] = (int32_t)(ctas * splits);
+  return DFLASH_OK;
+}
+
 static int device_sms() {
   static int sms = 0;
   if (!sms) {

@@ -348,9 +348,10 @@ static size_t tc_smem_bytes(int BN, int stages) {
   return 1024 + (size_t)stages * (128 * 64 * 2 + BN * 64 * 2) + (2 * stages + 1) * 8 + 16;
 }
 
-// tile shape and K split of one bf16 GEMM launch
+// tile shape, K split and launch shape of one bf16 GEMM launch
 struct TcPlan {
-  int BN, m_tiles, n_tiles, stages, n_kb, splits, kb_per;
+  int BN, m_tiles, n_tiles, stages, n_kb, splits, kb_per, threads;
+  size_t smem_bytes;
 };
 
 static cudaError_t ensure_tc_smem() {
@@ -362,7 +363,7 @@ static cudaError_t ensure_tc_smem() {
   return e;
 }
 
-static TcPlan plan_tc(dflash_ctx* ctx, int M, int N, int K, int kind, int max_splits) {
+static TcPlan plan_tc(int sm_count, int M, int N, int K, int kind, int max_splits) {
   TcPlan t;
   t.m_tiles = (M + 255) / 256;
   int BN = (M + t.m_tiles - 1) / t.m_tiles;
@@ -375,7 +376,7 @@ static TcPlan plan_tc(dflash_ctx* ctx, int M, int N, int K, int kind, int max_sp
   // K splits: as many as fit in ONE wave of resident CTAs (a partial second
   // wave would double the latency of these short, bandwidth-bound launches)
   const int per_sm = (t.BN <= 32) ? 2 : 1;
-  const int slots = per_sm * ctx->sm_count;
+  const int slots = per_sm * sm_count;
   int splits = ctas >= slots ? 1 : slots / ctas;
   // Tiles wider than 128 token rows take the whole K range when the unsplit
   // grid already covers a third of the SMs: their epilogue then runs
@@ -383,9 +384,9 @@ static TcPlan plan_tc(dflash_ctx* ctx, int M, int N, int K, int kind, int max_sp
   // tile costs more than the parallelism it adds.  Measured on the
   // concurrency sweep (b = 4, 8, 16, 32 at block 16): splitting pays up to
   // 128 rows, and above that only for grids of a few dozen CTAs.
-  if (t.BN > 128 && 3 * ctas >= ctx->sm_count) splits = 1;
-  // the K splits of a tile form one thread-block cluster (portable size <= 8;
-  // a SwiGLU cluster also holds the matching up tile)
+  if (t.BN > 128 && 3 * ctas >= sm_count) splits = 1;
+  // the K splits of a tile form one thread-block cluster (portable size <= 8);
+  // a SwiGLU tile holds gate and up rows in one CTA and is never split
   const int max_cluster_splits = kind == kEpiSwiGLU ? 1 : 8;  // SwiGLU: direct epilogue only
   if (splits > max_cluster_splits) splits = max_cluster_splits;
   if (splits > max_splits) splits = max_splits;
@@ -399,7 +400,26 @@ static TcPlan plan_tc(dflash_ctx* ctx, int M, int N, int K, int kind, int max_sp
   while (splits > 1 && (int64_t)ctas * splits * 8 > (int64_t)slots * 7) --splits;
   t.kb_per = (t.n_kb + splits - 1) / splits;
   t.splits = (t.n_kb + t.kb_per - 1) / t.kb_per;
+  // tiles of more than 32 token rows hold an SM alone (shared memory): a
+  // second group of 4 warps then shares the epilogue at no occupancy cost
+  t.threads = t.BN > 32 ? 256 : 128;
+  t.smem_bytes = tc_smem_bytes(t.BN, t.stages);
   return t;
+}
+
+dflash_status plan_gemm(int sm_count, int M, int N, int K, int kind, int max_splits, int32_t* out) {
+  if (!out || sm_count < 1 || M < 1 || N < 1 || K < 64 || K % 64 != 0 || max_splits < 1 ||
+      kind < kEpiSlab || kind > kEpiInject || (kind == kEpiSwiGLU && N % 128 != 0))
+    return DFLASH_E_INVALID_ARG;
+  const TcPlan t = plan_tc(sm_count, M, N, K, kind, max_splits);
+  out[0] = t.BN;
+  out[1] = t.m_tiles;
+  out[2] = t.n_tiles;
+  out[3] = t.stages;
+  out[4] = t.splits;
+  out[5] = t.threads;
+  out[6] = (int32_t)t.smem_bytes;
+  return DFLASH_OK;
 }
 
 dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs& segs,
@@ -456,7 +476,7 @@ dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs&
       set_error(ctx, "GEMM segment %d has %d rows (not a multiple of 128)", i, segs.rows[i]);
       return DFLASH_E_UNSUPPORTED;
     }
-  const TcPlan plan = plan_tc(ctx, M, N, K, epi_in.kind, max_splits);
+  const TcPlan plan = plan_tc(ctx->sm_count, M, N, K, epi_in.kind, max_splits);
   const int m_tiles = plan.m_tiles, BN = plan.BN, stages = plan.stages, n_tiles = plan.n_tiles;
   const int n_kb = plan.n_kb;
   const int kb_per = plan.kb_per;
@@ -506,11 +526,9 @@ dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs&
 
   DF_CUDA_TRY(ctx, ensure_tc_smem());
   dim3 grid(n_tiles, m_tiles, splits);
-  const size_t smem_bytes = tc_smem_bytes(BN, stages);
+  const size_t smem_bytes = plan.smem_bytes;
   const dim3 cluster(1, 1, splits);
-  // tiles of more than 32 token rows hold an SM alone (shared memory): a
-  // second group of 4 warps then shares the epilogue at no occupancy cost
-  const dim3 block(BN > 32 ? 256 : 128);
+  const dim3 block(plan.threads);
   DF_CUDA_TRY(ctx, launch_k_cluster(ctx->pdl, cluster, gemm_tc_kernel, grid, block, smem_bytes,
                                     st, maps, *xm, p));
   DF_LAUNCHED(ctx);

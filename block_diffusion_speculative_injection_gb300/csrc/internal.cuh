@@ -218,6 +218,9 @@ struct ProfScope {
 };
 
 int64_t block_attention_workspace(int batch, int H, int Hkv, int hd, int ctx_len, int block);
+dflash_status plan_attention(int sm_count, int batch, int H, int Hkv, int q_per_seq,
+                             int64_t max_keys, int min_splits, int32_t* out);
+dflash_status plan_gemm(int sm_count, int M, int N, int K, int kind, int max_splits, int32_t* out);
 dflash_status block_attention(int batch, int H, int Hkv, int hd, int ctx_len, int block, int causal,
                               const void* q, const void* k, const void* v, void* out,
                               void* workspace, int64_t workspace_bytes, cudaStream_t st);

@@ -404,6 +404,31 @@ DFLASH_API dflash_status dflash_profile(dflash_ctx *ctx, int32_t enable);
 DFLASH_API dflash_status dflash_profile_read(dflash_ctx *ctx, int32_t kind, int64_t *launches,
                                              double *ms, double *bytes, double *flops);
 
+/* ---- launch plans (host arithmetic only: no GPU, no context) -----------------
+ * The pages prescribe no kernel design; these report the shapes this library
+ * picks, so that a caller (or a test) can see them without a GPU.
+ *
+ * Tensor-core GEMM of M token rows by an N x K weight (K a multiple of 64)
+ * on a GPU with sm_count SMs.  kind: 0 fp32 result (lm_head), 1 QKV, 2 SwiGLU
+ * (N = gate rows + up rows, a multiple of 128), 3 residual add, 4 store,
+ * 5 injected K/V.  max_splits caps the K split.  plan_out[7] receives:
+ * token rows per tile, token-row tiles, 128-row weight tiles, pipeline stages,
+ * K splits (= thread-block cluster size), threads per CTA, dynamic shared
+ * memory bytes.  DFLASH_E_INVALID_ARG for sizes the GEMM does not take. */
+DFLASH_API dflash_status dflash_plan_gemm(int32_t sm_count, int32_t M, int32_t N, int32_t K,
+                                          int32_t kind, int32_t max_splits, int32_t *plan_out);
+
+/* Split-KV plan of the bf16 attention (head_dim 128) for `batch` sequences of
+ * q_per_seq query rows over at most max_keys keys, on sm_count SMs, with at
+ * least min_splits splits (the engine asks for 2 on batched passes; the op
+ * entry points for 1).  plan_out[3] receives: splits, keys per split (a
+ * multiple of 64; max_keys when unsplit), CTAs of the split kernel.
+ * DFLASH_E_INVALID_ARG for unsupported shapes. */
+DFLASH_API dflash_status dflash_plan_attention(int32_t sm_count, int32_t batch, int32_t n_heads,
+                                               int32_t n_kv_heads, int32_t q_per_seq,
+                                               int64_t max_keys, int32_t min_splits,
+                                               int32_t *plan_out);
+
 #ifdef __cplusplus
 }
 #endif
