@@ -1,9 +1,10 @@
-// Fused GEMM epilogues.  The K splits of a tile are summed in split order
-// (so the result does not depend on timing) -- from the partial tiles in
-// the shared memory of a thread-block cluster (bf16 tensor-core GEMM,
-// run_epilogue_cluster) or from fp32 slabs in global memory (fp32 SIMT
-// GEMM, run_epilogue) -- and the operation that follows the projection in
-// the pass is applied:
+// Fused GEMM epilogues.  A tile's accumulator comes straight from tensor
+// memory when the tile took the whole K range (run_epilogue_direct); else
+// its K splits are summed in split order (so the result does not depend on
+// timing) -- from the partial tiles in the shared memory of a thread-block
+// cluster (bf16 tensor-core GEMM, run_epilogue_cluster) or from fp32 slabs
+// in global memory (fp32 SIMT GEMM, run_epilogue).  Then the operation that
+// follows the projection in the pass is applied:
 //   QKV    RoPE on Q and K at the row's position; Q -> q_out, K/V -> cache
 //   SWIGLU act = SiLU(gate) * up            (tile pair: gate tile, up tile)
 //   RESID  residual += projection (+ bf16 capture of an injected layer)

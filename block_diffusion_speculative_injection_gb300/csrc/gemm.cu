@@ -6,10 +6,15 @@
 // and the compute-bound regime of a 512-row batch.  Operands are staged in
 // shared memory by TMA (128-byte swizzle) through an mbarrier ring; one
 // thread issues the MMAs, accumulators live in tensor memory and are read
-// back by all four warps.  K may be split across CTAs; every split writes
-// its own fp32 slab and the consumer kernels sum the slabs in a fixed order.
+// back by every warp of the CTA (4, or 8 on tiles of more than 32 token
+// rows).  The projection's epilogue (RoPE + cache scatter, SwiGLU, residual
+// add, store) is fused: straight from tensor memory when the tile takes the
+// whole K range, else the K splits of the tile form a thread-block cluster
+// and sum their partial tiles through distributed shared memory in split
+// order.  Only the lm_head writes a plain fp32 result.
 //
-// f32 storage: a tiled SIMT kernel (fp32 FMA), used by the small fp32 model.
+// f32 storage: a tiled SIMT kernel (fp32 FMA) writes per-split fp32 slabs
+// and an epilogue kernel sums them in a fixed order (the small fp32 model).
 #include <cstdio>
 #include <cstring>
 
