@@ -25,7 +25,6 @@ struct EpiArgs {
   int M, N, splits;
   long long split_stride;  // elements between slabs (= M * N)
   const float* slab;
-  int32_t* counters;
   // QKV / INJECT
   const int32_t* row_pos;
   const int32_t* row_slot;

@@ -1,7 +1,9 @@
-// Row-wise kernels of the target / draft passes.  Each consumes the fp32
-// GEMM slabs (summing K splits in a fixed order) and applies what follows
-// the projection: RoPE + KV-cache scatter, SwiGLU, residual add + RMSNorm
-// (+ capture of the injected layers), and the KV-injection scatter.
+// Row-wise kernels of the target / draft passes: the pass setup (per-sequence
+// and per-row metadata), the token / mask embedding into the fp32 residual
+// stream, and RMSNorm of residual rows into the next GEMM's input (optionally
+// gathering rows).  What follows each projection (RoPE + cache scatter,
+// SwiGLU, residual add + capture, injection) is fused into the GEMM's
+// epilogue instead.
 #include "internal.cuh"
 
 namespace dflash {
