@@ -318,6 +318,7 @@ class DFlashEngine:
         anchors = self.prefill(prompts)
         outs = [[int(t)] for t in anchors.tolist()]
         policy = AdaptiveBlock(self.B_max) if mode == "adaptive" else None
+        b_entry = self.B
         n_step = 0
         while min(len(o) for o in outs) < n_new:
             if mode in ("dflash", "adaptive") and (policy is not None or block_schedule is not None):
@@ -341,8 +342,8 @@ class DFlashEngine:
             anchors = self.next_anchor[:b].clone()
             for s, row in enumerate(em.tolist()):
                 outs[s].extend(int(t) for t in row if t >= 0)
-        if self.B != self.B_max:
-            self.set_block_size(self.B_max)
+        if self.B != b_entry:
+            self.set_block_size(b_entry)
         return [o[:n_new] for o in outs]
 
 
