@@ -53,4 +53,6 @@ def test_null_context_calls_fail_cleanly(lib):
     assert lib.dflash_check(None) == 1
     assert lib.dflash_launch_count(None) == -1
     assert lib.dflash_seq_lengths(None) is None
+    assert lib.dflash_set_block_size(None, 4) == 1
+    assert lib.dflash_draft_block(None, 1, None, None, None, 0, None, None, None, None) == 1
     lib.dflash_destroy(None)
