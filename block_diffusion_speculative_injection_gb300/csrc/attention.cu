@@ -568,24 +568,23 @@ dflash_status plan_attention(int sm_count, int batch, int H, int Hkv, int q_per_
   return DFLASH_OK;
 }
 
+// SM count of the current device (cached per device)
 static int device_sms() {
-  static int sms = 0;
-  if (!sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 1;
+  static std::atomic<int> sms[kMaxDevices];
+  const int dev = current_device_slot();
+  if (dev < 0) return 1;
+  int n = sms[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 1;
+    sms[dev].store(n, std::memory_order_relaxed);
   }
-  return sms;
+  return n;
 }
 
 static cudaError_t ensure_attn_smem() {
-  static bool attr = false;
-  if (attr) return cudaSuccess;
-  cudaError_t e =
-      cudaFuncSetAttribute(attn_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
-  if (e == cudaSuccess) attr = true;
-  return e;
+  static std::atomic<bool> done[kMaxDevices];
+  return ensure_smem_attr(done, attn_mma_kernel, kAttnSmem);
 }
 
 dflash_status attention(dflash_ctx* ctx, const AttnArgs& a, cudaStream_t st) {

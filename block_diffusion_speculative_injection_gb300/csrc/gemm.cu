@@ -360,12 +360,8 @@ struct TcPlan {
 };
 
 static cudaError_t ensure_tc_smem() {
-  static bool done = false;
-  if (done) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       210 * 1024);
-  if (e == cudaSuccess) done = true;
-  return e;
+  static std::atomic<bool> done[kMaxDevices];
+  return ensure_smem_attr(done, gemm_tc_kernel, 210 * 1024);
 }
 
 static TcPlan plan_tc(int sm_count, int M, int N, int K, int kind, int max_splits) {

@@ -8,6 +8,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <utility>
 #include <map>
@@ -197,6 +198,29 @@ dflash_status launch_tree_accept(dflash_ctx* ctx, int batch, const int32_t* seq_
                                  cudaStream_t st);
 
 void set_error(dflash_ctx* ctx, const char* fmt, ...);
+
+// Per-device one-time host state.  Kernel attributes set with
+// cudaFuncSetAttribute and SM counts belong to one device, so they are kept
+// per device index (slots are atomics: two host threads may race on a first
+// call; both store the same value).
+constexpr int kMaxDevices = 64;
+// current device index in [0, kMaxDevices), or -1
+inline int current_device_slot() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+// raises a kernel's dynamic shared-memory limit once per device
+template <typename K>
+inline cudaError_t ensure_smem_attr(std::atomic<bool>* done, K kernel, int bytes) {
+  const int dev = current_device_slot();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  if (done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(kernel),
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done[dev].store(true, std::memory_order_relaxed);
+  return e;
+}
 
 // Brackets the launches of one launcher with CUDA events when profiling is
 // on; `bytes` / `flops` are the algorithmic traffic and work of the launch.

@@ -20,27 +20,28 @@ namespace dflash {
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 static __device__ __align__(256) unsigned char g_attn_scratch[kNoAllocScratchBytes];
 
-// Device address of g_attn_scratch, looked up once per device.
-constexpr int kMaxDevices = 64;
-static void* g_scratch_ptr[kMaxDevices];
+// Device address of g_attn_scratch, looked up once per device.  Two host
+// threads making their first call on one device at the same moment both
+// look it up and store the same value.
+static std::atomic<void*> g_scratch_ptr[kMaxDevices];
 
 static dflash_status scratch_on_current_device(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+  const int dev = current_device_slot();
+  if (dev < 0) {
     fprintf(stderr, "dflash_block_attention_noalloc: no usable current device\n");
     return DFLASH_E_CUDA;
   }
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
+  void* p = g_scratch_ptr[dev].load(std::memory_order_relaxed);
+  if (!p) {
     const cudaError_t e = cudaGetSymbolAddress(&p, g_attn_scratch);
     if (e != cudaSuccess || !p) {
       fprintf(stderr, "dflash_block_attention_noalloc: cudaGetSymbolAddress failed: %s\n",
               cudaGetErrorString(e));
       return DFLASH_E_CUDA;
     }
-    g_scratch_ptr[dev] = p;
+    g_scratch_ptr[dev].store(p, std::memory_order_relaxed);
   }
-  *out = g_scratch_ptr[dev];
+  *out = p;
   return DFLASH_OK;
 }
 

@@ -331,11 +331,11 @@ DFLASH_API dflash_status dflash_block_attention_noalloc(int32_t batch, int32_t n
 
 /* ---- temperature-1 drafting and acceptance ------------------------------------
  * The pages run DFlash at temperature 1 ("DFlash benchmark results" report: an
- * average 4.03x) and say the drafter fills the block with sampled tokens and
- * the target accepts a draft token that matches its argmax "or sits within an
- * acceptance criterion" ("DFlash speculative decoding" glossary, section
- * "DFlash: architecture and workflow", stages 2 and 3); the criterion is not
- * stated.  These calls implement the standard speculative rejection rule,
+ * average 4.03x); at that temperature the drafter fills the block with
+ * sampled tokens, and besides an exact match with the target's argmax the
+ * target may also accept a draft token under a sampling rule that the page
+ * names but leaves unstated ("DFlash speculative decoding" glossary, section
+ * "DFlash: architecture and workflow", stages 2 and 3).  These calls implement the standard speculative rejection rule,
  * which keeps the output distributed exactly as sampling the target:
  *   d_j ~ p_j = softmax(drafter logits of slot j);
  *   d_j passes when u_j * p_j(d_j) < q_{j-1}(d_j), q_i = softmax(target logits
