@@ -33,7 +33,9 @@ Modules:
   ddtree    -- best-first heap tree builder, ancestor masks, tree accept walk
 
 Parity status: the transformer block composition (norm placement, SwiGLU,
-GQA head mapping inside a full layer) has no printed values on the pages;
-it is pinned by invariants and textbook special cases only.  See the
-test-suite docstrings for the pin of each function.
+GQA head mapping inside a full layer) and the draft pass (slot inputs, slot
+positions, the unmasked key set, the drafter's norms) have no printed values
+on the pages; they are pinned by invariants and closed-form special cases
+that reduce them to textbook routines.  See the test-suite docstrings for
+the pin of each function.
 """

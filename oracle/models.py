@@ -28,7 +28,7 @@ What the pages fix, and the reading taken where they are silent:
 """
 from __future__ import annotations
 
-from typing import Dict, List, Sequence
+from typing import Dict, List, Optional, Sequence
 
 import numpy as np
 
@@ -146,16 +146,20 @@ def inject_kv(w: Weights, shape, prec: Precision, dcache: KVCache,
 
 
 def draft_block_logits(w: Weights, shape, prec: Precision, dcache: KVCache,
-                       anchor: int, ctx_len: int, block_size: int) -> np.ndarray:
+                       anchor: int, ctx_len: int, block_size: int,
+                       pos0: Optional[int] = None) -> np.ndarray:
     """One block-diffusion draft pass; returns logits [B-1, V] of slots 1..B-1.
 
-    Slot j sits at position ctx_len + j.  Every slot attends to the injected
-    context rows 0..ctx_len-1 and to all B in-block rows (no mask).  The
-    in-block K/V are scratch and never enter the draft cache.
+    Slot j sits at position ctx_len + j (the frontier: the anchor is the
+    token at position P = ctx_len).  ``pos0`` overrides the position of
+    slot 0 (the tests use it to move the block against its context).  Every
+    slot attends to the injected context rows 0..ctx_len-1 and to all B
+    in-block rows (no mask).  The in-block K/V are scratch and never enter
+    the draft cache.
     """
     s = shape
     b = block_size
-    positions = ctx_len + np.arange(b)
+    positions = (ctx_len if pos0 is None else pos0) + np.arange(b)
     x = np.stack([w["tok_emb"][anchor]] + [w["draft.mask_emb"]] * (b - 1))
     for l in range(s.n_draft_layers):
         def attend_rows(q, k, v, l=l):

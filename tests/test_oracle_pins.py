@@ -6,6 +6,7 @@ closed forms, library routines for textbook special cases, invariants, and
 brute force on tiny inputs.  Chosen so that a plausible mistake (a dropped
 term, a sign, an index, a transposed operand) fails at least one of them.
 """
+import dataclasses
 import itertools
 import os
 
@@ -19,7 +20,8 @@ from oracle.ddtree import (build_tree, ddtree_generate, tree_accept, tree_verify
                            tree_commit, topk_logprobs)
 from oracle.decode import (Sequence1, accept_longest_prefix, dflash_generate, greedy_ar,
                            speedup_model)
-from oracle.models import KVCache, Weights, causal_visible, inject_kv, target_forward
+from oracle.models import (KVCache, Weights, causal_visible, draft_block_logits, inject_kv,
+                           target_forward)
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 TINY = wl.WORKLOADS["tiny_f32_e2e"]
@@ -306,6 +308,102 @@ def test_draft_block_is_bidirectional(tiny_w, tiny_prompt):
     # the injected context matters: an empty context gives other logits
     c = draft_block_logits(tiny_w, s, prec, seq.dcache, 5, 0, 4)
     assert np.abs(a - c).max() > 1e-6
+
+
+# --------------------------------------------------------------------------
+# the draft pass: closed-form special cases (Deep Research Report, "Key
+# points": B masked positions drafted in one pass over the injected context;
+# "Why DFlash beats EAGLE-3" item 3 and the MTP table: bidirectional block)
+# --------------------------------------------------------------------------
+
+def _one_layer_draft_shape(base):
+    return dataclasses.replace(base, name=base.name + "_d1", n_draft_layers=1, dtype="f32")
+
+
+def _draft_context(w, s, P, seed):
+    """Draft cache holding P injected context rows built from seeded capture
+    rows (the injection itself is pinned above)."""
+    rng = np.random.default_rng(seed)
+    hcat = rng.standard_normal((P, s.n_inject, s.d_model)) * 0.1
+    dc = KVCache(s.n_draft_layers, P + 64, s.n_kv_heads, s.head_dim)
+    inject_kv(w, s, nm.Precision("exact"), dc, hcat, np.arange(P))
+    return hcat, dc
+
+
+@pytest.mark.parametrize("base", [TINY.shape, wl.MINI_BF16], ids=["mha", "gqa4"])
+@pytest.mark.parametrize("zero", ["wq", "wk"])
+def test_draft_layer_with_zero_scores_is_a_mean_over_context_and_block(base, zero):
+    """W_q = 0 (or W_k = 0, which also zeroes the injected context keys) makes
+    every score 0, so every block slot takes the plain mean of all P injected
+    V rows and all B block V rows: no mask in the block or on the context.
+    With W_down = 0 the one draft layer gives x + W_o . mean(V) with
+    x = [E[anchor]; e_mask x (B-1)], block V = W_v . RMSNorm_g(x) (the draft
+    layer's own W_v and norm), context V = W_v . W_fuse . h_cat, query head h
+    reading KV head h // (H / H_kv); the logits of slots 1..B-1 are the shared
+    lm_head over the drafter's own final norm.  Non-unit norm gains make the
+    choice of gain visible."""
+    s = _one_layer_draft_shape(base)
+    d = s.d_model
+    rng = np.random.default_rng(21)
+    g_attn = (0.5 + rng.random(d)).astype(np.float32)
+    g_fin = (0.5 + rng.random(d)).astype(np.float32)
+    wshape = (s.q_dim, d) if zero == "wq" else (s.kv_dim, d)
+    over = {f"draft.layers.0.{zero}": np.zeros(wshape, np.float32),
+            "draft.layers.0.w_down": np.zeros((d, s.ffn_dim), np.float32),
+            "draft.layers.0.attn_norm": g_attn, "draft.final_norm": g_fin}
+    w = Weights(wl.SyntheticWeights(s).with_override(over))
+    P, B, anchor = 11, 6, 7
+    hcat, dc = _draft_context(w, s, P, 22)
+    got = draft_block_logits(w, s, nm.Precision("exact"), dc, anchor, P, B)
+    x = np.stack([w["tok_emb"][anchor]] + [w["draft.mask_emb"]] * (B - 1))
+    wv = w["draft.layers.0.wv"]
+    vb = (nm.rmsnorm(x, g_attn, s.rms_eps) @ wv.T).reshape(B, s.n_kv_heads, s.head_dim)
+    f = hcat.reshape(P, -1) @ w["draft.fuse"].T
+    vc = (f @ wv.T).reshape(P, s.n_kv_heads, s.head_dim)
+    mean = (vc.sum(0) + vb.sum(0)) / (P + B)
+    o = np.repeat(mean, s.n_heads // s.n_kv_heads, axis=0).reshape(s.q_dim)
+    x_out = x + o @ w["draft.layers.0.wo"].T
+    want = nm.rmsnorm(x_out[1:], g_fin, s.rms_eps) @ w["lm_head"].T
+    np.testing.assert_allclose(got, want, rtol=1e-9, atol=1e-11)
+
+
+def test_draft_logits_depend_on_relative_positions_only(tiny_w):
+    """RoPE makes every score a function of query position minus key
+    position.  Moving the injected context AND the block by the same offset
+    leaves the draft logits unchanged; moving the block alone changes them.
+    So the block sits at positions P + j against a context roped at 0..P-1."""
+    s = TINY.shape
+    P, B, anchor, off = 13, 5, 9, 500
+    prec = nm.Precision("exact")
+    hcat, c0 = _draft_context(tiny_w, s, P, 23)
+    ref = draft_block_logits(tiny_w, s, prec, c0, anchor, P, B)
+    big = KVCache(s.n_draft_layers, off + P, s.n_kv_heads, s.head_dim)
+    inject_kv(tiny_w, s, prec, big, hcat, off + np.arange(P))
+    c1 = KVCache(s.n_draft_layers, P, s.n_kv_heads, s.head_dim)
+    c1.k[:] = big.k[:, off:]
+    c1.v[:] = big.v[:, off:]
+    shifted = draft_block_logits(tiny_w, s, prec, c1, anchor, P, B, pos0=off + P)
+    np.testing.assert_allclose(shifted, ref, rtol=1e-9, atol=1e-9)
+    moved = draft_block_logits(tiny_w, s, prec, c0, anchor, P, B, pos0=P + 37)
+    assert np.abs(moved - ref).max() > 1e-4
+
+
+def test_draft_mask_slots_are_interchangeable():
+    """With a zero mask embedding, RMSNorm of slots 1..B-1 is 0, so their
+    queries, keys and values are 0; with W_q = 0 every slot averages the same
+    key set.  Slots 1..B-1 then enter and leave the layer identically, so
+    their logits are equal -- unless a mask (causal or otherwise) gives the
+    block slots different key sets."""
+    s = _one_layer_draft_shape(TINY.shape)
+    over = {"draft.mask_emb": np.zeros(s.d_model, np.float32),
+            "draft.layers.0.wq": np.zeros((s.q_dim, s.d_model), np.float32)}
+    w = Weights(wl.SyntheticWeights(s).with_override(over))
+    P, B = 9, 7
+    _, dc = _draft_context(w, s, P, 24)
+    got = draft_block_logits(w, s, nm.Precision("exact"), dc, 3, P, B)
+    for j in range(1, B - 1):
+        np.testing.assert_allclose(got[j], got[0], rtol=1e-12, atol=1e-12)
+    assert np.abs(got[0]).max() > 1e-3
 
 
 # --------------------------------------------------------------------------
