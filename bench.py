@@ -237,13 +237,17 @@ def run_reference(args, w: wl.Workload) -> None:
         times.append(sec)
         sampled.append(cpu_s)
     per_step = statistics.median(times)
-    info = smp.describe(statistics.median(sampled)) + f"; {args.steps} samples, median"
+    sample_s = statistics.median(sampled)
+    info = smp.describe(sample_s) + f"; {args.steps} samples, median"
     value = w.batch * 1.0 / per_step  # random-init weights: one verified token per sequence and step
+    # steps / ms_per_step describe what was timed: one bounded sample per
+    # step; the metric is extrapolated from it to a whole step of the workload
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": sample_s * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "extrapolated": True, "extrapolated_ms_per_workload_step": per_step * 1e3,
         "config": {"workload": w.name, "batch": w.batch, "prompt_len": w.prompt_len[0],
                    "block": w.block_size},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
@@ -356,6 +360,7 @@ def run_ours(args, w: wl.Workload) -> None:
     hbm, tflops, src = peaks()
     t_sus, t_src = sustained_tflops()
     g = prof["gemm_tc_kernel"]
+    gemm_step_bytes = g["bytes"] / max(args.prof_steps, 1)
     # one launch: algorithmic bytes / flops per launch over the mean launch time
     bound, achieved, peak, unit = gemm_roofline(g["bytes"] / max(g["n"], 1), g["flops"] / max(g["n"], 1),
                                                 g["ms"] / max(g["n"], 1), hbm, t_sus)
@@ -412,6 +417,32 @@ def run_ours(args, w: wl.Workload) -> None:
     if rank != 0:
         eng.close()
         return
+    weights = eng.weights
+    eng.close()
+    del eng
+    torch.cuda.empty_cache()
+    # the other bars of the step, measured in the same run (one GPU only: at
+    # N > 1 the replicas would repeat them)
+    extras = None
+    if world == 1 and not args.no_extras and w.name == "qwen3_8b_b1":
+        sx, wx = max(5, min(args.steps, 20)), 3
+        extras = {}
+        pts, clk = attn_op_points(min(args.steps, 10), wx, local)
+        head = next(pt for pt in pts if pt["ctx"] == 16384 and pt["batch"] == 32)
+        extras["attn_op"] = {
+            "kernel": ATTN_KERNELS, "headline": {"ctx": 16384, "batch": 32, "us": head["us"],
+                                                 "gbs": head["gbs"], "frac": head["frac"]},
+            "points": [{k: pt[k] for k in ("ctx", "batch", "us", "gbs", "frac")} for pt in pts],
+            "peak_gbs": hbm, "peak_source": src,
+            "l2": "256 MB buffer written before every timed call", "clocks": clk}
+        extras["b32"] = workload_steps(wl.WORKLOADS["qwen3_8b_b32"], sx, wx, 3, local,
+                                       weights=weights)[0]
+        del weights  # the Qwen-shaped weights are not needed past this point
+        torch.cuda.empty_cache()
+        extras["ddtree_b4"] = workload_steps(wl.WORKLOADS["llama31_8b_ddtree_b4"], sx, wx, 3,
+                                             local)[0]
+    else:
+        del weights
     cpu = None
     if not args.no_cpu_baseline:
         smp = OracleSample(w)
@@ -444,39 +475,49 @@ def run_ours(args, w: wl.Workload) -> None:
                      "peak_source": src if bound == "hbm" else t_src + " (sustained bf16)",
                      "bytes_per_launch": g["bytes"] / g["n"] if g["n"] else None,
                      "launches_per_step": g["launches_per_step"],
-                     "ms_per_step": g["ms_per_step"]},
+                     "ms_per_step": g["ms_per_step"],
+                     # the graph-replayed step: every GEMM byte of a step over the
+                     # whole step time (a lower bound on the GEMMs' own rate)
+                     "achieved_over_step": gemm_step_bytes / (step_ms / 1e3) / 1e9,
+                     "frac_over_step": gemm_step_bytes / (step_ms / 1e3) / 1e9 / hbm},
         "kernel_ms_per_step": {k: v["ms_per_step"] for k, v in prof.items()},
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": 4 * b,
                 "d2h_bytes_per_step": 4 * b * max(B, nmax) + 8 * b},
         "cpu_baseline": cpu,
     }
+    if extras is not None:
+        line.update(extras)
+        line["bars"] = {
+            "attention_hbm_frac": {f"ctx{pt['ctx']}_b{pt['batch']}": round(pt["frac"], 3)
+                                   for pt in extras["attn_op"]["points"] if pt["ctx"] >= 8192},
+            "b32_gemm_frac_sustained_live": extras["b32"]["gemm"]["frac_live"],
+            "b32_gemm_frac_sustained_over_step": extras["b32"]["gemm"]["frac_over_step"]}
     print(json.dumps(line))
-    eng.close()
 
 
 KERNEL_REV = "gemm-v5"
+ATTN_KERNELS = "attn_mma_kernel (+ attn_combine_kernel)"
 
 
-def run_attn_op(args) -> None:
+def attn_op_points(steps: int, warmup: int, local: int):
     """Block attention op (dflash_block_attention) over the grid of context
     lengths x batches: Q [b,16,32,128], K/V [b,8,ctx+16,128] bf16, block
-    visible without mask.  Each point: W warm-up calls, then K calls timed
-    one by one with CUDA events on the launching stream, a 256 MB buffer
-    written between calls so that every call starts with a cold L2; the
-    median is reported against the measured HBM peak."""
+    visible without mask.  Each point: `warmup` calls, then `steps` calls
+    timed one by one with CUDA events on the launching stream, a 256 MB
+    buffer written between calls so that every call starts with a cold L2;
+    the median against the measured HBM peak.  Returns (points, clocks)."""
     import torch
 
     from block_diffusion_speculative_injection_gb300 import capi
     from block_diffusion_speculative_injection_gb300.engine import device_operand
 
-    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
     H, HKV, HD = wl.ATTN_OP_HEADS
     BLK = 16
-    hbm, _, src = peaks()
+    hbm, _, _ = peaks()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
-    sampler = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    sampler = ClockSampler(local)
     points = []
     sampler.start()
     for ctx in wl.ATTN_OP_CTX:
@@ -487,10 +528,10 @@ def run_attn_op(args) -> None:
             out = torch.empty_like(q)
             need = capi.dflash_block_attention_workspace(b, H, HKV, ctx, BLK)
             ws = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
-            for _ in range(args.warmup):
+            for _ in range(warmup):
                 capi.dflash_block_attention(b, H, HKV, ctx, BLK, 0, q, k, v, out, ws)
             times = []
-            for _ in range(args.steps):
+            for _ in range(steps):
                 flush.fill_(1)
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
@@ -506,6 +547,20 @@ def run_attn_op(args) -> None:
                            "frac": gbs / hbm, "roofline_us": nbytes / (hbm * 1e9) * 1e6})
             del q, k, v, out, ws
     clocks = sampler.stop()
+    del flush
+    torch.cuda.empty_cache()
+    return points, clocks
+
+
+def run_attn_op(args) -> None:
+    """The block attention op grid as its own benchmark line (headline point:
+    the largest context and batch)."""
+    import torch
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    hbm, _, src = peaks()
+    points, clocks = attn_op_points(args.steps, args.warmup, local)
     head = next(pt for pt in points if pt["ctx"] == max(wl.ATTN_OP_CTX) and pt["batch"] == max(wl.ATTN_OP_BATCH))
     line = {
         "metric": "block attention op: achieved HBM bandwidth (Q [b,16,32,128] over ctx+16 keys, GQA 4:1)",
@@ -515,13 +570,95 @@ def run_attn_op(args) -> None:
         "config": {"workload": "attn_op", "points": f"ctx {list(wl.ATTN_OP_CTX)} x batch {list(wl.ATTN_OP_BATCH)}",
                    "headline_point": {"ctx": head["ctx"], "batch": head["batch"]},
                    "l2": "256 MB buffer written before every timed call"},
-        "roofline": {"bound": "hbm", "kernel": "attn_mma_kernel (+ attn_combine_kernel)", "achieved": head["gbs"],
+        "roofline": {"bound": "hbm", "kernel": ATTN_KERNELS, "achieved": head["gbs"],
                      "peak": hbm, "unit": "GB/s", "frac": head["gbs"] / hbm, "traffic": None,
                      "peak_source": src},
         "points": points,
         "clocks": clocks,
     }
     print(json.dumps(line))
+
+
+def workload_steps(w: wl.Workload, steps: int, warmup: int, prof_steps: int, local: int,
+                   weights=None):
+    """Graph-replayed steps of one workload on this GPU (the same step the
+    headline times: draft, verify, accept, injection; the tree step for a
+    DDTree workload).  Returns (summary, weights) so that a later workload of
+    the same model can reuse the uploaded weights."""
+    import torch
+
+    from block_diffusion_speculative_injection_gb300 import capi
+    from block_diffusion_speculative_injection_gb300.engine import DFlashEngine, capture_step_graph
+
+    B, b = w.block_size, w.batch
+    lens = wl.prompt_lengths(w)
+    tree = w.tree_budget > 0
+    nmax = w.tree_budget + 1 if tree else 0
+    total = warmup + steps + prof_steps + 6
+    max_ctx = max(lens) + B * (total + 2) + nmax + 64
+    eng = DFlashEngine(w.shape, B, b, max_ctx, max_rows=max(max(lens), b * max(B, nmax)),
+                       max_tree_nodes=nmax, seed=w.seed, weights=weights)
+    sid = eng.seq_ids(b)
+    eng.prefill(wl.prompts(w))
+
+    def one():
+        if tree:
+            eng.tree_step(sid, eng.next_anchor[:b], w.topk, w.tree_budget)
+        else:
+            eng.step(sid, eng.next_anchor[:b])
+
+    for _ in range(warmup):
+        one()
+    graph = capture_step_graph(eng, sid, tree=tree, topk=w.topk, budget=w.tree_budget)
+    for _ in range(2):
+        graph.replay()
+    stream = torch.cuda.current_stream()
+    gen = eng.gen_counts()
+    sampler = ClockSampler(local)
+    sampler.start()
+    torch.cuda.synchronize()
+    g0 = gen.clone()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(steps):
+        graph.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    emitted = int((gen - g0)[:b].sum().item())
+    step_ms = ms / steps
+    capi.dflash_profile(eng.ctx, True)
+    for _ in range(prof_steps):
+        one()
+    capi.dflash_profile(eng.ctx, False)
+    n, gms, gbytes, gflops = capi.dflash_profile_read(eng.ctx, capi.PROF_GEMM)
+    na, ams, _, _ = capi.dflash_profile_read(eng.ctx, capi.PROF_ATTN)
+    t_sus, t_src = sustained_tflops()
+    flops_step = gflops / max(prof_steps, 1)
+    gemm_ms_live = gms / max(prof_steps, 1)
+    out = {
+        "workload": w.name, "batch": b, "block": B, "steps": steps, "warmup": warmup,
+        "prompt_len": [min(lens), max(lens)], "tree_nodes": nmax or None,
+        "step_ms": step_ms, "tokens_per_s": emitted / (ms / 1e3), "tau": emitted / (steps * b),
+        "gemm": {"launches_per_step": n / max(prof_steps, 1), "tflop_per_step": flops_step / 1e12,
+                 "ms_per_step_live": gemm_ms_live,
+                 "tflops_live": flops_step / (gemm_ms_live / 1e3) / 1e12 if gemm_ms_live else None,
+                 "frac_live": (flops_step / (gemm_ms_live / 1e3) / 1e12 / t_sus) if gemm_ms_live else None,
+                 "tflops_over_step": flops_step / (step_ms / 1e3) / 1e12,
+                 "frac_over_step": flops_step / (step_ms / 1e3) / 1e12 / t_sus,
+                 "peak_tflops": t_sus, "peak_source": t_src + " (sustained bf16)"},
+        "attention_ms_per_step_live": ams / max(prof_steps, 1),
+        "clocks": clocks,
+        "timing": "CUDA-graph replays, CUDA events on the launching stream; live per-launch "
+                  "classes from an eager pass with an event pair around every launch",
+    }
+    weights = eng.weights
+    eng.close()
+    del eng, graph
+    torch.cuda.empty_cache()
+    return out, weights
 
 
 def run_spec_sample_op(args) -> None:
@@ -680,6 +817,9 @@ def main() -> None:
     ap.add_argument("--ar-steps", type=int, default=50)
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the attention-op grid, batch-32 and DDTree measurements that the "
+                         "default single-GPU run adds to its line")
     ap.add_argument("--no-graph", action="store_true",
                     help="time eager C-ABI calls instead of a CUDA-graph replay of the step")
     args = ap.parse_args()

@@ -83,6 +83,7 @@ _SIGS = {
     "dflash_plan_attention": ([_I, _I, _I, _I, _I, ctypes.c_int64, _I, _P], _I),
     "dflash_profile": ([_P, _I], _I),
     "dflash_debug_trace": ([_P, _P, ctypes.c_int64], _I),
+    "dflash_debug_trace_draft": ([_P, _P, ctypes.c_int64], _I),
     "dflash_profile_read": ([_P, _I, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double),
                              ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)], _I),
 }
@@ -329,3 +330,10 @@ def dflash_debug_trace(ctx, dst=None) -> None:
     """Registers (or clears with None) a [L][max_rows][d] fp32 residual trace."""
     nbytes = dst.numel() * dst.element_size() if dst is not None else 0
     _check(ctx, load().dflash_debug_trace(ctx, _ptr(dst), nbytes))
+
+
+def dflash_debug_trace_draft(ctx, dst=None) -> None:
+    """Registers (or clears with None) a [L_d][max_rows][d] fp32 residual trace
+    of the draft passes."""
+    nbytes = dst.numel() * dst.element_size() if dst is not None else 0
+    _check(ctx, load().dflash_debug_trace_draft(ctx, _ptr(dst), nbytes))

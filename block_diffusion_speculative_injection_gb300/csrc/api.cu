@@ -563,7 +563,8 @@ dflash_status dflash_draft_block(dflash_ctx* ctx, int32_t batch, const int32_t* 
     void* kc = static_cast<uint8_t*>(ctx->dkc) + off;
     void* vc = static_cast<uint8_t*>(ctx->dvc) + off;
     const void* next_gain = l + 1 < c.n_draft_layers ? ctx->dl[l + 1].attn_norm : nullptr;
-    s = run_layer(ctx, ctx->dl[l], rows, kc, vc, ab, next_gain, nullptr, 0, nullptr, st);
+    float* tr = ctx->dtrace ? ctx->dtrace + (size_t)l * c.max_rows * c.d_model : nullptr;
+    s = run_layer(ctx, ctx->dl[l], rows, kc, vc, ab, next_gain, nullptr, 0, tr, st);
   }
   ctx->pass_seq = save[0];
   ctx->pass_ctx = save[1];
@@ -761,6 +762,15 @@ dflash_status dflash_debug_trace(dflash_ctx* ctx, float* dst_dev, int64_t bytes)
   if (dst_dev && bytes < (int64_t)c.n_target_layers * c.max_rows * c.d_model * (int64_t)sizeof(float))
     return fail(ctx, DFLASH_E_CAPACITY, "trace buffer needs n_target_layers*max_rows*d_model floats");
   ctx->trace = dst_dev;
+  return DFLASH_OK;
+}
+
+dflash_status dflash_debug_trace_draft(dflash_ctx* ctx, float* dst_dev, int64_t bytes) {
+  if (!ctx) return DFLASH_E_INVALID_ARG;
+  const dflash_config& c = ctx->cfg;
+  if (dst_dev && bytes < (int64_t)c.n_draft_layers * c.max_rows * c.d_model * (int64_t)sizeof(float))
+    return fail(ctx, DFLASH_E_CAPACITY, "trace buffer needs n_draft_layers*max_rows*d_model floats");
+  ctx->dtrace = dst_dev;
   return DFLASH_OK;
 }
 

@@ -124,6 +124,7 @@ struct dflash_ctx {
 
 
   float* trace = nullptr;  // debug: residual after every target layer [L][max_rows][d]
+  float* dtrace = nullptr; // debug: residual after every draft layer [L_d][max_rows][d]
   bool pdl = true;  // programmatic dependent launch between this context's kernels
   int64_t launches = 0;
   std::string last_error;

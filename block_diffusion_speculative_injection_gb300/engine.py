@@ -273,7 +273,15 @@ class DFlashEngine:
 
     # -- one DDTree step -----------------------------------------------------
     def tree_step(self, seq_ids: torch.Tensor, anchors: torch.Tensor, topk: int, budget: int,
-                  want_logits: bool = False):
+                  want_logits: bool = False, tree_override: Optional[dict] = None,
+                  want_draft_logits: bool = False, before_commit=None):
+        """One DDTree step.  tree_override (tests: teacher forcing) replaces the
+        built tree with the caller's arrays before the verify pass: device
+        tensors tok, parent, depth [b][max_nodes] int32, anc [b][max_nodes]
+        [anc_words] int64 and n_nodes [b] int32, in the layout of
+        dtree_buffers; the drafter and the heap builder still run.
+        before_commit, if given, is called between the verify pass and the
+        accept call (tests snapshot the caches there)."""
         b = seq_ids.numel()
         B = self.B
         m = self.tree_mem
@@ -281,14 +289,27 @@ class DFlashEngine:
         ids = m["topk_ids"][: b * (B - 1) * topk]
         lps = m["topk_logp"][: b * (B - 1) * topk]
         block = self.block[: b * B]
-        capi.dflash_draft_block(self.ctx, b, seq_ids, anchors, block, topk, ids, lps, None)
+        dlog = None
+        if want_draft_logits:
+            dlog = torch.empty(b * (B - 1) * self.shape.vocab, dtype=torch.float32,
+                               device=self.device)
+        capi.dflash_draft_block(self.ctx, b, seq_ids, anchors, block, topk, ids, lps, dlog)
         capi.dtree_build(self.ctx, b, anchors, ids, lps, topk, budget, self.tree)
+        if tree_override is not None:
+            w = self.tree.anc_words
+            m["tok"][: b * n].copy_(tree_override["tok"].reshape(-1))
+            m["parent"][: b * n].copy_(tree_override["parent"].reshape(-1))
+            m["depth"][: b * n].copy_(tree_override["depth"].reshape(-1))
+            m["anc"][: b * n * w].copy_(tree_override["anc"].reshape(-1))
+            m["n_nodes"][:b].copy_(tree_override["n_nodes"].reshape(-1))
         argmax = self.argmax[: b * n]
         margin = self.margin[: b * n]
         vlog = None
         if want_logits:
             vlog = torch.empty(b * n * self.shape.vocab, dtype=torch.float32, device=self.device)
         capi.dtree_verify(self.ctx, b, seq_ids, self.tree, argmax, margin, vlog)
+        if before_commit is not None:
+            before_commit()
         emitted = self.emitted[: b * n]
         capi.dflash_accept_commit(self.ctx, b, seq_ids, None, argmax, self.tree,
                                   capi.DFLASH_ACCEPT_GREEDY, self.accept_len[:b],
@@ -303,6 +324,8 @@ class DFlashEngine:
                    emitted=emitted.view(b, n))
         if want_logits:
             res["logits"] = vlog.view(b, n, -1)
+        if want_draft_logits:
+            res["draft_logits"] = dlog.view(b, B - 1, -1)
         return res
 
     # -- whole generations ---------------------------------------------------

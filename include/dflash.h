@@ -272,6 +272,13 @@ DFLASH_API dflash_status dflash_debug_view(const dflash_ctx *ctx, const char *na
  * n_target_layers * max_rows * d_model floats.  NULL switches it off. */
 DFLASH_API dflash_status dflash_debug_trace(dflash_ctx *ctx, float *dst_dev, int64_t bytes);
 
+/* Debug: the same trace for draft passes: while dst_dev is set, every
+ * dflash_draft_block also writes the residual stream after each draft layer,
+ * fp32, to dst_dev[layer][row][d_model] (row = b*B + j of the pass).  bytes
+ * must cover n_draft_layers * max_rows * d_model floats.  NULL switches it
+ * off. */
+DFLASH_API dflash_status dflash_debug_trace_draft(dflash_ctx *ctx, float *dst_dev, int64_t bytes);
+
 DFLASH_API void dflash_destroy(dflash_ctx *ctx);
 
 /* ---- op-level block attention (no context) --------------------------------

@@ -9,9 +9,11 @@ decision against the stated rule, then commits the GPU's accepted rows.
 import numpy as np
 import torch
 
+import workloads as wl
+
 from oracle import numerics as nm
 from oracle.decode import Sequence1, accept_longest_prefix
-from oracle.ddtree import build_tree, tree_accept, tree_commit, tree_verify
+from oracle.ddtree import DraftTree, build_tree, tree_accept, tree_commit, tree_verify
 
 MARGIN = 1e-2
 
@@ -128,3 +130,118 @@ def replay_tree(eng, W, shape, prec, prompts, n_steps, topk, budget, atol, rtol,
         anchors = r["next_anchor"].clone()
     assert eng.lengths(b) == [sq.length for sq in seqs]
     return seqs
+
+
+# ---------------------------------------------------------------------------
+# teacher-forced draft trees (DDTree accept walk and KV compaction)
+# ---------------------------------------------------------------------------
+
+def forced_tree(anchor, path_tokens, next_token, n_nodes, vocab, depth_max):
+    """A draft tree whose greedy walk follows ``path_tokens`` (the target's
+    greedy continuation after ``anchor``) at slots s_j > j.
+
+    Node 0 is the anchor.  A decoy sibling (a token other than the path
+    token) takes the slot before path nodes 1 and 3, so the path sits at
+    s = 0, 2, 3, 5, 6, 7, ...: compaction then writes slots that are
+    themselves sources of earlier path rows (the overlapping case of the
+    two-phase gather).  The last path node gets a decoy child whose token
+    differs from ``next_token``, so the walk stops there.  The rest of the
+    budget is filled by decoy children of node 1, off the path."""
+    tok, parent, depth = [int(anchor)], [-1], [0]
+
+    def add(t, p):
+        tok.append(int(t) % vocab)
+        parent.append(p)
+        depth.append(depth[p] + 1)
+        return len(tok) - 1
+
+    cur = 0
+    for j, t in enumerate(path_tokens, start=1):
+        if j in (1, 3):
+            add(int(t) + 1, cur)
+        cur = add(t, cur)
+    assert depth[cur] <= depth_max
+    if depth[cur] < depth_max and len(tok) < n_nodes:
+        add(int(next_token) + 1, cur)
+    k = 2
+    while len(tok) < n_nodes:
+        add(int(path_tokens[0]) + k, 1)
+        k += 1
+    anc = []
+    for i, p in enumerate(parent):
+        anc.append((anc[p] if p >= 0 else 0) | (1 << i))
+    n = len(tok)
+    return DraftTree(tok, parent, depth, [0] * n, [0.0] * n, anc)
+
+
+def tree_arrays(trees, max_nodes, device="cuda"):
+    """The dtree_buffers arrays of oracle trees (one per sequence), on the
+    device, in the layout dtree_build writes."""
+    b, words = len(trees), (max_nodes + 63) // 64
+    tok = np.full((b, max_nodes), -1, np.int32)
+    parent = np.full((b, max_nodes), -1, np.int32)
+    depth = np.zeros((b, max_nodes), np.int32)
+    anc = np.zeros((b, max_nodes, words), np.int64)
+    for s, t in enumerate(trees):
+        n = t.n_nodes
+        tok[s, :n], parent[s, :n], depth[s, :n] = t.tok, t.parent, t.depth
+        for i in range(n):
+            for w in range(words):
+                v = (t.ancestors[i] >> (64 * w)) & ((1 << 64) - 1)
+                anc[s, i, w] = v - (1 << 64) if v >= (1 << 63) else v
+    n_nodes = np.array([t.n_nodes for t in trees], np.int32)
+    arr = dict(tok=tok, parent=parent, depth=depth, anc=anc, n_nodes=n_nodes)
+    return {k: torch.from_numpy(v).to(device) for k, v in arr.items()}
+
+
+def cache_band(eng, names_layers, b, lo, hi):
+    """Host copies of cache slots [lo, hi) of the first b sequences:
+    {(name, layer): array [b][H_kv][hi-lo][hd] float32}."""
+    return {(nm_, l): eng.debug_view(nm_, l)[:b, :, lo:hi].float().cpu().numpy()
+            for nm_, l in names_layers}
+
+
+# ---------------------------------------------------------------------------
+# full-size spot checks (the oracle computes sampled rows and layers only)
+# ---------------------------------------------------------------------------
+
+def lm_logits(shape, seed, h_final, gain_name="final_norm"):
+    """Oracle lm_head logits [n, V] of fp32 residual rows h_final [n, d]
+    after the final RMSNorm (norm gains are 1 in the synthetic weights; the
+    gain name only documents which norm it is), streaming the lm_head rows in
+    chunks so that the whole table is never held in fp64."""
+    assert gain_name in ("final_norm", "draft.final_norm")
+    sw = wl.SyntheticWeights(shape, seed)
+    h = np.atleast_2d(np.asarray(h_final, dtype=np.float64))
+    hn = nm.round_bf16(nm.rmsnorm(h, np.ones(shape.d_model), shape.rms_eps))
+    offs = sw.offsets("lm_head")
+    out = np.empty((h.shape[0], shape.vocab))
+    for c0 in range(0, shape.vocab, 16384):
+        rows = wl.pool_rows(sw.pool(), offs[c0: c0 + 16384], shape.d_model).astype(np.float64)
+        out[:, c0: c0 + len(rows)] = hn @ rows.T
+    return out
+
+
+def draft_inputs(shape, seed, anchor, block):
+    """Residual rows entering the first draft layer: the anchor's embedding,
+    then the mask embedding in every other slot."""
+    sw = wl.SyntheticWeights(shape, seed)
+    emb = wl.pool_rows(sw.pool(), sw.offsets("tok_emb")[[int(anchor)]], shape.d_model)[0]
+    return np.stack([emb] + [sw["draft.mask_emb"]] * (block - 1)).astype(np.float64)
+
+
+def draft_layer_forced(W, shape, l, x, ctx_len, ctx_k, ctx_v):
+    """Oracle draft layer l over all B block rows x [B, d] at positions
+    ctx_len .. ctx_len + B - 1, teacher-forced: every row sees the context
+    rows ctx_k / ctx_v [ctx_len, H_kv, hd] (the GPU's draft cache) and the
+    K/V of all B block rows (no mask)."""
+    from oracle.models import _layer
+    B = x.shape[0]
+
+    def attend_rows(q, k, v):
+        kk = np.concatenate([ctx_k, k])
+        vv = np.concatenate([ctx_v, v])
+        return np.stack([nm.attend(q[i], kk, vv) for i in range(B)])
+
+    return _layer(W, shape, nm.Precision("bf16emu"), f"draft.layers.{l}", x,
+                  ctx_len + np.arange(B), attend_rows)

@@ -15,6 +15,10 @@ the oracle exactly the inputs the GPU consumed at that point):
     residual;
   * the drafter's layer-0 cache rows written by KV injection from the GPU's
     capture rows (W_fuse, then Wk / Wv of draft layer 0, RoPE);
+  * every draft layer of the block draft pass over all 16 block rows,
+    teacher-forced on the GPU's draft residual trace (dflash_debug_trace_draft)
+    and the GPU's draft cache (no mask), and the draft logits / drafted tokens
+    from the GPU's final draft residual;
   * the accept decision against the stated rule.
 Tolerance: max-abs 2e-2, relative 1e-2 (bf16 path); argmax exact where the
 oracle's top-1/top-2 margin exceeds 1e-2.
@@ -28,7 +32,8 @@ from oracle import numerics as nm
 from oracle.decode import accept_longest_prefix
 from oracle.models import Weights, _layer
 
-from gpu_replay import check_argmax, check_close
+from gpu_replay import (check_argmax, check_close, draft_inputs, draft_layer_forced,
+                        lm_logits)
 
 pytestmark = pytest.mark.gpu
 ATOL, RTOL = 2e-2, 1e-2
@@ -51,10 +56,15 @@ def run():
     dv0 = eng.debug_view("dv_cache", 0)[0].float().cpu().numpy()
     from block_diffusion_speculative_injection_gb300 import capi
     trace = torch.zeros(w.shape.n_layers, P, w.shape.d_model, dtype=torch.float32, device="cuda")
+    dtrace = torch.zeros(w.shape.n_draft_layers, P, w.shape.d_model, dtype=torch.float32,
+                         device="cuda")
     capi.dflash_debug_trace(eng.ctx, trace)
+    capi.dflash_debug_trace_draft(eng.ctx, dtrace)
+    anchor = int(anchors[0].item())
     out, dlog, vlog, margin = eng.step(sid, anchors, want_logits=True)
     torch.cuda.synchronize()
     capi.dflash_debug_trace(eng.ctx, None)
+    capi.dflash_debug_trace_draft(eng.ctx, None)
     r = dict(
         w=w, prompt=prompt, P=P,
         block=out.block[0].cpu().numpy(), argmax=out.argmax[0].cpu().numpy(),
@@ -67,6 +77,10 @@ def run():
         v_cache={l: eng.debug_view("v_cache", l)[0, :, : P + 16].float().cpu().numpy()
                  for l in LAYERS},
         trace=trace[:, :16].cpu().numpy(),
+        anchor=anchor, dtrace=dtrace[:, :16].cpu().numpy(),
+        dctx={l: (eng.debug_view("dk_cache", l)[0, :, :P].float().cpu().numpy().transpose(1, 0, 2),
+                  eng.debug_view("dv_cache", l)[0, :, :P].float().cpu().numpy().transpose(1, 0, 2))
+              for l in range(w.shape.n_draft_layers)},
         length=eng.lengths(1)[0],
         dk_after=eng.debug_view("dk_cache", 0)[0, :, : P + 16].float().cpu().numpy(),
         dv_after=eng.debug_view("dv_cache", 0)[0, :, : P + 16].float().cpu().numpy(),
@@ -177,3 +191,30 @@ def test_draft_injection_cache_rows(run):
     check_close(run["dv_after"][:, pos].transpose(1, 0, 2), v, ATOL, RTOL, "injected draft V")
     # prompt rows injected at prefill are untouched by the step
     np.testing.assert_array_equal(run["dk_after"][:, : run["P"]], run["dk0"][:, : run["P"]])
+
+
+@pytest.mark.parametrize("l", [0, 1, 2, 3, 4])
+def test_draft_layer_teacher_forced(run, l):
+    """Draft layer l over the 16 block rows [anchor, mask x 15] at positions
+    P..P+15: input = the GPU's fp32 residual after draft layer l-1 (the
+    embeddings for layer 0), keys = the GPU's draft cache rows 0..P-1 (the
+    injected context) plus the block's own K/V, no mask; output against the
+    GPU's residual after layer l."""
+    s = run["w"].shape
+    P = run["P"]
+    x = (draft_inputs(s, run["w"].seed, run["anchor"], 16) if l == 0
+         else run["dtrace"][l - 1].astype(np.float64))
+    kc, vc = run["dctx"][l]
+    y = draft_layer_forced(run["W"], s, l, x, P, kc, vc)
+    run["W"]._cache.clear()
+    check_close(run["dtrace"][l], y, ATOL, RTOL, f"draft layer {l}")
+
+
+def test_draft_logits_and_argmax(run):
+    """The drafter's final norm and the shared lm_head over the GPU's final
+    draft residual of slots 1..15, against the GPU's draft logits; the
+    drafted tokens are their argmax."""
+    s = run["w"].shape
+    lg = lm_logits(s, run["w"].seed, run["dtrace"][-1][1:], "draft.final_norm")
+    check_close(run["dlog"], lg, ATOL, RTOL, "draft logits")
+    check_argmax(run["block"][1:], lg, "drafted tokens")

@@ -23,9 +23,10 @@ import workloads as wl
 from oracle import numerics as nm
 from oracle.ddtree import DraftTree, build_tree, tree_accept
 from oracle.decode import accept_longest_prefix
-from oracle.models import Weights, _layer
+from oracle.models import KVCache, Weights, _layer, inject_kv
 
-from gpu_replay import check_argmax, check_close
+from gpu_replay import (cache_band, check_argmax, check_close, draft_inputs, draft_layer_forced,
+                        forced_tree, lm_logits, tree_arrays)
 
 pytestmark = pytest.mark.gpu
 ATOL, RTOL = 2e-2, 1e-2
@@ -56,6 +57,7 @@ def _lm_logits(shape, seed, h_final):
 # batch 32, ragged
 # ---------------------------------------------------------------------------
 B32_LAYERS = (1, 18, 35)
+B32_DRAFT_LAYERS = (0, 4)
 
 
 @pytest.fixture(scope="module")
@@ -70,10 +72,14 @@ def b32():
     anchors = eng.prefill(prompts)
     trace = torch.zeros(w.shape.n_layers, eng.max_rows, w.shape.d_model, dtype=torch.float32,
                         device="cuda")
+    dtrace = torch.zeros(w.shape.n_draft_layers, eng.max_rows, w.shape.d_model,
+                         dtype=torch.float32, device="cuda")
     capi.dflash_debug_trace(eng.ctx, trace)
+    capi.dflash_debug_trace_draft(eng.ctx, dtrace)
     out, dlog, vlog, _ = eng.step(sid, anchors, want_logits=True)
     torch.cuda.synchronize()
     capi.dflash_debug_trace(eng.ctx, None)
+    capi.dflash_debug_trace_draft(eng.ctx, None)
     picks = [(3, 0), (17, 9)]  # (sequence, block row)
     r = dict(w=w, prompts=prompts, lens=lens, picks=picks,
              block=out.block.cpu().numpy(), argmax=out.argmax.cpu().numpy(),
@@ -81,14 +87,21 @@ def b32():
              length=eng.lengths(w.batch),
              vlog={(s, j): vlog[s, j].cpu().numpy() for s, j in picks},
              trace={(s, j): trace[:, s * 16 + j].cpu().numpy() for s, j in picks},
-             cache={})
+             cache={},
+             dtrace={s: dtrace[:, s * 16:(s + 1) * 16].cpu().numpy() for s, _ in picks},
+             dlog={s: dlog[s].cpu().numpy() for s, _ in picks},
+             dctx={(s, l): (eng.debug_view("dk_cache", l)[s, :, :lens[s]].float().cpu().numpy()
+                            .transpose(1, 0, 2),
+                            eng.debug_view("dv_cache", l)[s, :, :lens[s]].float().cpu().numpy()
+                            .transpose(1, 0, 2))
+                   for s, _ in picks for l in B32_DRAFT_LAYERS})
     for s, j in picks:
         n = lens[s] + 16
         for l in (0,) + B32_LAYERS:
             r["cache"][(s, l)] = (eng.debug_view("k_cache", l)[s, :, :n].float().cpu().numpy().transpose(1, 0, 2),
                                   eng.debug_view("v_cache", l)[s, :, :n].float().cpu().numpy().transpose(1, 0, 2))
     eng.close()
-    del eng, trace, vlog
+    del eng, trace, dtrace, vlog, dlog
     torch.cuda.empty_cache()
     r["W"] = Weights(wl.SyntheticWeights(w.shape, w.seed))
     return r
@@ -135,6 +148,28 @@ def test_b32_final_logits(b32):
         lg = _lm_logits(w.shape, w.seed, b32["trace"][(s, j)][-1].astype(np.float64))
         check_close(b32["vlog"][(s, j)], lg, ATOL, RTOL, f"seq {s} row {j} logits")
         check_argmax([b32["argmax"][s, j]], lg[None, :], f"seq {s} row {j} argmax")
+
+
+@pytest.mark.parametrize("l", B32_DRAFT_LAYERS)
+def test_b32_draft_layers_teacher_forced(b32, l):
+    """Draft layer l of two sequences' blocks (16 rows each, ragged contexts),
+    teacher-forced on the GPU's draft residual trace and draft cache."""
+    w = b32["w"]
+    for s, _ in b32["picks"]:
+        P = b32["lens"][s]
+        x = (draft_inputs(w.shape, w.seed, b32["block"][s, 0], 16) if l == 0
+             else b32["dtrace"][s][l - 1].astype(np.float64))
+        y = draft_layer_forced(b32["W"], w.shape, l, x, P, *b32["dctx"][(s, l)])
+        b32["W"]._cache.clear()
+        check_close(b32["dtrace"][s][l], y, ATOL, RTOL, f"seq {s} draft layer {l}")
+
+
+def test_b32_draft_logits_and_argmax(b32):
+    w = b32["w"]
+    for s, _ in b32["picks"]:
+        lg = lm_logits(w.shape, w.seed, b32["dtrace"][s][-1][1:], "draft.final_norm")
+        check_close(b32["dlog"][s], lg, ATOL, RTOL, f"seq {s} draft logits")
+        check_argmax(b32["block"][s, 1:], lg, f"seq {s} drafted tokens")
 
 
 # ---------------------------------------------------------------------------
@@ -267,3 +302,144 @@ def test_tree_accept_walk_and_compaction(tree):
                     np.testing.assert_array_equal(tree["post"][l][which][s, :, P + j],
                                                   tree["pre"][l][which][s, :, P + node])
             np.testing.assert_array_equal(tree["post"][l][0][s, :, :P], tree["pre"][l][0][s, :, :P])
+
+
+# ---------------------------------------------------------------------------
+# DDTree commit at full size: a teacher-forced tree (the drafter's own trees
+# are never accepted with random weights).  The path carries the target's
+# greedy continuation (GPU AR decoding) at slots s = 0, 2, 3, 5, 6, ... (decoy
+# siblings before path nodes 1 and 3), so compaction writes rows that are
+# sources of earlier path rows.
+# ---------------------------------------------------------------------------
+FORCED_PATH = 5
+FORCED_DRAFT_LAYERS = (0, 4)
+
+
+@pytest.fixture(scope="module")
+def forced():
+    from block_diffusion_speculative_injection_gb300 import capi
+    from block_diffusion_speculative_injection_gb300.engine import DFlashEngine
+    w = wl.WORKLOADS["llama31_8b_ddtree_b4"]
+    s, b = w.shape, w.batch
+    prompts = wl.prompts(w)
+    P = len(prompts[0])
+    nmax = w.tree_budget + 1
+    eng = DFlashEngine(s, 16, b, P + nmax + 64, max_rows=P, max_tree_nodes=nmax)
+    ar = eng.generate(prompts, FORCED_PATH + 3, mode="ar")
+    sid = eng.seq_ids(b)
+    anchors = eng.prefill(prompts)
+    torch.cuda.synchronize()
+    assert anchors.tolist() == [a[0] for a in ar]
+    trees = [forced_tree(ar[q][0], ar[q][1:1 + FORCED_PATH], ar[q][1 + FORCED_PATH], nmax,
+                         s.vocab, 15) for q in range(b)]
+    tl = [(n, l) for l in range(s.n_layers) for n in ("k_cache", "v_cache")]
+    lo, hi = P - 2, P + nmax
+    snap = {}
+    r = eng.tree_step(sid, anchors, w.topk, w.tree_budget, tree_override=tree_arrays(trees, nmax),
+                      before_commit=lambda: snap.update(cache_band(eng, tl, b, lo, hi)))
+    torch.cuda.synchronize()
+    out = {k: v.cpu().numpy() for k, v in r.items()}
+    post = cache_band(eng, tl, b, lo, hi)
+    dl = [(n, l) for l in range(s.n_draft_layers) for n in ("dk_cache", "dv_cache")]
+    dpost = cache_band(eng, dl, b, P, P + FORCED_PATH + 1)
+    capture = eng.debug_view("capture")[: b * nmax].float().cpu().numpy()
+    lengths = eng.lengths(b)
+    # the next draft pass, over the committed and injected path
+    dtrace = torch.zeros(s.n_draft_layers, eng.max_rows, s.d_model, dtype=torch.float32,
+                         device="cuda")
+    capi.dflash_debug_trace_draft(eng.ctx, dtrace)
+    anchors2 = r["next_anchor"][:b].clone()
+    dlog = torch.empty(b * 15 * s.vocab, dtype=torch.float32, device="cuda")
+    capi.dflash_draft_block(eng.ctx, b, sid, anchors2, eng.block[: b * 16], 0, None, None, dlog)
+    torch.cuda.synchronize()
+    capi.dflash_debug_trace_draft(eng.ctx, None)
+    q0 = int(np.argmax(out["accept_len"][:b]))  # the longest accepted path
+    P2 = lengths[q0]
+    res = dict(w=w, P=P, lo=lo, nmax=nmax, trees=trees, out=out, snap=snap, post=post,
+               dpost=dpost, capture=capture, lengths=lengths, q0=q0, P2=P2,
+               anchor2=int(anchors2[q0].item()),
+               dtrace=dtrace[:, q0 * 16:(q0 + 1) * 16].cpu().numpy(),
+               dlog=dlog.view(b, 15, -1)[q0].cpu().numpy(),
+               dblock=eng.block[q0 * 16:(q0 + 1) * 16].cpu().numpy(),
+               dctx={l: (eng.debug_view("dk_cache", l)[q0, :, :P2].float().cpu().numpy()
+                         .transpose(1, 0, 2),
+                         eng.debug_view("dv_cache", l)[q0, :, :P2].float().cpu().numpy()
+                         .transpose(1, 0, 2)) for l in FORCED_DRAFT_LAYERS})
+    eng.close()
+    del eng, dtrace, dlog
+    torch.cuda.empty_cache()
+    res["W"] = Weights(wl.SyntheticWeights(s, w.seed))
+    return res
+
+
+def _forced_path(r, q):
+    t = r["trees"][q]
+    return tree_accept(t, [int(v) for v in r["out"]["argmax"][q, : t.n_nodes]])
+
+
+def test_forced_tree_walk_full_size(forced):
+    best = 0
+    for q in range(forced["w"].batch):
+        t = forced["trees"][q]
+        n = t.n_nodes
+        assert list(forced["out"]["tok"][q, :n]) == t.tok
+        a, path, emitted = _forced_path(forced, q)
+        assert a == int(forced["out"]["accept_len"][q])
+        assert emitted == [int(v) for v in forced["out"]["emitted"][q] if v >= 0]
+        assert forced["lengths"][q] == forced["P"] + a + 1
+        assert path[:4] == [0, 2, 3, 5][: a + 1]
+        best = max(best, a)
+    assert best >= 3, "no forced path was accepted"
+
+
+def test_forced_tree_compaction_full_size(forced):
+    """Every target layer: committed row P + j is the pre-commit row P + s_j,
+    bit for bit; rows before P and past the path are untouched."""
+    P, lo = forced["P"], forced["lo"]
+    for q in range(forced["w"].batch):
+        _, path, _ = _forced_path(forced, q)
+        for (name, l), pre in forced["snap"].items():
+            post = forced["post"][(name, l)][q]
+            for j, node in enumerate(path):
+                np.testing.assert_array_equal(post[:, P + j - lo], pre[q][:, P + node - lo],
+                                              err_msg=f"seq {q} {name} {l} row {j}")
+            np.testing.assert_array_equal(post[:, : P - lo], pre[q][:, : P - lo])
+            np.testing.assert_array_equal(post[:, P + len(path) - lo:],
+                                          pre[q][:, P + len(path) - lo:])
+
+
+def test_forced_tree_injection_full_size(forced):
+    """Draft cache rows P .. P + a of every draft layer hold the injection of
+    the captured rows of the accepted nodes s_j at positions P + j."""
+    w, P = forced["w"], forced["P"]
+    s = w.shape
+    prec = nm.Precision("bf16emu")
+    for q in range(w.batch):
+        a, path, _ = _forced_path(forced, q)
+        rows = forced["capture"][q * forced["nmax"] + np.array(path)].astype(np.float64)
+        pos = P + np.arange(a + 1)
+        dc = KVCache(s.n_draft_layers, P + a + 1, s.n_kv_heads, s.head_dim)
+        inject_kv(forced["W"], s, prec, dc, rows, pos)
+        for l in range(s.n_draft_layers):
+            gk = forced["dpost"][("dk_cache", l)][q][:, : a + 1].transpose(1, 0, 2)
+            gv = forced["dpost"][("dv_cache", l)][q][:, : a + 1].transpose(1, 0, 2)
+            check_close(gk, dc.k[l, pos], ATOL, RTOL, f"seq {q} draft layer {l} K")
+            check_close(gv, dc.v[l, pos], ATOL, RTOL, f"seq {q} draft layer {l} V")
+    forced["W"]._cache.clear()
+
+
+@pytest.mark.parametrize("l", FORCED_DRAFT_LAYERS)
+def test_next_draft_layers_after_tree_commit(forced, l):
+    w = forced["w"]
+    x = (draft_inputs(w.shape, w.seed, forced["anchor2"], 16) if l == 0
+         else forced["dtrace"][l - 1].astype(np.float64))
+    y = draft_layer_forced(forced["W"], w.shape, l, x, forced["P2"], *forced["dctx"][l])
+    forced["W"]._cache.clear()
+    check_close(forced["dtrace"][l], y, ATOL, RTOL, f"next draft layer {l}")
+
+
+def test_next_draft_logits_after_tree_commit(forced):
+    w = forced["w"]
+    lg = lm_logits(w.shape, w.seed, forced["dtrace"][-1][1:], "draft.final_norm")
+    check_close(forced["dlog"], lg, ATOL, RTOL, "next draft logits")
+    check_argmax(forced["dblock"][1:], lg, "next drafted tokens")
