@@ -84,6 +84,7 @@ _SIGS = {
     "dflash_profile": ([_P, _I], _I),
     "dflash_debug_trace": ([_P, _P, ctypes.c_int64], _I),
     "dflash_debug_trace_draft": ([_P, _P, ctypes.c_int64], _I),
+    "dflash_debug_trace_draft_attn": ([_P, _P, _P, ctypes.c_int64], _I),
     "dflash_profile_read": ([_P, _I, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double),
                              ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)], _I),
 }
@@ -337,3 +338,11 @@ def dflash_debug_trace_draft(ctx, dst=None) -> None:
     of the draft passes."""
     nbytes = dst.numel() * dst.element_size() if dst is not None else 0
     _check(ctx, load().dflash_debug_trace_draft(ctx, _ptr(dst), nbytes))
+
+
+def dflash_debug_trace_draft_attn(ctx, q=None, attn=None) -> None:
+    """Registers (or clears with None) per-draft-layer copies of the roped
+    queries and of the attention output, [L_d][max_rows][H*hd] each."""
+    t = q if q is not None else attn
+    nbytes = t.numel() * t.element_size() if t is not None else 0
+    _check(ctx, load().dflash_debug_trace_draft_attn(ctx, _ptr(q), _ptr(attn), nbytes))

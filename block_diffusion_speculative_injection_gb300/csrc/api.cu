@@ -195,7 +195,8 @@ static EpiArgs epi_base(dflash_ctx* ctx, int kind) {
 
 static dflash_status run_layer(dflash_ctx* ctx, const LayerW& w, int rows, void* kc, void* vc,
                                const AttnArgs& attn_base, const void* next_gain, void* capture,
-                               int cap_slot, float* trace, cudaStream_t st) {
+                               int cap_slot, float* trace, cudaStream_t st, void* copy_q = nullptr,
+                               void* copy_ao = nullptr) {
   const dflash_config& c = ctx->cfg;
   const int d = c.d_model, qd = c.n_heads * c.head_dim, kvd = c.n_kv_heads * c.head_dim;
   int sp = 1;
@@ -209,6 +210,10 @@ static dflash_status run_layer(dflash_ctx* ctx, const LayerW& w, int rows, void*
   a.kc = kc;
   a.vc = vc;
   DF_TRY(attention(ctx, a, st));
+  // debug copies of the attention inputs / outputs (dflash_debug_trace_draft_attn)
+  const size_t qbytes = (size_t)rows * qd * ctx->esize;
+  if (copy_q) DF_CUDA_TRY(ctx, cudaMemcpyAsync(copy_q, ctx->qb, qbytes, cudaMemcpyDeviceToDevice, st));
+  if (copy_ao) DF_CUDA_TRY(ctx, cudaMemcpyAsync(copy_ao, ctx->ao, qbytes, cudaMemcpyDeviceToDevice, st));
   EpiArgs er = epi_base(ctx, kEpiResid);
   GemmSegs o{{w.wo}, {d}, 1};
   DF_TRY(gemm(ctx, ctx->ao, rows, qd, o, er, 16, &sp, st));
@@ -564,7 +569,10 @@ dflash_status dflash_draft_block(dflash_ctx* ctx, int32_t batch, const int32_t* 
     void* vc = static_cast<uint8_t*>(ctx->dvc) + off;
     const void* next_gain = l + 1 < c.n_draft_layers ? ctx->dl[l + 1].attn_norm : nullptr;
     float* tr = ctx->dtrace ? ctx->dtrace + (size_t)l * c.max_rows * c.d_model : nullptr;
-    s = run_layer(ctx, ctx->dl[l], rows, kc, vc, ab, next_gain, nullptr, 0, tr, st);
+    const size_t qoff = (size_t)l * c.max_rows * c.n_heads * c.head_dim * ctx->esize;
+    void* cq = ctx->dtrace_q ? static_cast<uint8_t*>(ctx->dtrace_q) + qoff : nullptr;
+    void* cao = ctx->dtrace_ao ? static_cast<uint8_t*>(ctx->dtrace_ao) + qoff : nullptr;
+    s = run_layer(ctx, ctx->dl[l], rows, kc, vc, ab, next_gain, nullptr, 0, tr, st, cq, cao);
   }
   ctx->pass_seq = save[0];
   ctx->pass_ctx = save[1];
@@ -774,6 +782,20 @@ dflash_status dflash_debug_trace_draft(dflash_ctx* ctx, float* dst_dev, int64_t 
   return DFLASH_OK;
 }
 
+dflash_status dflash_debug_trace_draft_attn(dflash_ctx* ctx, void* q_dev, void* attn_dev,
+                                            int64_t bytes_each) {
+  if (!ctx) return DFLASH_E_INVALID_ARG;
+  const dflash_config& c = ctx->cfg;
+  const int64_t need =
+      (int64_t)c.n_draft_layers * c.max_rows * c.n_heads * c.head_dim * (int64_t)ctx->esize;
+  if ((q_dev || attn_dev) && bytes_each < need)
+    return fail(ctx, DFLASH_E_CAPACITY,
+                "each trace buffer needs n_draft_layers*max_rows*n_heads*head_dim elements");
+  ctx->dtrace_q = q_dev;
+  ctx->dtrace_ao = attn_dev;
+  return DFLASH_OK;
+}
+
 dflash_status dflash_profile(dflash_ctx* ctx, int32_t enable) {
   if (!ctx) return DFLASH_E_INVALID_ARG;
   if (enable) {
@@ -836,6 +858,11 @@ dflash_status dflash_debug_view(const dflash_ctx* ctx, const char* name, int32_t
   if (n == "gen_count") {
     *dev_ptr = ctx->gen_count;
     *bytes = (int64_t)c.max_batch * sizeof(int32_t);
+    return DFLASH_OK;
+  }
+  if (n == "fused") {
+    *dev_ptr = ctx->fb;
+    *bytes = (int64_t)c.max_rows * c.d_model * ctx->esize;
     return DFLASH_OK;
   }
   if (n == "capture") {

@@ -125,6 +125,8 @@ struct dflash_ctx {
 
   float* trace = nullptr;  // debug: residual after every target layer [L][max_rows][d]
   float* dtrace = nullptr; // debug: residual after every draft layer [L_d][max_rows][d]
+  void* dtrace_q = nullptr;  // debug: roped Q of every draft layer [L_d][max_rows][H*hd]
+  void* dtrace_ao = nullptr; // debug: attention output of every draft layer, same layout
   bool pdl = true;  // programmatic dependent launch between this context's kernels
   int64_t launches = 0;
   std::string last_error;

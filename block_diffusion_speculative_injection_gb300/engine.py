@@ -164,6 +164,8 @@ class DFlashEngine:
         s = self.shape
         if name == "capture":
             return t.view(self.max_rows, s.n_inject, s.d_model)
+        if name == "fused":
+            return t.view(self.max_rows, s.d_model)
         return t.view(self.max_batch, s.n_kv_heads, self.cfg.max_ctx, s.head_dim)
 
     def prefill(self, prompts: Sequence[np.ndarray], chunk: Optional[int] = None) -> torch.Tensor:

@@ -259,6 +259,8 @@ DFLASH_API int64_t dflash_launch_count(const dflash_ctx *ctx);
  *   "k_cache"/"v_cache"   target layer `layer`: [max_batch][n_kv_heads][max_ctx][head_dim]
  *   "dk_cache"/"dv_cache" draft layer `layer`: same layout
  *   "capture"             [max_rows][n_inject][d_model] (row = b*q + j of the last pass)
+ *   "fused"               [max_rows][d_model]: the fused feature F = W_fuse h_cat of the
+ *                         rows of the last dflash_inject_kv (row order of that call)
  *   "gen_count"           [max_batch] int32: tokens emitted per slot since its reset
  *                         (prefill counts its first token; a step counts a + 1)
  * Element type = the storage dtype unless stated.  *bytes receives the view's size. */
@@ -278,6 +280,15 @@ DFLASH_API dflash_status dflash_debug_trace(dflash_ctx *ctx, float *dst_dev, int
  * must cover n_draft_layers * max_rows * d_model floats.  NULL switches it
  * off. */
 DFLASH_API dflash_status dflash_debug_trace_draft(dflash_ctx *ctx, float *dst_dev, int64_t bytes);
+
+/* Debug: while set, every dflash_draft_block also copies, per draft layer, the
+ * roped queries (q_dev) and the attention output (attn_dev) of the pass, in the
+ * storage dtype, to [layer][row][n_heads*head_dim] (row = b*B + j); each buffer
+ * must hold n_draft_layers * max_rows * n_heads * head_dim elements (bytes_each).
+ * Either may be NULL; both NULL switch it off.  With these a test can check the
+ * attention of a draft layer on the exact inputs the kernel saw. */
+DFLASH_API dflash_status dflash_debug_trace_draft_attn(dflash_ctx *ctx, void *q_dev, void *attn_dev,
+                                                       int64_t bytes_each);
 
 DFLASH_API void dflash_destroy(dflash_ctx *ctx);
 

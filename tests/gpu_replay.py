@@ -230,18 +230,61 @@ def draft_inputs(shape, seed, anchor, block):
     return np.stack([emb] + [sw["draft.mask_emb"]] * (block - 1)).astype(np.float64)
 
 
-def draft_layer_forced(W, shape, l, x, ctx_len, ctx_k, ctx_v):
-    """Oracle draft layer l over all B block rows x [B, d] at positions
-    ctx_len .. ctx_len + B - 1, teacher-forced: every row sees the context
-    rows ctx_k / ctx_v [ctx_len, H_kv, hd] (the GPU's draft cache) and the
-    K/V of all B block rows (no mask)."""
+def check_draft_layer(W, shape, l, x, ctx_len, ctx_k, ctx_v, q_gpu, attn_gpu, out_gpu, what,
+                      atol=2e-2, rtol=1e-2):
+    """Teacher-forced check of draft layer l over all B block rows, in three
+    well-conditioned stages (each gets the exact inputs the GPU consumed):
+      1. the roped queries: the oracle's, from the block rows x [B, d] at
+         positions ctx_len .., against the GPU's q_gpu [B, H*hd];
+      2. the attention: the GPU's queries over the context rows ctx_k / ctx_v
+         [ctx_len, H_kv, hd] (the GPU's draft cache) and the block's own K/V
+         (no mask), against the GPU's attention output attn_gpu [B, H*hd];
+      3. the rest of the layer (O projection, residual, FFN) from the GPU's
+         attention output, against the GPU's residual after the layer.
+    The injected context keys of a random-init drafter are large, so its
+    softmax is close to a hard maximum: one bf16 rounding of a query element
+    that lands on the other side of a rounding boundary can move weight
+    between two near-tied keys.  Stage 2 therefore uses the GPU's queries."""
     from oracle.models import _layer
     B = x.shape[0]
+    rec = {}
+    G = shape.n_heads // shape.n_kv_heads
+    qg = np.asarray(q_gpu, dtype=np.float64).reshape(B, shape.n_heads, shape.head_dim)
 
     def attend_rows(q, k, v):
+        rec["q"] = q
         kk = np.concatenate([ctx_k, k])
         vv = np.concatenate([ctx_v, v])
-        return np.stack([nm.attend(q[i], kk, vv) for i in range(B)])
+        rec["attn"] = np.stack([nm.attend(qg[i], kk, vv) for i in range(B)])
+        assert kk.shape[1] * G == shape.n_heads
+        return np.asarray(attn_gpu, dtype=np.float64).reshape(B, shape.n_heads, shape.head_dim)
 
-    return _layer(W, shape, nm.Precision("bf16emu"), f"draft.layers.{l}", x,
-                  ctx_len + np.arange(B), attend_rows)
+    y = _layer(W, shape, nm.Precision("bf16emu"), f"draft.layers.{l}", x,
+               ctx_len + np.arange(B), attend_rows)
+    check_close(q_gpu, rec["q"].reshape(B, -1), atol, rtol, f"{what}: roped queries")
+    check_close(attn_gpu, rec["attn"].reshape(B, -1), atol, rtol, f"{what}: attention output")
+    check_close(out_gpu, y, atol, rtol, f"{what}: layer output")
+
+
+def check_injection(W, shape, hcat, fused_gpu, positions, k_gpu, v_gpu, what, atol=2e-2,
+                    rtol=1e-2):
+    """KV injection of rows hcat [n, n_inject, d] at ``positions``, in two
+    stages: F = bf16(W_fuse h_cat) against the GPU's F (fused_gpu [n, d]), then
+    every draft layer's K = RoPE(W_k F) and V = W_v F from the GPU's F against
+    the GPU's cache rows k_gpu[l] / v_gpu[l] [n, H_kv, hd].  (F of a deep
+    random target is large, so one bf16 rounding of F that differs between
+    the two sides would show up in K beyond the element-wise tolerance of
+    near-zero elements; each stage on its own is well conditioned.)"""
+    n = hcat.shape[0]
+    prec = nm.Precision("bf16emu")
+    f = prec.store(nm.linear(np.asarray(hcat, dtype=np.float64).reshape(n, -1), W["draft.fuse"]))
+    check_close(fused_gpu, f, atol, rtol, f"{what}: fused feature F")
+    fg = np.asarray(fused_gpu, dtype=np.float64)
+    pos = np.asarray(positions)
+    for l in range(shape.n_draft_layers):
+        k = nm.linear(fg, W[f"draft.layers.{l}.wk"]).reshape(n, shape.n_kv_heads, shape.head_dim)
+        k = prec.store(nm.apply_rope(k, pos, shape.rope_theta))
+        v = prec.store(nm.linear(fg, W[f"draft.layers.{l}.wv"]).reshape(n, shape.n_kv_heads,
+                                                                         shape.head_dim))
+        check_close(k_gpu[l], k, atol, rtol, f"{what}: draft layer {l} K")
+        check_close(v_gpu[l], v, atol, rtol, f"{what}: draft layer {l} V")

@@ -32,8 +32,7 @@ from oracle import numerics as nm
 from oracle.decode import accept_longest_prefix
 from oracle.models import Weights, _layer
 
-from gpu_replay import (check_argmax, check_close, draft_inputs, draft_layer_forced,
-                        lm_logits)
+from gpu_replay import check_argmax, check_close, check_draft_layer, draft_inputs, lm_logits
 
 pytestmark = pytest.mark.gpu
 ATOL, RTOL = 2e-2, 1e-2
@@ -58,13 +57,17 @@ def run():
     trace = torch.zeros(w.shape.n_layers, P, w.shape.d_model, dtype=torch.float32, device="cuda")
     dtrace = torch.zeros(w.shape.n_draft_layers, P, w.shape.d_model, dtype=torch.float32,
                          device="cuda")
+    qa = [torch.zeros(w.shape.n_draft_layers, P, w.shape.q_dim, dtype=torch.bfloat16,
+                      device="cuda") for _ in range(2)]
     capi.dflash_debug_trace(eng.ctx, trace)
     capi.dflash_debug_trace_draft(eng.ctx, dtrace)
+    capi.dflash_debug_trace_draft_attn(eng.ctx, *qa)
     anchor = int(anchors[0].item())
     out, dlog, vlog, margin = eng.step(sid, anchors, want_logits=True)
     torch.cuda.synchronize()
     capi.dflash_debug_trace(eng.ctx, None)
     capi.dflash_debug_trace_draft(eng.ctx, None)
+    capi.dflash_debug_trace_draft_attn(eng.ctx, None, None)
     r = dict(
         w=w, prompt=prompt, P=P,
         block=out.block[0].cpu().numpy(), argmax=out.argmax[0].cpu().numpy(),
@@ -78,6 +81,7 @@ def run():
                  for l in LAYERS},
         trace=trace[:, :16].cpu().numpy(),
         anchor=anchor, dtrace=dtrace[:, :16].cpu().numpy(),
+        dq=qa[0][:, :16].float().cpu().numpy(), dao=qa[1][:, :16].float().cpu().numpy(),
         dctx={l: (eng.debug_view("dk_cache", l)[0, :, :P].float().cpu().numpy().transpose(1, 0, 2),
                   eng.debug_view("dv_cache", l)[0, :, :P].float().cpu().numpy().transpose(1, 0, 2))
               for l in range(w.shape.n_draft_layers)},
@@ -196,18 +200,19 @@ def test_draft_injection_cache_rows(run):
 @pytest.mark.parametrize("l", [0, 1, 2, 3, 4])
 def test_draft_layer_teacher_forced(run, l):
     """Draft layer l over the 16 block rows [anchor, mask x 15] at positions
-    P..P+15: input = the GPU's fp32 residual after draft layer l-1 (the
-    embeddings for layer 0), keys = the GPU's draft cache rows 0..P-1 (the
-    injected context) plus the block's own K/V, no mask; output against the
-    GPU's residual after layer l."""
+    P..P+15, input = the GPU's fp32 residual after draft layer l-1 (the
+    embeddings for layer 0), context = the GPU's draft cache rows 0..P-1 (the
+    injected context), no mask; checked in three stages (queries, attention
+    on the GPU's queries, the rest of the layer on the GPU's attention
+    output) against the GPU's traces."""
     s = run["w"].shape
     P = run["P"]
     x = (draft_inputs(s, run["w"].seed, run["anchor"], 16) if l == 0
          else run["dtrace"][l - 1].astype(np.float64))
     kc, vc = run["dctx"][l]
-    y = draft_layer_forced(run["W"], s, l, x, P, kc, vc)
+    check_draft_layer(run["W"], s, l, x, P, kc, vc, run["dq"][l], run["dao"][l], run["dtrace"][l],
+                      f"draft layer {l}")
     run["W"]._cache.clear()
-    check_close(run["dtrace"][l], y, ATOL, RTOL, f"draft layer {l}")
 
 
 def test_draft_logits_and_argmax(run):

@@ -23,10 +23,10 @@ import workloads as wl
 from oracle import numerics as nm
 from oracle.ddtree import DraftTree, build_tree, tree_accept
 from oracle.decode import accept_longest_prefix
-from oracle.models import KVCache, Weights, _layer, inject_kv
+from oracle.models import Weights, _layer
 
-from gpu_replay import (cache_band, check_argmax, check_close, draft_inputs, draft_layer_forced,
-                        forced_tree, lm_logits, tree_arrays)
+from gpu_replay import (cache_band, check_argmax, check_close, check_draft_layer, check_injection,
+                        draft_inputs, forced_tree, lm_logits, tree_arrays)
 
 pytestmark = pytest.mark.gpu
 ATOL, RTOL = 2e-2, 1e-2
@@ -74,12 +74,16 @@ def b32():
                         device="cuda")
     dtrace = torch.zeros(w.shape.n_draft_layers, eng.max_rows, w.shape.d_model,
                          dtype=torch.float32, device="cuda")
+    qa = [torch.zeros(w.shape.n_draft_layers, eng.max_rows, w.shape.q_dim, dtype=torch.bfloat16,
+                      device="cuda") for _ in range(2)]
     capi.dflash_debug_trace(eng.ctx, trace)
     capi.dflash_debug_trace_draft(eng.ctx, dtrace)
+    capi.dflash_debug_trace_draft_attn(eng.ctx, *qa)
     out, dlog, vlog, _ = eng.step(sid, anchors, want_logits=True)
     torch.cuda.synchronize()
     capi.dflash_debug_trace(eng.ctx, None)
     capi.dflash_debug_trace_draft(eng.ctx, None)
+    capi.dflash_debug_trace_draft_attn(eng.ctx, None, None)
     picks = [(3, 0), (17, 9)]  # (sequence, block row)
     r = dict(w=w, prompts=prompts, lens=lens, picks=picks,
              block=out.block.cpu().numpy(), argmax=out.argmax.cpu().numpy(),
@@ -89,6 +93,8 @@ def b32():
              trace={(s, j): trace[:, s * 16 + j].cpu().numpy() for s, j in picks},
              cache={},
              dtrace={s: dtrace[:, s * 16:(s + 1) * 16].cpu().numpy() for s, _ in picks},
+             dq={s: qa[0][:, s * 16:(s + 1) * 16].float().cpu().numpy() for s, _ in picks},
+             dao={s: qa[1][:, s * 16:(s + 1) * 16].float().cpu().numpy() for s, _ in picks},
              dlog={s: dlog[s].cpu().numpy() for s, _ in picks},
              dctx={(s, l): (eng.debug_view("dk_cache", l)[s, :, :lens[s]].float().cpu().numpy()
                             .transpose(1, 0, 2),
@@ -101,7 +107,7 @@ def b32():
             r["cache"][(s, l)] = (eng.debug_view("k_cache", l)[s, :, :n].float().cpu().numpy().transpose(1, 0, 2),
                                   eng.debug_view("v_cache", l)[s, :, :n].float().cpu().numpy().transpose(1, 0, 2))
     eng.close()
-    del eng, trace, dtrace, vlog, dlog
+    del eng, trace, dtrace, qa, vlog, dlog
     torch.cuda.empty_cache()
     r["W"] = Weights(wl.SyntheticWeights(w.shape, w.seed))
     return r
@@ -153,15 +159,16 @@ def test_b32_final_logits(b32):
 @pytest.mark.parametrize("l", B32_DRAFT_LAYERS)
 def test_b32_draft_layers_teacher_forced(b32, l):
     """Draft layer l of two sequences' blocks (16 rows each, ragged contexts),
-    teacher-forced on the GPU's draft residual trace and draft cache."""
+    teacher-forced on the GPU's draft traces and draft cache (three stages:
+    queries, attention on the GPU's queries, the rest of the layer)."""
     w = b32["w"]
     for s, _ in b32["picks"]:
         P = b32["lens"][s]
         x = (draft_inputs(w.shape, w.seed, b32["block"][s, 0], 16) if l == 0
              else b32["dtrace"][s][l - 1].astype(np.float64))
-        y = draft_layer_forced(b32["W"], w.shape, l, x, P, *b32["dctx"][(s, l)])
+        check_draft_layer(b32["W"], w.shape, l, x, P, *b32["dctx"][(s, l)], b32["dq"][s][l],
+                          b32["dao"][s][l], b32["dtrace"][s][l], f"seq {s} draft layer {l}")
         b32["W"]._cache.clear()
-        check_close(b32["dtrace"][s][l], y, ATOL, RTOL, f"seq {s} draft layer {l}")
 
 
 def test_b32_draft_logits_and_argmax(b32):
@@ -343,20 +350,27 @@ def forced():
     dl = [(n, l) for l in range(s.n_draft_layers) for n in ("dk_cache", "dv_cache")]
     dpost = cache_band(eng, dl, b, P, P + FORCED_PATH + 1)
     capture = eng.debug_view("capture")[: b * nmax].float().cpu().numpy()
+    fused = eng.debug_view("fused")[: b * nmax].float().cpu().numpy()
     lengths = eng.lengths(b)
     # the next draft pass, over the committed and injected path
     dtrace = torch.zeros(s.n_draft_layers, eng.max_rows, s.d_model, dtype=torch.float32,
                          device="cuda")
+    qa = [torch.zeros(s.n_draft_layers, eng.max_rows, s.q_dim, dtype=torch.bfloat16,
+                      device="cuda") for _ in range(2)]
     capi.dflash_debug_trace_draft(eng.ctx, dtrace)
+    capi.dflash_debug_trace_draft_attn(eng.ctx, *qa)
     anchors2 = r["next_anchor"][:b].clone()
     dlog = torch.empty(b * 15 * s.vocab, dtype=torch.float32, device="cuda")
     capi.dflash_draft_block(eng.ctx, b, sid, anchors2, eng.block[: b * 16], 0, None, None, dlog)
     torch.cuda.synchronize()
     capi.dflash_debug_trace_draft(eng.ctx, None)
+    capi.dflash_debug_trace_draft_attn(eng.ctx, None, None)
     q0 = int(np.argmax(out["accept_len"][:b]))  # the longest accepted path
     P2 = lengths[q0]
     res = dict(w=w, P=P, lo=lo, nmax=nmax, trees=trees, out=out, snap=snap, post=post,
-               dpost=dpost, capture=capture, lengths=lengths, q0=q0, P2=P2,
+               dpost=dpost, capture=capture, fused=fused, lengths=lengths, q0=q0, P2=P2,
+               dq=qa[0][:, q0 * 16:(q0 + 1) * 16].float().cpu().numpy(),
+               dao=qa[1][:, q0 * 16:(q0 + 1) * 16].float().cpu().numpy(),
                anchor2=int(anchors2[q0].item()),
                dtrace=dtrace[:, q0 * 16:(q0 + 1) * 16].cpu().numpy(),
                dlog=dlog.view(b, 15, -1)[q0].cpu().numpy(),
@@ -366,7 +380,7 @@ def forced():
                          eng.debug_view("dv_cache", l)[q0, :, :P2].float().cpu().numpy()
                          .transpose(1, 0, 2)) for l in FORCED_DRAFT_LAYERS})
     eng.close()
-    del eng, dtrace, dlog
+    del eng, dtrace, qa, dlog
     torch.cuda.empty_cache()
     res["W"] = Weights(wl.SyntheticWeights(s, w.seed))
     return res
@@ -410,21 +424,19 @@ def test_forced_tree_compaction_full_size(forced):
 
 def test_forced_tree_injection_full_size(forced):
     """Draft cache rows P .. P + a of every draft layer hold the injection of
-    the captured rows of the accepted nodes s_j at positions P + j."""
+    the captured rows of the accepted nodes s_j at positions P + j (checked
+    as F, then K / V from the GPU's F)."""
     w, P = forced["w"], forced["P"]
     s = w.shape
-    prec = nm.Precision("bf16emu")
     for q in range(w.batch):
         a, path, _ = _forced_path(forced, q)
-        rows = forced["capture"][q * forced["nmax"] + np.array(path)].astype(np.float64)
-        pos = P + np.arange(a + 1)
-        dc = KVCache(s.n_draft_layers, P + a + 1, s.n_kv_heads, s.head_dim)
-        inject_kv(forced["W"], s, prec, dc, rows, pos)
-        for l in range(s.n_draft_layers):
-            gk = forced["dpost"][("dk_cache", l)][q][:, : a + 1].transpose(1, 0, 2)
-            gv = forced["dpost"][("dv_cache", l)][q][:, : a + 1].transpose(1, 0, 2)
-            check_close(gk, dc.k[l, pos], ATOL, RTOL, f"seq {q} draft layer {l} K")
-            check_close(gv, dc.v[l, pos], ATOL, RTOL, f"seq {q} draft layer {l} V")
+        rows = q * forced["nmax"] + np.array(path)
+        kg = [forced["dpost"][("dk_cache", l)][q][:, : a + 1].transpose(1, 0, 2)
+              for l in range(s.n_draft_layers)]
+        vg = [forced["dpost"][("dv_cache", l)][q][:, : a + 1].transpose(1, 0, 2)
+              for l in range(s.n_draft_layers)]
+        check_injection(forced["W"], s, forced["capture"][rows], forced["fused"][rows],
+                        P + np.arange(a + 1), kg, vg, f"seq {q}")
     forced["W"]._cache.clear()
 
 
@@ -433,9 +445,9 @@ def test_next_draft_layers_after_tree_commit(forced, l):
     w = forced["w"]
     x = (draft_inputs(w.shape, w.seed, forced["anchor2"], 16) if l == 0
          else forced["dtrace"][l - 1].astype(np.float64))
-    y = draft_layer_forced(forced["W"], w.shape, l, x, forced["P2"], *forced["dctx"][l])
+    check_draft_layer(forced["W"], w.shape, l, x, forced["P2"], *forced["dctx"][l],
+                      forced["dq"][l], forced["dao"][l], forced["dtrace"][l], f"next draft layer {l}")
     forced["W"]._cache.clear()
-    check_close(forced["dtrace"][l], y, ATOL, RTOL, f"next draft layer {l}")
 
 
 def test_next_draft_logits_after_tree_commit(forced):
