@@ -21,7 +21,7 @@ import torch
 
 import workloads as wl
 from oracle import numerics as nm
-from oracle.ddtree import DraftTree, build_tree, tree_accept
+from oracle.ddtree import build_tree, tree_accept
 from oracle.decode import accept_longest_prefix
 from oracle.models import Weights, _layer
 
