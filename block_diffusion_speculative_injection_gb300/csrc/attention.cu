@@ -10,11 +10,11 @@
 //
 // bf16, head_dim 128: one CTA takes 64 query rows = (64/G) block positions x
 // the G query heads that share one KV head, so each K/V tile streamed from
-// HBM feeds G heads at once.  K/V tiles of 64 slots are staged in shared
-// memory with cp.async (16-byte chunks, XOR-swizzled rows) in a two-deep
-// ring; QK^T and PV run on mma.sync m16n8k16 with an online softmax in
-// registers (exp2 domain).  Long contexts are split across CTAs; a combine
-// kernel merges the partial (m, l, O).
+// HBM feeds G heads at once.  Q and the K/V tiles (128 keys) arrive by TMA;
+// S = Q K^T and O += P V run on tcgen05 with the accumulators in tensor
+// memory; the online softmax (exp2 domain) runs in one warp group that owns
+// one query row per thread (attn_tc_kernel).  Long contexts are split across
+// CTAs; a combine kernel merges the partial (m, l, O).
 #include <cfloat>
 #include <cmath>
 #include <cstring>
@@ -41,6 +41,7 @@ struct AttnK {
   int rows_total;
   float scale_log2;
   int uni_ctx, uni_blk;  // used when pass_seq == nullptr: seq = b, same lengths
+  int32_t* status;       // sticky device status (bounded waits that gave up)
 };
 
 __device__ __forceinline__ void seq_meta(const AttnK& p, int b, int& seq, int& ctx, int& blk) {
@@ -55,28 +56,6 @@ __device__ __forceinline__ void seq_meta(const AttnK& p, int b, int& seq, int& c
   }
 }
 
-// ---------------------------------------------------------------------------
-// small PTX wrappers (legacy warp-level MMA path)
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1,
-                                          uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void mma_bf16(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
 // (x0, x1) -> packed bf16 high parts and packed bf16 residuals x - hi
 __device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t& hi, uint32_t& lo) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
@@ -84,11 +63,6 @@ __device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t& hi, uin
       __floats2bfloat162_rn(x0 - __low2float(h), x1 - __high2float(h));
   hi = *reinterpret_cast<const uint32_t*>(&h);
   lo = *reinterpret_cast<const uint32_t*>(&l);
-}
-
-// byte offset of 16-byte chunk c (0..15) of row r in a [rows][256 B] tile
-__device__ __forceinline__ uint32_t swz(int r, int c) {
-  return (uint32_t)(r * 256 + ((c ^ (r & 7)) << 4));
 }
 
 __device__ __forceinline__ bool key_visible(int mask, int kidx, int ctx_len, int blk, int j,
@@ -101,16 +75,68 @@ __device__ __forceinline__ bool key_visible(int mask, int kidx, int ctx_len, int
   return (anc_row[i >> 6] >> (i & 63)) & 1ull;
 }
 
-constexpr int kTileKeys = 64;
 constexpr int kHd = 128;
-constexpr int kAttnSmem = 3 * 64 * 256 * 2 - 64 * 256;  // Q + 2 x (K, V) = 80 KB
+constexpr int kTK = 128;  // keys per tile
 
-__global__ void __launch_bounds__(128) attn_mma_kernel(const AttnK p) {
+// 2^x on the special-function unit (approximate, flushing results below the
+// normal range to zero); P never needs more than fp32's normal range
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ---------------------------------------------------------------------------
+// bf16 attention on the 5th-generation tensor cores.
+//
+// One CTA: 64 query rows (64 / G block positions x the G query heads of one
+// KV head) against one split of the sequence's keys, in tiles of 128 keys.
+// Shared memory (1024-aligned), 128-byte-swizzled K-major boxes of 64 columns:
+//   Q     [64 rows][128 hd]             2 boxes of 8 KB       (TMA, 3-D box)
+//   stage s = 0, 1: K [128 keys][128 hd] 2 boxes of 16 KB; V the same
+//   P buffer u = 0, 1: P_hi [64 rows][128 keys] 2 boxes of 8 KB; P_lo the same
+// Tensor memory (512 columns): S buffers at columns 0 and 128 (fp32 scores of
+// a tile), O at column 256 (fp32 [64 rows][128 hd]).  An M = 64 accumulator
+// keeps row m in lane (m / 16) * 32 + m % 16, so warp w of the softmax group
+// owns rows 16w .. 16w + 15 in its lanes 0 .. 15.
+//
+// Warps 0-3 (softmax): per tile, read S, mask, running max, P = exp2(S - m)
+// split into a bf16 high part and a bf16 residual (P keeps ~16 bits), write
+// P to shared memory in the MMA's K-major layout.  The running max used for
+// the exponentials is raised only when a tile's max exceeds it by more than
+// 8 (a factor 256): then O is rescaled in tensor memory (after the previous
+// P.V has completed) and the sum l with it.  Any consistent max gives the
+// same O / l; the threshold keeps the rescales rare.
+// Warp 4 (producer): TMA of Q, then K and V tiles into a two-stage ring.
+// Warp 5 (MMA): S(t) = Q K(t)^T, then O += P_hi(t-1) V(t-1) + P_lo(t-1) V(t-1)
+// with V as an MN-major operand, so S of the next tile forms while the
+// softmax works on the current one.
+// Only one CTA fits an SM (shared memory), so the 512-column allocation never
+// waits on another CTA of this kernel, and no other kernel of the library
+// that holds tensor memory fits beside it.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kQBox = 64 * 128, kQBytes = 2 * kQBox;
+constexpr uint32_t kKBox = kTK * 128, kKBytes = 2 * kKBox;
+constexpr uint32_t kPBox = 64 * 128, kPBytes = 4 * kPBox;
+constexpr uint32_t kOffKV = kQBytes;
+constexpr uint32_t kOffP = kOffKV + 2 * 2 * kKBytes;
+constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;
+constexpr int kAttnSmem = (int)kOffBar + 256 + 1024;  // barriers + alignment slack
+constexpr int kAttnThreads = 192;
+constexpr uint32_t kTmemCols = 512, kTmemO = 256;
+constexpr float kRescaleLog2 = 8.f;
+
+struct AttnMaps {
+  CUtensorMap q, k, v;
+};
+
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attn_tc_kernel(const __grid_constant__ AttnMaps maps, const AttnK p) {
   pdl_trigger();
   pdl_wait();
-  extern __shared__ __align__(128) uint8_t sm[];
-  uint8_t* qs = sm;                   // 64 x 256 B
-  uint8_t* ks0 = sm + 64 * 256;       // 2 stages x (K 16 KB, V 16 KB)
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.G, POS = 64 / G;
   const int b = blockIdx.z / p.n_splits, split = blockIdx.z % p.n_splits;
@@ -120,266 +146,360 @@ __global__ void __launch_bounds__(128) attn_mma_kernel(const AttnK p) {
   const int j0 = blockIdx.x * POS;
   if (j0 >= blk) return;
   const int jmax = min(j0 + POS, blk);  // exclusive
-  int key_end = (p.mask == kMaskCausal) ? ctx_len + jmax : ctx_len + blk;
-  // causal and draft passes: this sequence's keys in equal whole-tile
-  // shares over the splits (the launch is sized for the longest context;
-  // shorter ones must not leave the later splits idle).  Tree verify keeps
-  // the plan's fixed share, which measured faster there.
+  const int key_end = (p.mask == kMaskCausal) ? ctx_len + jmax : ctx_len + blk;
+  // causal and draft passes: this sequence's keys in equal whole-tile shares
+  // over the splits (the launch is sized for the longest context); tree
+  // verify keeps the plan's fixed share
   const int kps =
       p.mask == kMaskTree
           ? p.keys_per_split
           : min(p.keys_per_split,
-                max(kTileKeys, (key_end + p.n_splits * kTileKeys - 1) / (p.n_splits * kTileKeys) *
-                                   kTileKeys));
+                max(kTK, (key_end + p.n_splits * kTK - 1) / (p.n_splits * kTK) * kTK));
   const int k_begin = split * kps;
   const int k_stop = min(key_end, k_begin + kps);
 
-  // this thread's two query rows (within the CTA tile) and their block index
-  const int r0 = warp * 16 + (lane >> 2), r1 = r0 + 8;
-  const int jr0 = j0 + r0 / G, jr1 = j0 + r1 / G;
-  const int hr0 = kvh * G + r0 % G, hr1 = kvh * G + r1 % G;
-  const bool live0 = jr0 < blk, live1 = jr1 < blk;
-  const size_t grow0 = (size_t)b * p.q_stride + jr0, grow1 = (size_t)b * p.q_stride + jr1;
+  // the row this thread works on (softmax warps; lanes t and t + 16 share
+  // row 16 w + t)
+  const bool row_thr = warp < 4;
+  const int r = warp * 16 + (lane & 15);
+  const int jr = j0 + r / G, hr = kvh * G + r % G;
+  const bool live = row_thr && jr < blk;
+  const size_t grow = (size_t)b * p.q_stride + jr;
 
   if (k_begin >= k_stop) {  // empty split: neutral partial
-    if (p.n_splits > 1 && (lane & 3) == 0) {
-      if (live0) {
-        float* ml = p.part_ml + (((size_t)split * p.rows_total + grow0) * p.H + hr0) * 2;
-        ml[0] = -INFINITY;
-        ml[1] = 0.f;
-      }
-      if (live1) {
-        float* ml = p.part_ml + (((size_t)split * p.rows_total + grow1) * p.H + hr1) * 2;
-        ml[0] = -INFINITY;
-        ml[1] = 0.f;
-      }
-    }
-    if (p.n_splits > 1) {
-      // zero the partial outputs of this thread's columns
-      for (int nt = 0; nt < 16; ++nt) {
-        const int d = nt * 8 + (lane & 3) * 2;
-        if (live0) {
-          float* o = p.part_o + (((size_t)split * p.rows_total + grow0) * p.H + hr0) * kHd + d;
-          o[0] = 0.f;
-          o[1] = 0.f;
-        }
-        if (live1) {
-          float* o = p.part_o + (((size_t)split * p.rows_total + grow1) * p.H + hr1) * kHd + d;
-          o[0] = 0.f;
-          o[1] = 0.f;
-        }
-      }
+    if (p.n_splits > 1 && live) {
+      const size_t base = ((size_t)split * p.rows_total + grow) * p.H + hr;
+      if (lane < 16) *reinterpret_cast<float2*>(p.part_ml + base * 2) = make_float2(-INFINITY, 0.f);
+      float4* o = reinterpret_cast<float4*>(p.part_o + base * kHd) + (lane >> 4) * (kHd / 8);
+      for (int i = 0; i < kHd / 8; ++i) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     return;
   }
+  const int n_tiles = (k_stop - k_begin + kTK - 1) / kTK;
 
-  const bf16* qg = static_cast<const bf16*>(p.q);
-  const size_t head_base = ((size_t)seq * p.Hkv + kvh) * (size_t)p.max_ctx;
-  const bf16* kg = static_cast<const bf16*>(p.kc) + head_base * kHd;
-  const bf16* vg = static_cast<const bf16*>(p.vc) + head_base * kHd;
+  uint8_t* const qs = sm;
+  uint8_t* const kvs = sm + kOffKV;   // stage s: K at s * 2 * kKBytes, V after it
+  uint8_t* const ps = sm + kOffP;     // buffer u: hi boxes, then lo boxes
+  uint64_t* const bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
+  uint64_t* const q_full = bars;
+  uint64_t* const k_full = bars + 1;
+  uint64_t* const v_full = bars + 3;
+  uint64_t* const k_empty = bars + 5;
+  uint64_t* const v_empty = bars + 7;
+  uint64_t* const s_full = bars + 9;
+  uint64_t* const s_free = bars + 11;
+  uint64_t* const p_full = bars + 13;
+  uint64_t* const pv_done = bars + 15;
+  uint32_t* const tslot = reinterpret_cast<uint32_t*>(bars + 17);
 
-  // ---- Q tile -> shared (rows past blk are zero)
-  for (int i = threadIdx.x; i < 64 * 16; i += 128) {
-    const int r = i >> 4, c = i & 15;
-    const int j = j0 + r / G, h = kvh * G + r % G;
-    const bf16* src = qg + (((size_t)b * p.q_stride + (j < blk ? j : 0)) * p.H + h) * kHd + c * 8;
-    cp_async16(smem_u32(qs + swz(r, c)), src, j < blk ? 16u : 0u);
-  }
-  cp_async_commit();
-
-  auto load_kv = [&](int tile_start, int stage) {
-    uint8_t* ks = ks0 + stage * (2 * 64 * 256);
-    uint8_t* vs = ks + 64 * 256;
-    for (int i = threadIdx.x; i < 64 * 16; i += 128) {
-      const int r = i >> 4, c = i & 15;
-      const int slot = tile_start + r;
-      const bool in = slot < k_stop;
-      const size_t off = (size_t)(in ? slot : 0) * kHd + c * 8;
-      cp_async16(smem_u32(ks + swz(r, c)), kg + off, in ? 16u : 0u);
-      cp_async16(smem_u32(vs + swz(r, c)), vg + off, in ? 16u : 0u);
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 4);
+      mbar_init(&p_full[i], 4);
+      mbar_init(&pv_done[i], 1);
     }
-    cp_async_commit();
-  };
-
-  const int n_tiles = (k_stop - k_begin + kTileKeys - 1) / kTileKeys;
-  load_kv(k_begin, 0);
-
-  // anc words of this thread's rows (tree mask)
-  const uint64_t* anc0 = nullptr;
-  const uint64_t* anc1 = nullptr;
-  if (p.mask == kMaskTree) {
-    anc0 = p.anc + ((size_t)b * p.q_stride + (live0 ? jr0 : 0)) * p.anc_words;
-    anc1 = p.anc + ((size_t)b * p.q_stride + (live1 ? jr1 : 0)) * p.anc_words;
+    mbar_fence_init();
   }
-  const int mask_from = (p.mask == kMaskNone) ? ctx_len + blk
-                        : (p.mask == kMaskCausal) ? ctx_len + j0 + 1
-                                                  : ctx_len;
-
-  cp_async_wait<1>();
+  if (warp == 0) {
+    tmem_alloc(tslot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
   __syncthreads();
-  uint32_t qf[8][4];
-#pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    const int mi = lane >> 3;
-    const int r = warp * 16 + (mi & 1) * 8 + (lane & 7);
-    const int c = 2 * kk + (mi >> 1);
-    ldsm_x4(smem_u32(qs + swz(r, c)), qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
-  }
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  int32_t* const status = p.status;
 
-  float o[16][4];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-
-  for (int t = 0; t < n_tiles; ++t) {
-    const int tile_start = k_begin + t * kTileKeys;
-    if (t + 1 < n_tiles) {
-      load_kv(tile_start + kTileKeys, (t + 1) & 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-    const uint8_t* ks = ks0 + (t & 1) * (2 * 64 * 256);
-    const uint8_t* vs = ks + 64 * 256;
-
-    float s[8][4];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        const int mi = lane >> 3;
-        const int r = np * 16 + (mi >> 1) * 8 + (lane & 7);
-        const int c = 2 * kk + (mi & 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(smem_u32(ks + swz(r, c)), b0, b1, b2, b3);
-        mma_bf16(s[2 * np], qf[kk], b0, b1);
-        mma_bf16(s[2 * np + 1], qf[kk], b2, b3);
-      }
-    }
-    // scale, mask, row max
-    const bool need_mask = tile_start + kTileKeys > mask_from || tile_start + kTileKeys > k_stop;
-    float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float v = s[nt][e] * p.scale_log2;
-        if (need_mask) {
-          const int kidx = tile_start + nt * 8 + (lane & 3) * 2 + (e & 1);
-          const bool row1 = e >= 2;
-          const bool vis = kidx < k_stop &&
-                           key_visible(p.mask, kidx, ctx_len, blk, row1 ? jr1 : jr0,
-                                       row1 ? anc1 : anc0);
-          if (!vis) v = -INFINITY;
+  if (warp == 4) {
+    if (lane == 0) {
+      // ---- producer: K(t) once S(t-2) has read its stage, V(t) once
+      // P.V(t-2) has; K runs one tile ahead of V in issue order
+      tma_prefetch_desc(&maps.q);
+      tma_prefetch_desc(&maps.k);
+      tma_prefetch_desc(&maps.v);
+      mbar_arrive_expect_tx(q_full, kQBytes);
+      const int qz = b * p.q_stride + j0;
+      tma_load_3d(qs, &maps.q, 0, kvh * G, qz, q_full);
+      tma_load_3d(qs + kQBox, &maps.q, 64, kvh * G, qz, q_full);
+      const int row0 = (seq * p.Hkv + kvh) * p.max_ctx + k_begin;
+      int k_issued = 0, v_issued = 0;
+      auto load = [&](int t, bool is_v) -> bool {
+        const int st = t & 1;
+        uint64_t* empty = is_v ? &v_empty[st] : &k_empty[st];
+        uint64_t* full = is_v ? &v_full[st] : &k_full[st];
+        if (t >= 2 && !mbar_wait(empty, ((t >> 1) - 1) & 1, status)) return false;
+        uint8_t* dst = kvs + st * 2 * kKBytes + (is_v ? kKBytes : 0);
+        const CUtensorMap* map = is_v ? &maps.v : &maps.k;
+        const int y = row0 + t * kTK;
+        mbar_arrive_expect_tx(full, kKBytes);
+        tma_load_2d(dst, map, 0, y, full);
+        tma_load_2d(dst + kKBox, map, 64, y, full);
+        return true;
+      };
+      for (int t = 0; t <= n_tiles; ++t) {
+        if (t < n_tiles) {
+          if (!load(t, false)) break;
+          k_issued = t + 1;
         }
-        s[nt][e] = v;
-      }
-      mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
-      mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
-    }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float base0 = (mn0 == -INFINITY) ? 0.f : mn0;
-    const float base1 = (mn1 == -INFINITY) ? 0.f : mn1;
-    const float al0 = exp2f(m0 - base0), al1 = exp2f(m1 - base1);
-    m0 = mn0;
-    m1 = mn1;
-    float rs0 = 0.f, rs1 = 0.f;
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      s[nt][0] = exp2f(s[nt][0] - base0);
-      s[nt][1] = exp2f(s[nt][1] - base0);
-      s[nt][2] = exp2f(s[nt][2] - base1);
-      s[nt][3] = exp2f(s[nt][3] - base1);
-      rs0 += s[nt][0] + s[nt][1];
-      rs1 += s[nt][2] + s[nt][3];
-    }
-    l0 = l0 * al0 + rs0;
-    l1 = l1 * al1 + rs1;
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      o[nt][0] *= al0;
-      o[nt][1] *= al0;
-      o[nt][2] *= al1;
-      o[nt][3] *= al1;
-    }
-    // O += P V.  P is split into a bf16 high part and a bf16 residual
-    // (P = P_hi + P_lo, ~16 significant bits) and both halves go through the
-    // tensor cores, so the probabilities keep fp32-like precision; the extra
-    // MMAs are free in this HBM-bound loop.
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint32_t a[4], alo[4];
-      split_bf16(s[2 * c][0], s[2 * c][1], a[0], alo[0]);
-      split_bf16(s[2 * c][2], s[2 * c][3], a[1], alo[1]);
-      split_bf16(s[2 * c + 1][0], s[2 * c + 1][1], a[2], alo[2]);
-      split_bf16(s[2 * c + 1][2], s[2 * c + 1][3], a[3], alo[3]);
-      // two column pairs at a time: the four high-part MMAs, then the four
-      // residual MMAs into the same accumulators, four MMAs apart
-#pragma unroll
-      for (int np = 0; np < 8; np += 2) {
-        const int mi = lane >> 3;
-        const int r = c * 16 + (mi & 1) * 8 + (lane & 7);
-        uint32_t b[2][4];
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-          ldsm_x4_t(smem_u32(vs + swz(r, 2 * (np + h) + (mi >> 1))), b[h][0], b[h][1], b[h][2],
-                    b[h][3]);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          mma_bf16(o[2 * (np + h)], a, b[h][0], b[h][1]);
-          mma_bf16(o[2 * (np + h) + 1], a, b[h][2], b[h][3]);
+        if (t >= 1) {
+          if (!load(t - 1, true)) break;
+          v_issued = t;
         }
+      }
+      // every issued copy has landed before this thread leaves
+      mbar_wait(q_full, 0, status);
+      for (int t = max(0, k_issued - 2); t < k_issued; ++t)
+        mbar_wait(&k_full[t & 1], (t >> 1) & 1, status);
+      for (int t = max(0, v_issued - 2); t < v_issued; ++t)
+        mbar_wait(&v_full[t & 1], (t >> 1) & 1, status);
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    if (lane == 0) {
+      // ---- MMA issuer: S(t), then P.V(t-1)
+      const uint32_t id_s = idesc_bf16_f32(64, kTK);
+      const uint32_t id_o = idesc_bf16_f32(64, kHd) | kIdescBMajorMN;
+      const uint32_t qa = smem_u32(qs);
+      bool ok = mbar_wait(q_full, 0, status);
+      for (int t = 0; ok && t <= n_tiles; ++t) {
+        if (t < n_tiles) {
+          const int st = t & 1;
+          if (!mbar_wait(&k_full[st], (t >> 1) & 1, status)) break;
+          if (t >= 2 && !mbar_wait(&s_free[st], ((t >> 1) - 1) & 1, status)) break;
+          tc_fence_after();
+          const uint32_t ka = smem_u32(kvs + st * 2 * kKBytes);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          mma_bf16(o[2 * (np + h)], alo, b[h][0], b[h][1]);
-          mma_bf16(o[2 * (np + h) + 1], alo, b[h][2], b[h][3]);
+          for (int kk = 0; kk < 8; ++kk)
+            tc_mma_bf16(tmem + st * kTK, sw128_desc(qa + (kk >> 2) * kQBox + (kk & 3) * 32),
+                        sw128_desc(ka + (kk >> 2) * kKBox + (kk & 3) * 32), id_s,
+                        kk > 0 ? 1u : 0u);
+          tc_commit(&s_full[st]);
+          tc_commit(&k_empty[st]);
+        }
+        if (t >= 1) {
+          const int u = t - 1, su = u & 1;
+          if (!mbar_wait(&p_full[su], (u >> 1) & 1, status)) break;
+          if (!mbar_wait(&v_full[su], (u >> 1) & 1, status)) break;
+          tc_fence_after();
+          const uint32_t va = smem_u32(kvs + su * 2 * kKBytes + kKBytes);
+          const uint32_t pa = smem_u32(ps + su * kPBytes);
+#pragma unroll
+          for (int half = 0; half < 2; ++half)
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              tc_mma_bf16(tmem + kTmemO,
+                          sw128_desc(pa + half * 2 * kPBox + (kk >> 2) * kPBox + (kk & 3) * 32),
+                          sw128_desc_mn(va + kk * 16 * 128, kKBox), id_o,
+                          (u > 0 || half > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(&pv_done[su]);
+          tc_commit(&v_empty[su]);
         }
       }
     }
-    __syncthreads();
-  }
-
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-
-  if (p.n_splits == 1) {
-    bf16* og = static_cast<bf16*>(p.out);
-    const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      const int d = nt * 8 + (lane & 3) * 2;
-      if (live0)
-        *reinterpret_cast<__nv_bfloat162*>(og + (grow0 * p.H + hr0) * kHd + d) =
-            __floats2bfloat162_rn(o[nt][0] * inv0, o[nt][1] * inv0);
-      if (live1)
-        *reinterpret_cast<__nv_bfloat162*>(og + (grow1 * p.H + hr1) * kHd + d) =
-            __floats2bfloat162_rn(o[nt][2] * inv1, o[nt][3] * inv1);
-    }
+    __syncwarp();
   } else {
-    const size_t base0 = ((size_t)split * p.rows_total + grow0) * p.H + hr0;
-    const size_t base1 = ((size_t)split * p.rows_total + grow1) * p.H + hr1;
+    // ---- softmax warps 0..3: lanes t and t + 16 share row 16 w + t; the
+    // half h = lane / 16 holds columns 64 h .. 64 h + 63 of every S tile
+    // (keys) and of O (head dims)
+    const int h = lane >> 4;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint64_t* anc = nullptr;
+    if (p.mask == kMaskTree)
+      anc = p.anc + ((size_t)b * p.q_stride + (live ? jr : 0)) * p.anc_words;
+    const int mask_from = (p.mask == kMaskNone)     ? ctx_len + blk
+                          : (p.mask == kMaskCausal) ? ctx_len + j0 + 1
+                                                    : ctx_len;
+    // bits below n set (n clamped to 0..32)
+    auto below = [](int n) -> uint32_t {
+      return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
+    };
+    // visibility of keys kb .. kb+31 for this thread's row
+    auto visible32 = [&](int kb) -> uint32_t {
+      uint32_t m = below(k_stop - kb);
+      if (p.mask == kMaskCausal) return m & below(ctx_len + jr + 1 - kb);
+      if (p.mask == kMaskNone) return m & below(ctx_len + blk - kb);
+      // tree: the context, then block key i where bit i of the ancestor set
+      const int i0 = kb - ctx_len;
+      uint32_t tb = 0;
+      if (i0 >= 0) {
+        const int w = i0 >> 6, sh = i0 & 63;
+        uint64_t x = w < p.anc_words ? anc[w] >> sh : 0ull;
+        if (sh > 32 && w + 1 < p.anc_words) x |= anc[w + 1] << (64 - sh);
+        tb = (uint32_t)x;
+      } else if (i0 > -32) {
+        tb = (uint32_t)(anc[0] << (-i0));
+      }
+      return m & (below(-i0) | (tb & below(blk - i0)));
+    };
+    const float scale = p.scale_log2;
+    float m_used = -INFINITY, l = 0.f;  // l: this thread's half of the row sum
+    bool ok = true;
+    for (int t = 0; t < n_tiles; ++t) {
+      const int st = t & 1;
+      const int tile_start = k_begin + t * kTK;
+      const int kb0 = tile_start + 64 * h;
+      if (lane == 0) ok = mbar_wait(&s_full[st], (t >> 1) & 1, status);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const bool need_mask = tile_start + kTK > mask_from || tile_start + kTK > k_stop;
+      // pass 1: tile max of the visible scores (scaled after the max: scale > 0)
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        uint32_t v[32];
+        tmem_ld_half32_nowait<64>(lane_base + st * kTK + c * 32, v);
+        tmem_wait_ld();
+        if (need_mask) {
+          const uint32_t vis = visible32(kb0 + 32 * c);
 #pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      const int d = nt * 8 + (lane & 3) * 2;
-      if (live0)
-        *reinterpret_cast<float2*>(p.part_o + base0 * kHd + d) = make_float2(o[nt][0], o[nt][1]);
-      if (live1)
-        *reinterpret_cast<float2*>(p.part_o + base1 * kHd + d) = make_float2(o[nt][2], o[nt][3]);
+          for (int i = 0; i < 32; ++i)
+            mx = fmaxf(mx, ((vis >> i) & 1u) ? __uint_as_float(v[i]) : -INFINITY);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(v[i]));
+        }
+      }
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16)) * scale;
+      // raise the running max only when it would otherwise grow by > 2^8
+      const bool resc = mx > m_used + kRescaleLog2;
+      const float alpha = resc ? ex2_approx(m_used - mx) : 1.f;
+      if (__any_sync(0xffffffffu, resc) && t > 0) {
+        // O holds tiles 0 .. t-1 once P.V(t-1) has completed
+        if (lane == 0) ok = mbar_wait(&pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, status);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+          uint32_t o[32];
+          tmem_ld_half32_nowait<64>(lane_base + kTmemO + c * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st_half32<64>(lane_base + kTmemO + c * 32, o);
+        }
+        tmem_wait_st();
+      }
+      if (resc) {
+        l *= alpha;
+        m_used = mx;
+      }
+      const float nbase = m_used == -INFINITY ? 0.f : -m_used;
+      // the P buffer of this tile was last read by P.V(t-2)
+      if (t >= 2) {
+        if (lane == 0) ok = mbar_wait(&pv_done[st], ((t >> 1) - 1) & 1, status);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+      }
+      // pass 2: P = 2^(s * scale - max), split into a bf16 high part and a
+      // bf16 residual, stored in the K-major layout of the P.V MMA's A
+      // operand (this half's 64 keys are box h)
+      uint8_t* const pb = ps + st * kPBytes + h * kPBox;
+      float rs = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        uint32_t v[32];
+        tmem_ld_half32_nowait<64>(lane_base + st * kTK + c * 32, v);
+        tmem_wait_ld();
+        const uint32_t vis = need_mask ? visible32(kb0 + 32 * c) : 0xffffffffu;
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8) {
+          float e[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int k = q8 * 8 + i;
+            e[i] = ex2_approx(fmaf(__uint_as_float(v[k]), scale, nbase));
+            if (need_mask && !((vis >> k) & 1u)) e[i] = 0.f;
+            rs += e[i];
+          }
+          uint4 hi, lo;
+          split_bf16(e[0], e[1], hi.x, lo.x);
+          split_bf16(e[2], e[3], hi.y, lo.y);
+          split_bf16(e[4], e[5], hi.z, lo.z);
+          split_bf16(e[6], e[7], hi.w, lo.w);
+          const int c8 = c * 4 + q8;
+          const uint32_t off = (uint32_t)r * 128 + ((uint32_t)(c8 ^ (r & 7)) << 4);
+          *reinterpret_cast<uint4*>(pb + off) = hi;
+          *reinterpret_cast<uint4*>(pb + 2 * kPBox + off) = lo;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[st]);
+      l += rs;
+      // a partial last tile: the V rows past the split's keys may hold any
+      // bits (another sequence's rows, or a caller's tensor); zero them so
+      // that P = 0 never meets a non-finite value
+      if (tile_start + kTK > k_stop) {
+        if (lane == 0) ok = mbar_wait(&v_full[st], (t >> 1) & 1, status);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        const int first = k_stop - tile_start;
+        uint8_t* vs = kvs + st * 2 * kKBytes + kKBytes;
+        for (int i = warp * 32 + lane; i < (kTK - first) * 16; i += 128) {
+          const int row = first + (i >> 4), ch = i & 15;
+          *reinterpret_cast<uint4*>(vs + (ch >> 3) * kKBox + row * 128 + (((ch & 7) ^ (row & 7)) << 4)) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[st]);
     }
-    if ((lane & 3) == 0) {
-      if (live0) *reinterpret_cast<float2*>(p.part_ml + base0 * 2) = make_float2(m0, l0);
-      if (live1) *reinterpret_cast<float2*>(p.part_ml + base1 * 2) = make_float2(m1, l1);
+    // ---- epilogue: this half of the row's O (unnormalised) once the last
+    // P.V is done
+    l += __shfl_xor_sync(0xffffffffu, l, 16);
+    if (ok) {
+      const int u = n_tiles - 1;
+      if (lane == 0) ok = mbar_wait(&pv_done[u & 1], (u >> 1) & 1, status);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+    }
+    if (ok) {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const size_t pbase = ((size_t)split * p.rows_total + grow) * p.H + hr;
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        uint32_t o[32];
+        tmem_ld_half32_nowait<64>(lane_base + kTmemO + c * 32, o);
+        tmem_wait_ld();
+        const int d0 = 64 * h + 32 * c;
+        if (live && p.n_splits == 1) {
+          uint4* og = reinterpret_cast<uint4*>(static_cast<bf16*>(p.out) + (grow * p.H + hr) * kHd + d0);
+#pragma unroll
+          for (int q8 = 0; q8 < 4; ++q8) {
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              __nv_bfloat162 hv = __floats2bfloat162_rn(__uint_as_float(o[q8 * 8 + 2 * i]) * inv,
+                                                        __uint_as_float(o[q8 * 8 + 2 * i + 1]) * inv);
+              w[i] = *reinterpret_cast<uint32_t*>(&hv);
+            }
+            og[q8] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        } else if (live) {
+          float4* po = reinterpret_cast<float4*>(p.part_o + pbase * kHd + d0);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            po[i] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
+                                __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
+        }
+      }
+      if (live && h == 0 && p.n_splits > 1)
+        *reinterpret_cast<float2*>(p.part_ml + pbase * 2) = make_float2(m_used, l);
     }
   }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
 constexpr int kMaxSplits = 256;
@@ -519,14 +639,14 @@ __global__ void attn_simt_f32_kernel(const AttnK p) {
 }
 
 // number of KV splits and keys per split for a launch of `ctas` CTAs.  The
-// split count minimises the estimated makespan: waves of resident CTAs (2 per
-// SM) x (key tiles per split + a fixed cost of about two tiles for the Q
+// split count minimises the estimated makespan: waves of resident CTAs (one
+// per SM) x (key tiles per split + a fixed cost of about two tiles for the Q
 // load, the partial write and the combine), so that a launch never ends with
 // a nearly empty extra wave of full-length splits.
 static void plan_splits(int sm_count, int ctas, int64_t max_keys, size_t part_cap, int rows_heads,
                         int* n_splits, int* keys_per_split, int min_splits = 1) {
-  const int64_t key_tiles = std::max<int64_t>(1, (max_keys + kTileKeys - 1) / kTileKeys);
-  const int64_t slots = 2 * (int64_t)sm_count;
+  const int64_t key_tiles = std::max<int64_t>(1, (max_keys + kTK - 1) / kTK);
+  const int64_t slots = (int64_t)sm_count;
   int best = 1;
   int64_t best_cost = INT64_MAX;
   const int64_t s_max = std::min<int64_t>(kMaxSplits, key_tiles);
@@ -544,7 +664,7 @@ static void plan_splits(int sm_count, int ctas, int64_t max_keys, size_t part_ca
   *keys_per_split = 1 << 30;
   if (best > 1) {
     const int64_t tiles_per = (key_tiles + best - 1) / best;
-    *keys_per_split = (int)(tiles_per * kTileKeys);
+    *keys_per_split = (int)(tiles_per * kTK);
     best = (int)((key_tiles + tiles_per - 1) / tiles_per);
   }
   *n_splits = best;
@@ -584,7 +704,23 @@ static int device_sms() {
 
 static cudaError_t ensure_attn_smem() {
   static std::atomic<bool> done[kMaxDevices];
-  return ensure_smem_attr(done, attn_mma_kernel, kAttnSmem);
+  return ensure_smem_attr(done, attn_tc_kernel, kAttnSmem);
+}
+
+// Q tensor map: [rows][H][128] bf16 read as a 3-D box of (64 of hd) x (the G
+// heads of one KV head) x (64/G block positions)
+static bool q_map(CUtensorMap* m, const void* q, int H, int64_t rows, int G) {
+  const uint64_t dims[3] = {(uint64_t)kHd, (uint64_t)H, (uint64_t)rows};
+  const uint64_t strides[2] = {(uint64_t)kHd * 2, (uint64_t)H * kHd * 2};
+  const uint32_t box[3] = {64u, (uint32_t)G, (uint32_t)(64 / G)};
+  return encode_tmap_bf16(m, q, 3, dims, strides, box);
+}
+// K or V rows [rows][128] bf16, box of 128 rows x 64
+static bool kv_map(CUtensorMap* m, const void* base, int64_t rows) {
+  const uint64_t dims[2] = {(uint64_t)kHd, (uint64_t)rows};
+  const uint64_t strides[1] = {(uint64_t)kHd * 2};
+  const uint32_t box[2] = {64u, (uint32_t)kTK};
+  return encode_tmap_bf16(m, base, 2, dims, strides, box);
 }
 
 dflash_status attention(dflash_ctx* ctx, const AttnArgs& a, cudaStream_t st) {
@@ -625,6 +761,33 @@ dflash_status attention(dflash_ctx* ctx, const AttnArgs& a, cudaStream_t st) {
     set_error(ctx, "bf16 attention needs head_dim 128 and a GQA group dividing 64");
     return DFLASH_E_UNSUPPORTED;
   }
+  p.status = ctx->dev_status;
+  AttnMaps maps;
+  const int64_t kv_rows = (int64_t)c.max_batch * c.n_kv_heads * c.max_ctx;
+  if (kv_rows >= (int64_t)1 << 31) {
+    set_error(ctx, "bf16 attention needs max_batch * n_kv_heads * max_ctx < 2^31");
+    return DFLASH_E_UNSUPPORTED;
+  }
+  {
+    const CUtensorMap* mk = nullptr;
+    const CUtensorMap* mv = nullptr;
+    DF_TRY(tmap_2d(ctx, a.kc, kv_rows, kHd, kTK, &mk));
+    DF_TRY(tmap_2d(ctx, a.vc, kv_rows, kHd, kTK, &mv));
+    maps.k = *mk;
+    maps.v = *mv;
+    // Q maps are cached under a key no 2-D map uses (a negative box height)
+    const auto key = std::make_tuple(a.q, (int64_t)p.rows_total, (int64_t)c.n_heads, -p.G);
+    auto it = ctx->tmaps.find(key);
+    if (it == ctx->tmaps.end()) {
+      CUtensorMap m;
+      if (!q_map(&m, a.q, c.n_heads, p.rows_total, p.G)) {
+        set_error(ctx, "cuTensorMapEncodeTiled failed for the query map");
+        return DFLASH_E_CUDA;
+      }
+      it = ctx->tmaps.emplace(key, m).first;
+    }
+    maps.q = it->second;
+  }
   const int POS = 64 / p.G;
   const int q_tiles = (a.q_stride + POS - 1) / POS;
   const int ctas = q_tiles * c.n_kv_heads * a.batch;
@@ -636,7 +799,8 @@ dflash_status attention(dflash_ctx* ctx, const AttnArgs& a, cudaStream_t st) {
   p.n_splits = splits;
   DF_CUDA_TRY(ctx, ensure_attn_smem());
   dim3 grid(q_tiles, c.n_kv_heads, a.batch * splits);
-  DF_CUDA_TRY(ctx, launch_k(ctx->pdl, attn_mma_kernel, dim3(grid), dim3(128), kAttnSmem, st, p));
+  DF_CUDA_TRY(ctx, launch_k(ctx->pdl, attn_tc_kernel, dim3(grid), dim3(kAttnThreads), kAttnSmem, st,
+                            maps, p));
   DF_LAUNCHED(ctx);
   if (splits > 1) {
     dim3 g2(p.rows_total, (c.n_heads + 3) / 4);
@@ -651,7 +815,9 @@ dflash_status attention(dflash_ctx* ctx, const AttnArgs& a, cudaStream_t st) {
 // ---------------------------------------------------------------------------
 static bool op_shape_ok(int batch, int H, int Hkv, int hd, int ctx_len, int block) {
   return batch >= 1 && H >= 1 && Hkv >= 1 && H % Hkv == 0 && hd == kHd && 64 % (H / Hkv) == 0 &&
-         ctx_len >= 0 && block >= 1 && block <= 64 && (int64_t)ctx_len + block < (1 << 30);
+         ctx_len >= 0 && block >= 1 && block <= 64 && (int64_t)ctx_len + block < (1 << 30) &&
+         (int64_t)batch * Hkv * (ctx_len + block) < ((int64_t)1 << 31) &&
+         (int64_t)batch * block * H < ((int64_t)1 << 31);
 }
 
 int64_t block_attention_workspace(int batch, int H, int Hkv, int hd, int ctx_len, int block) {
@@ -706,8 +872,14 @@ dflash_status block_attention(int batch, int H, int Hkv, int hd, int ctx_len, in
   }
   p.n_splits = splits;
   if (ensure_attn_smem() != cudaSuccess) return DFLASH_E_CUDA;
+  AttnMaps maps;
+  const int64_t kv_rows = (int64_t)batch * Hkv * (ctx_len + block);
+  if (!q_map(&maps.q, q, H, p.rows_total, p.G) || !kv_map(&maps.k, k, kv_rows) ||
+      !kv_map(&maps.v, v, kv_rows))
+    return DFLASH_E_CUDA;
   dim3 grid(q_tiles, Hkv, batch * splits);
-  if (launch_k(true, attn_mma_kernel, dim3(grid), dim3(128), kAttnSmem, st, p) != cudaSuccess)
+  if (launch_k(true, attn_tc_kernel, dim3(grid), dim3(kAttnThreads), kAttnSmem, st, maps, p) !=
+      cudaSuccess)
     return DFLASH_E_CUDA;
   if (splits > 1) {
     dim3 g2(p.rows_total, (H + 3) / 4);

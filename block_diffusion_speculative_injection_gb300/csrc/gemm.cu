@@ -292,6 +292,9 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+static dflash_status get_tmap(dflash_ctx* ctx, const void* ptr, int64_t rows, int64_t cols,
+                              int box_rows, const CUtensorMap** out);
+
 static EncodeTiledFn get_encode_fn() {
   static EncodeTiledFn fn = nullptr;
   if (!fn) {
@@ -303,6 +306,28 @@ static EncodeTiledFn get_encode_fn() {
       fn = reinterpret_cast<EncodeTiledFn>(p);
   }
   return fn;
+}
+
+bool encode_tmap_bf16(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims,
+                      const uint64_t* strides, const uint32_t* box) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn || rank < 1 || rank > 3) return false;
+  memset(m, 0, sizeof(*m));
+  cuuint64_t gdim[3], gstride[2];
+  cuuint32_t bx[3], estride[3] = {1u, 1u, 1u};
+  for (int i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    bx[i] = box[i];
+  }
+  for (int i = 0; i + 1 < rank; ++i) gstride[i] = strides[i];
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(ptr), gdim,
+            gstride, bx, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+dflash_status tmap_2d(dflash_ctx* ctx, const void* ptr, int64_t rows, int64_t cols, int box_rows,
+                      const CUtensorMap** out) {
+  return get_tmap(ctx, ptr, rows, cols, box_rows, out);
 }
 
 // 2-D bf16 tensor [rows][cols] (row-major), box [box_rows][64], 128-byte swizzle.

@@ -82,18 +82,48 @@ def test_block_attention_full_grid_sampled(b, ctx):
     assert np.isfinite(out).all()
 
 
+# one KV head of 4 query heads over a long context: a single CTA per split,
+# so the planner spreads the keys over more than 32 splits (the merge's
+# batched path)
+MANY_SPLITS = (1, 4, 1, 6000)  # batch, q heads, kv heads, context
+
+
+def test_many_splits_merge_path():
+    from block_diffusion_speculative_injection_gb300 import capi
+    b, h, hkv, ctx = MANY_SPLITS
+    g = torch.Generator(device="cuda").manual_seed(11)
+    q = torch.randn(b, BLK, h, HD, device="cuda", generator=g).to(torch.bfloat16)
+    k = torch.randn(b, hkv, ctx + BLK, HD, device="cuda", generator=g).to(torch.bfloat16)
+    v = torch.randn(b, hkv, ctx + BLK, HD, device="cuda", generator=g).to(torch.bfloat16)
+    out = torch.empty_like(q)
+    need = capi.dflash_block_attention_workspace(b, h, hkv, ctx, BLK)
+    assert need // (b * BLK * h * (HD + 2) * 4) > 32
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    for causal in (0, 1):
+        capi.dflash_block_attention(b, h, hkv, ctx, BLK, causal, q, k, v, out, ws)
+        torch.cuda.synchronize()
+        kk = k[0, 0].float().cpu().numpy().astype(np.float64)
+        vv = v[0, 0].float().cpu().numpy().astype(np.float64)
+        qq = q[0].float().cpu().numpy().astype(np.float64)
+        got = out[0].float().cpu().numpy()
+        for j in range(BLK):
+            n = ctx + j + 1 if causal else ctx + BLK
+            ref = attend(qq[j], kk[:n, None, :], vv[:n, None, :])
+            np.testing.assert_allclose(got[j], ref, atol=2e-2, rtol=1e-2)
+
+
 def test_full_grid_covers_every_combine_regime():
     """The split merge has three code paths: up to 8 splits, up to 32 (all
     loads in flight at once) and more (batches of 32).  The sampled grid
-    above must reach each of them."""
+    above and the many-splits case must reach each of them."""
     from block_diffusion_speculative_injection_gb300 import capi
     seen = set()
-    for b in wl.ATTN_OP_BATCH:
-        for ctx in wl.ATTN_OP_CTX:
-            need = capi.dflash_block_attention_workspace(b, H, HKV, ctx, BLK)
-            splits = need // (b * BLK * H * (HD + 2) * 4) if need > 0 else 1
-            if splits > 1:
-                seen.add(0 if splits <= 8 else (1 if splits <= 32 else 2))
+    shapes = [(b, H, HKV, ctx) for b in wl.ATTN_OP_BATCH for ctx in wl.ATTN_OP_CTX]
+    for b, h, hkv, ctx in shapes + [MANY_SPLITS]:
+        need = capi.dflash_block_attention_workspace(b, h, hkv, ctx, BLK)
+        splits = need // (b * BLK * h * (HD + 2) * 4) if need > 0 else 1
+        if splits > 1:
+            seen.add(0 if splits <= 8 else (1 if splits <= 32 else 2))
     assert seen == {0, 1, 2}, seen
 
 

@@ -84,12 +84,12 @@ def test_gemm_plan_refuses_bad_sizes(lib):
 
 
 def test_attention_plan_one_sequence(lib):
-    # 16 rows x 32 heads over 2048 + 16 keys: 8 KV heads, 33 key tiles, one
-    # tile per split in a single wave
+    # 16 rows x 32 heads over 2048 + 16 keys: 8 KV heads, 17 key tiles of 128,
+    # one tile per split, all CTAs (one per SM) in a single wave
     p = capi.dflash_plan_attention(GB300_SMS, 1, 32, 8, 16, 2048 + 16)
-    assert p == {"splits": 33, "keys_per_split": 64, "ctas": 8 * 33}
+    assert p == {"splits": 17, "keys_per_split": 128, "ctas": 8 * 17}
     # short context: no split
-    assert capi.dflash_plan_attention(GB300_SMS, 1, 32, 8, 16, 64)["splits"] == 1
+    assert capi.dflash_plan_attention(GB300_SMS, 1, 32, 8, 16, 128)["splits"] == 1
 
 
 @pytest.mark.parametrize("sms", [GB300_SMS, 40])
@@ -99,12 +99,12 @@ def test_attention_plan_rules(lib, sms):
         q = 16
         p = capi.dflash_plan_attention(sms, batch, H, Hkv, q, keys, min_s)
         s, kps, ctas = p["splits"], p["keys_per_split"], p["ctas"]
-        tiles = (keys + 63) // 64
+        tiles = (keys + 127) // 128
         assert 1 <= s <= min(256, tiles)
         base = ((q + 64 // (H // Hkv) - 1) // (64 // (H // Hkv))) * Hkv * batch
         assert ctas == base * s
         if s > 1:
-            assert kps % 64 == 0
+            assert kps % 128 == 0
             assert s * kps >= keys and (s - 1) * kps < keys  # no split is empty
         else:
             assert kps == keys

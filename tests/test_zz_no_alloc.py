@@ -47,13 +47,24 @@ def test_noalloc_matches_workspace_entry_twice(b, ctx, causal):
 
 
 def test_noalloc_refuses_sizes_beyond_its_array():
+    """A shape whose split-KV partials exceed the fixed array is refused with
+    DFLASH_E_CAPACITY (the first candidate that needs more than 16 MiB on this
+    GPU; many heads of 64 query rows each give many CTAs, hence many
+    partial rows)."""
     from block_diffusion_speculative_injection_gb300 import capi
-    b, ctx = 32, 16384
-    need = capi.dflash_block_attention_workspace(b, H, HKV, ctx, BLK)
-    if need <= LIMIT:
-        pytest.skip("on this GPU these sizes fit the fixed array")
-    q, k, v = _inputs(b, ctx, 7)
+    cands = [(32, 32, 8, 16384, 16), (1, 512, 512, 4096, 64), (2, 512, 512, 4096, 64),
+             (1, 1024, 1024, 2048, 64)]
+    pick = None
+    for b, h, hkv, ctx, blk in cands:
+        if capi.dflash_block_attention_workspace(b, h, hkv, ctx, blk) > LIMIT:
+            pick = (b, h, hkv, ctx, blk)
+            break
+    assert pick is not None, "no candidate shape exceeds the fixed array"
+    b, h, hkv, ctx, blk = pick
+    q = torch.zeros(b, blk, h, HD, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(b, hkv, ctx + blk, HD, dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros_like(k)
     out = torch.empty_like(q)
     with pytest.raises(capi.DFlashError) as e:
-        capi.dflash_block_attention_noalloc(b, H, HKV, ctx, BLK, 0, q, k, v, out)
+        capi.dflash_block_attention_noalloc(b, h, hkv, ctx, blk, 0, q, k, v, out)
     assert e.value.status == 2  # DFLASH_E_CAPACITY
