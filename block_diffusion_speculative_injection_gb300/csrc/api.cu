@@ -237,16 +237,43 @@ static dflash_status run_lm_head(dflash_ctx* ctx, int n, int topk, int32_t* argm
                                  int32_t* topk_ids, float* topk_logp, float* logits,
                                  cudaStream_t st) {
   const dflash_config& c = ctx->cfg;
+  const int32_t* lm_arg = ctx->lm_rows + c.max_rows;
+  GemmSegs lm_w{{ctx->lm_head}, {c.vocab}, 1};
+  if (c.dtype != DFLASH_F32) {
+    // the lm_head epilogue reduces every 128-feature tile of the vocabulary
+    // to candidates, and the logits reach memory only for the rows the
+    // caller asked for; a small second kernel merges the tiles
+    const int K = topk > 2 ? topk : 2;
+    const int n_tiles = (c.vocab + 127) / 128;
+    // rows per launch: what the candidate buffers hold (every decode pass
+    // fits in one; a long prefill that keeps every row's result takes several)
+    const int chunk = (int)std::min<size_t>(ctx->vpart_cap / ((size_t)n_tiles * K), (size_t)n);
+    if (n > 0 && chunk < 1) return fail(ctx, DFLASH_E_CAPACITY, "vocab partial buffer too small");
+    for (int i0 = 0; i0 < n; i0 += chunk) {
+      const int m = std::min(chunk, n - i0);
+      EpiArgs e = epi_base(ctx, kEpiVocab);
+      e.vr_id = ctx->vk_part;
+      e.vr_v = ctx->vv_part;
+      e.vr_lse = topk > 0 ? ctx->vv_part + ctx->vpart_cap : nullptr;
+      e.vr_vec = lm_arg + i0 + c.max_rows;
+      e.vr_logits = logits;
+      e.vr_k = K;
+      int sp = 1;
+      const void* x = static_cast<const uint8_t*>(ctx->lm_in) + (size_t)i0 * c.d_model * ctx->esize;
+      DF_TRY(gemm(ctx, x, m, c.d_model, lm_w, e, 1, &sp, st));
+      DF_TRY(launch_vocab_merge(ctx, m, n_tiles, K, lm_arg + i0, topk, argmax, margin, topk_ids,
+                                topk_logp, st));
+    }
+    return DFLASH_OK;
+  }
   const size_t chunk_rows = ctx->ws_elems / (size_t)c.vocab;
   if (chunk_rows < 1) return fail(ctx, DFLASH_E_CAPACITY, "workspace smaller than one vocab row");
-  const int32_t* lm_arg = ctx->lm_rows + c.max_rows;
   for (int i0 = 0; i0 < n; i0 += (int)chunk_rows) {
     const int m = (int)std::min<size_t>(chunk_rows, (size_t)(n - i0));
-    GemmSegs lm{{ctx->lm_head}, {c.vocab}, 1};
     int sp = 1;
     const void* x = static_cast<const uint8_t*>(ctx->lm_in) + (size_t)i0 * c.d_model * ctx->esize;
-    DF_TRY(gemm(ctx, x, m, c.d_model, lm, epi_base(ctx, kEpiSlab), 1, &sp, st));
-    DF_TRY(launch_vocab_reduce(ctx, m, c.vocab, lm_arg + i0, m, topk, argmax, margin, topk_ids,
+    DF_TRY(gemm(ctx, x, m, c.d_model, lm_w, epi_base(ctx, kEpiSlab), 1, &sp, st));
+    DF_TRY(launch_vocab_reduce(ctx, m, c.vocab, lm_arg + i0, topk, argmax, margin, topk_ids,
                                topk_logp, logits, st));
   }
   return DFLASH_OK;
@@ -347,10 +374,14 @@ dflash_status dflash_create(const dflash_config* cfg, dflash_ctx** out) {
                                       (size_t)std::min(c.n_draft_layers, 6) * 2 * c.n_kv_heads *
                                           c.head_dim});
   const size_t lm_rows = (size_t)c.max_batch * std::max(c.block_size, std::max(c.max_tree_nodes, 1));
-  wsn = std::max(wsn, lm_rows * (size_t)c.vocab);
+  // fp32 storage writes the lm_head logits to the workspace (bf16 reduces
+  // them in the GEMM epilogue)
+  if (c.dtype == DFLASH_F32) wsn = std::max(wsn, lm_rows * (size_t)c.vocab);
   ctx->ws_elems = wsn;
   ctx->part_rows_cap = std::max<size_t>(R * c.n_heads, 1 << 18);
-  const int n_chunks = (c.vocab + 4095) / 4096;
+  // vocabulary candidates: up to 16 per row and chunk (4096 ids for fp32,
+  // one 128-feature lm_head tile for bf16)
+  const size_t n_chunks = c.dtype == DFLASH_F32 ? (c.vocab + 4095) / 4096 : (c.vocab + 127) / 128;
   ctx->vpart_cap = std::max<size_t>(lm_rows, 1) * n_chunks * 16;
   ctx->rope_len = c.max_ctx;
 

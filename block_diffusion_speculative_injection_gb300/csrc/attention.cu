@@ -12,9 +12,10 @@
 // the G query heads that share one KV head, so each K/V tile streamed from
 // HBM feeds G heads at once.  Q and the K/V tiles (128 keys) arrive by TMA;
 // S = Q K^T and O += P V run on tcgen05 with the accumulators in tensor
-// memory; the online softmax (exp2 domain) runs in one warp group that owns
-// one query row per thread (attn_tc_kernel).  Long contexts are split across
-// CTAs; a combine kernel merges the partial (m, l, O).
+// memory; the online softmax (exp2 domain) runs in one warp group, two
+// threads per query row, each taking 64 of the 128 keys of a tile
+// (attn_tc_kernel).  Long contexts are split across CTAs; a combine kernel
+// merges the partial (m, l, O).
 #include <cfloat>
 #include <cmath>
 #include <cstring>

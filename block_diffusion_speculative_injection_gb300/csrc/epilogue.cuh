@@ -18,7 +18,7 @@
 namespace dflash {
 
 enum EpiKind { kEpiSlab = 0, kEpiQKV = 1, kEpiSwiGLU = 2, kEpiResid = 3, kEpiStore = 4,
-               kEpiInject = 5 };
+               kEpiInject = 5, kEpiVocab = 6 };
 
 struct EpiArgs {
   int kind;
@@ -47,6 +47,16 @@ struct EpiArgs {
   float* trace;  // optional fp32 copy of the updated residual rows
   // STORE
   void* out;
+  // VOCAB (lm_head): per token row and 128-feature tile, the best vr_k
+  // logits (value descending, id ascending) and, with vr_lse, the tile's
+  // (max, sum exp(x - max)); the logits themselves only for rows with
+  // vr_vec[row] >= 0 when vr_logits is set
+  int32_t* vr_id;          // [row][tile][vr_k]
+  float* vr_v;             // [row][tile][vr_k]
+  float* vr_lse;           // [row][tile][2] or NULL
+  const int32_t* vr_vec;   // [row] row of vr_logits, < 0: none
+  float* vr_logits;        // [vec row][N] or NULL
+  int vr_k;                // 2..16
   int32_t* status;
 };
 

@@ -11,10 +11,13 @@
 // add, store) is fused: straight from tensor memory when the tile takes the
 // whole K range, else the K splits of the tile form a thread-block cluster
 // and sum their partial tiles through distributed shared memory in split
-// order.  Only the lm_head writes a plain fp32 result.
+// order.  The lm_head's epilogue reduces each 128-feature vocabulary tile to
+// per-row candidates (best logits, max and sum of exp) instead of writing the
+// logits; the plain fp32 result remains for the small fp32 model.
 //
 // f32 storage: a tiled SIMT kernel (fp32 FMA) writes per-split fp32 slabs
 // and an epilogue kernel sums them in a fixed order (the small fp32 model).
+#include <climits>
 #include <cstdio>
 #include <cstring>
 
@@ -39,6 +42,76 @@ struct TcParams {
   int32_t* status;
   EpiArgs epi;
 };
+
+// lm_head tile reduction: the CTA's 128 x BN logits sit feature-major in
+// shared memory (row pitch BN + 1 floats, so both the TMEM-order writes and
+// these per-token column scans are free of bank conflicts).  One thread per
+// token row scans the tile's features in id order: a strict "greater" keeps
+// the lower id of equal logits ahead.
+__device__ __forceinline__ void vocab_tile_reduce(const EpiArgs& e, const float* tile, int pitch,
+                                                  int nf, int n0, int m0, int BN, int M) {
+  const int K = e.vr_k;
+  for (int u = threadIdx.x; u < BN; u += blockDim.x) {
+    const int t = m0 + u;
+    if (t >= M) break;
+    const size_t pb = (size_t)t * gridDim.x + blockIdx.x;
+    const float* col = tile + u;
+    float top;
+    if (K == 2) {  // argmax and margin
+      float v1 = -INFINITY, v2 = -INFINITY;
+      int i1 = INT_MAX, i2 = INT_MAX;
+      for (int f = 0; f < nf; ++f) {
+        const float x = col[f * pitch];
+        if (x > v2) {
+          if (x > v1) {
+            v2 = v1;
+            i2 = i1;
+            v1 = x;
+            i1 = n0 + f;
+          } else {
+            v2 = x;
+            i2 = n0 + f;
+          }
+        }
+      }
+      e.vr_id[pb * 2] = i1;
+      e.vr_id[pb * 2 + 1] = i2;
+      e.vr_v[pb * 2] = v1;
+      e.vr_v[pb * 2 + 1] = v2;
+      top = v1;
+    } else {  // a sorted list of K (insertion; most logits fail the first compare)
+      float lv[16];
+      int li[16];
+      for (int k = 0; k < K; ++k) {
+        lv[k] = -INFINITY;
+        li[k] = INT_MAX;
+      }
+      for (int f = 0; f < nf; ++f) {
+        const float x = col[f * pitch];
+        if (x > lv[K - 1]) {
+          int q = K - 1;
+          while (q > 0 && x > lv[q - 1]) {
+            lv[q] = lv[q - 1];
+            li[q] = li[q - 1];
+            --q;
+          }
+          lv[q] = x;
+          li[q] = n0 + f;
+        }
+      }
+      for (int k = 0; k < K; ++k) {
+        e.vr_id[pb * K + k] = li[k];
+        e.vr_v[pb * K + k] = lv[k];
+      }
+      top = lv[0];
+    }
+    if (e.vr_lse) {
+      float se = 0.f;
+      for (int f = 0; f < nf; ++f) se += __expf(col[f * pitch] - top);
+      *reinterpret_cast<float2*>(e.vr_lse + pb * 2) = make_float2(top, se);
+    }
+  }
+}
 
 __global__ void __launch_bounds__(256, 1)
     gemm_tc_kernel(const __grid_constant__ TmapSet wmaps, const __grid_constant__ CUtensorMap xmap,
@@ -167,6 +240,31 @@ __global__ void __launch_bounds__(256, 1)
   // a warp reads TMEM lane quarter warp % 4; with 8 warps the two groups of
   // 4 take alternate 16-row chunks
   const int quarter = warp & 3, c_first = (warp >> 2) * 16, c_step = ((int)blockDim.x >> 7) * 16;
+  if (p.epi.kind == kEpiVocab) {  // lm_head: reduce the tile over its 128 features
+    const EpiArgs& e = p.epi;
+    const int pitch = BN + 1;
+    float* tile = reinterpret_cast<float*>(smem);  // the pipeline buffers are idle now
+    const int f = quarter * 32 + lane, feat = n0 + f;
+    for (int c = c_first; c < BN; c += c_step) {
+      float v[16];
+      tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c, v);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) tile[f * pitch + c + i] = v[i];
+      if (e.vr_logits && feat < p.N) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int t = m0 + c + i;
+          const int vi = t < p.M ? __ldg(e.vr_vec + t) : -1;
+          if (vi >= 0) e.vr_logits[(size_t)vi * p.N + feat] = v[i];
+        }
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, tmem_cols);
+    vocab_tile_reduce(e, tile, pitch, min(128, p.N - n0), n0, m0, BN, p.M);
+    return;
+  }
   if (p.epi.kind == kEpiSlab) {  // plain fp32 result (lm_head logits), no K split
     const int feat = n0 + quarter * 32 + lane;
     for (int c = c_first; c < BN; c += c_step) {
@@ -367,7 +465,9 @@ static size_t tc_smem_bytes(int BN, int stages);
 
 static int tc_stages(int BN) {
   const int per = 128 * 64 * 2 + BN * 64 * 2;
-  int budget = (BN <= 32) ? 110 * 1024 : 200 * 1024;  // small tiles: 2 CTAs per SM
+  // small tiles: 2 CTAs per SM (a third, left for the next launch's weight
+  // prefetch, measured slower: its 3 stages per CTA hold too little in flight)
+  int budget = (BN <= 32) ? 110 * 1024 : 200 * 1024;
   int s = budget / per;
   if (s > 8) s = 8;
   if (s < 2) s = 2;
@@ -417,7 +517,7 @@ static TcPlan plan_tc(int sm_count, int M, int N, int K, int kind, int max_split
   if (splits > max_cluster_splits) splits = max_cluster_splits;
   if (splits > max_splits) splits = max_splits;
   if (splits > t.n_kb / 4) splits = t.n_kb / 4;
-  if (splits < 1 || kind == kEpiSlab) splits = 1;
+  if (splits < 1 || kind == kEpiSlab || kind == kEpiVocab) splits = 1;
   // ... and every cluster of the launch resident at once: clusters that wait
   // for a second wave double the launch time.  A cluster sits inside one GPC,
   // so fewer than slots / size clusters fit; on GB300 (152 SMs, 2 CTAs per
@@ -435,7 +535,7 @@ static TcPlan plan_tc(int sm_count, int M, int N, int K, int kind, int max_split
 
 dflash_status plan_gemm(int sm_count, int M, int N, int K, int kind, int max_splits, int32_t* out) {
   if (!out || sm_count < 1 || M < 1 || N < 1 || K < 64 || K % 64 != 0 || max_splits < 1 ||
-      kind < kEpiSlab || kind > kEpiInject || (kind == kEpiSwiGLU && N % 128 != 0))
+      kind < kEpiSlab || kind > kEpiVocab || (kind == kEpiSwiGLU && N % 128 != 0))
     return DFLASH_E_INVALID_ARG;
   const TcPlan t = plan_tc(sm_count, M, N, K, kind, max_splits);
   out[0] = t.BN;
@@ -458,10 +558,19 @@ dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs&
   int N = 0;
   for (int i = 0; i < segs.n; ++i) N += segs.rows[i];
   if (segs.n < 1 || segs.n > kMaxSeg) return DFLASH_E_INVALID_ARG;
-  ProfScope prof(ctx, kProfGemm, st, ((double)N * K + (double)M * K) * ctx->esize + 4.0 * M * N,
+  // result bytes: the fp32 logits, or the vocabulary partials of every tile
+  const double out_bytes = epi_in.kind == kEpiVocab
+                               ? (double)M * ((N + 127) / 128) * (8.0 * epi_in.vr_k +
+                                                                  (epi_in.vr_lse ? 8.0 : 0.0))
+                               : 4.0 * M * N;
+  ProfScope prof(ctx, kProfGemm, st, ((double)N * K + (double)M * K) * ctx->esize + out_bytes,
                  2.0 * M * N * K);
 
   if (ctx->cfg.dtype == DFLASH_F32) {
+    if (epi_in.kind == kEpiVocab) {
+      set_error(ctx, "the fused lm_head reduction needs bf16 storage");
+      return DFLASH_E_UNSUPPORTED;
+    }
     SegPtrs sp;
     memset(&sp, 0, sizeof(sp));
     sp.n = segs.n;
@@ -510,6 +619,13 @@ dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs&
   if (epi_in.kind == kEpiSlab && (size_t)M * N > ctx->ws_elems) {
     set_error(ctx, "GEMM output %dx%d exceeds workspace", M, N);
     return DFLASH_E_CAPACITY;
+  }
+  if (epi_in.kind == kEpiVocab &&
+      (epi_in.vr_k < 2 || epi_in.vr_k > 16 || !epi_in.vr_id || !epi_in.vr_v ||
+       (epi_in.vr_logits && !epi_in.vr_vec) ||
+       (size_t)128 * (BN + 1) * sizeof(float) > (size_t)stages * (128 * 64 * 2 + BN * 64 * 2))) {
+    set_error(ctx, "lm_head reduction: bad candidate count or buffers");
+    return DFLASH_E_INVALID_ARG;
   }
   if (epi_in.kind == kEpiSwiGLU &&
       (segs.n != 2 || segs.rows[0] != epi_in.F || segs.rows[1] != epi_in.F || epi_in.F % 64 != 0)) {

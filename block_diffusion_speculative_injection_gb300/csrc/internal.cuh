@@ -182,10 +182,16 @@ dflash_status launch_embed(dflash_ctx* ctx, const int32_t* tokens, int rows, int
 // out[i] = RMSNorm(resid[rows_in ? rows_in[i] : i]) * gain, i < n_out
 dflash_status launch_norm(dflash_ctx* ctx, int n_out, const int32_t* rows_in, const void* gain,
                           void* out, cudaStream_t st);
+// fp32 logits slab (ctx->ws) -> chunk candidates -> per-row results
 dflash_status launch_vocab_reduce(dflash_ctx* ctx, int rows, int vocab, const int32_t* row_out,
-                                  int n_out, int topk, int32_t* argmax, float* margin,
-                                  int32_t* topk_ids, float* topk_logp, float* logits_copy,
-                                  cudaStream_t st);
+                                  int topk, int32_t* argmax, float* margin, int32_t* topk_ids,
+                                  float* topk_logp, float* logits_copy, cudaStream_t st);
+// per-row results from K candidates of each of n_chunks chunks already in
+// ctx->vk_part / ctx->vv_part (the lm_head epilogue's); row_out = [arg_idx |
+// vec_idx] (vec_idx at + max_rows)
+dflash_status launch_vocab_merge(dflash_ctx* ctx, int rows, int n_chunks, int K,
+                                 const int32_t* row_out, int topk, int32_t* argmax, float* margin,
+                                 int32_t* topk_ids, float* topk_logp, cudaStream_t st);
 
 // speculation control
 dflash_status launch_accept_linear(dflash_ctx* ctx, int batch, const int32_t* seq_ids,

@@ -1,10 +1,12 @@
 // Reductions over the vocabulary of one lm_head pass.
 //
-// Pass 1 (grid rows x chunks): each CTA scans one chunk of a row's logits
-// and keeps its best K candidates (value descending, id ascending) plus the
-// chunk's (max, sum exp(x - max)).  Pass 2 (one CTA per row) merges the
-// chunks: argmax, top-1 minus top-2 margin, top-k ids and log-softmax
-// values (logit - logsumexp, temperature 1).
+// Pass 1 gives, per row and chunk of the vocabulary, the chunk's best K
+// candidates (value descending, id ascending) plus its (max, sum exp(x -
+// max)).  With bf16 storage the lm_head GEMM's epilogue produces them per
+// 128-feature tile (the logits never reach memory); the fp32 model's slab
+// is scanned here in chunks of 4096 (vocab_pass1_kernel).  Pass 2 (one CTA
+// per row) merges the chunks: argmax, top-1 minus top-2 margin, top-k ids
+// and log-softmax values (logit - logsumexp, temperature 1).
 #include <cfloat>
 #include <climits>
 
@@ -55,6 +57,22 @@ __device__ void block_select(const float* lv, const int* li, int n, int K, Cand*
     if (head < n && li[head] == out[k].id && lv[head] == out[k].v) ++head;
     __syncthreads();
   }
+}
+
+// block-wide sum (kSum) or max, result in every thread; red holds 32 floats
+template <bool kSum>
+__device__ float block_reduce(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float w = __shfl_xor_sync(0xffffffffu, v, o);
+    v = kSum ? v + w : fmaxf(v, w);
+  }
+  __syncthreads();  // red may still be read from an earlier call
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  v = red[0];
+  for (int i = 1; i < (int)(blockDim.x >> 5); ++i) v = kSum ? v + red[i] : fmaxf(v, red[i]);
+  return v;
 }
 
 __global__ void __launch_bounds__(kVocabThreads)
@@ -159,15 +177,21 @@ __global__ void __launch_bounds__(kVocabThreads)
     }
   }
   block_select(lv, li, n, K, best, red);
-  if (threadIdx.x == 0) {
+  if (topk > 0) {  // log-sum-exp over the chunks (only the top-k log-probs use it)
+    __shared__ float lred[32];
+    const float2* pl = reinterpret_cast<const float2*>(part_lse) + (size_t)row * n_chunks;
     float M = -INFINITY;
-    for (int c = 0; c < n_chunks; ++c) M = fmaxf(M, part_lse[((size_t)row * n_chunks + c) * 2]);
+    for (int c = threadIdx.x; c < n_chunks; c += kVocabThreads) M = fmaxf(M, pl[c].x);
+    M = block_reduce<false>(M, lred);
     float S = 0.f;
-    for (int c = 0; c < n_chunks; ++c) {
-      const size_t pb = ((size_t)row * n_chunks + c) * 2;
-      S += part_lse[pb + 1] * __expf(part_lse[pb] - M);
+    for (int c = threadIdx.x; c < n_chunks; c += kVocabThreads) {
+      const float2 ms = pl[c];
+      S += ms.y * __expf(ms.x - M);
     }
-    lse_s = M + logf(S);
+    S = block_reduce<true>(S, lred);
+    if (threadIdx.x == 0) lse_s = M + logf(S);
+  }
+  if (threadIdx.x == 0) {
     const int ai = arg_idx[row];
     if (ai >= 0) {
       if (argmax) argmax[ai] = best[0].id;
@@ -182,12 +206,27 @@ __global__ void __launch_bounds__(kVocabThreads)
   }
 }
 
-dflash_status launch_vocab_reduce(dflash_ctx* ctx, int rows, int vocab, const int32_t* row_out,
-                                  int n_out, int topk, int32_t* argmax, float* margin,
-                                  int32_t* topk_ids, float* topk_logp, float* logits_copy,
-                                  cudaStream_t st) {
+dflash_status launch_vocab_merge(dflash_ctx* ctx, int rows, int n_chunks, int K,
+                                 const int32_t* row_out, int topk, int32_t* argmax, float* margin,
+                                 int32_t* topk_ids, float* topk_logp, cudaStream_t st) {
   ProfScope prof__(ctx, kProfVocab, st);
-  (void)n_out;
+  if (rows <= 0) return DFLASH_OK;
+  if ((size_t)rows * n_chunks * K > ctx->vpart_cap || K < 2 || K > kMaxK || topk > K) {
+    set_error(ctx, "vocab partial buffer too small");
+    return DFLASH_E_CAPACITY;
+  }
+  // row_out = [arg_idx | vec_idx] for these rows
+  DF_CUDA_TRY(ctx, launch_k(ctx->pdl, vocab_pass2_kernel, dim3(rows), dim3(kVocabThreads), 0, st,
+                            K, topk, n_chunks, ctx->vk_part, ctx->vv_part,
+                            ctx->vv_part + ctx->vpart_cap, row_out, row_out + ctx->cfg.max_rows,
+                            argmax, margin, topk_ids, topk_logp));
+  DF_LAUNCHED(ctx);
+  return DFLASH_OK;
+}
+
+dflash_status launch_vocab_reduce(dflash_ctx* ctx, int rows, int vocab, const int32_t* row_out,
+                                  int topk, int32_t* argmax, float* margin, int32_t* topk_ids,
+                                  float* topk_logp, float* logits_copy, cudaStream_t st) {
   if (rows <= 0) return DFLASH_OK;
   const int K = topk > 2 ? topk : 2;
   const int n_chunks = (vocab + kVocabChunk - 1) / kVocabChunk;
@@ -195,20 +234,17 @@ dflash_status launch_vocab_reduce(dflash_ctx* ctx, int rows, int vocab, const in
     set_error(ctx, "vocab partial buffer too small");
     return DFLASH_E_CAPACITY;
   }
-  // row_out = [arg_idx | vec_idx] for these rows
-  const int32_t* arg_idx = row_out;
-  const int32_t* vec_idx = row_out + ctx->cfg.max_rows;
-  float* part_v = ctx->vv_part;
-  float* part_lse = ctx->vv_part + ctx->vpart_cap;
-  dim3 g1(rows, n_chunks);
-  DF_CUDA_TRY(ctx, launch_k(ctx->pdl, vocab_pass1_kernel, dim3(g1), dim3(kVocabThreads), 0, st, ctx->ws, vocab, K, vec_idx, logits_copy,
-                                                   ctx->vk_part, part_v, part_lse, n_chunks));
-  DF_LAUNCHED(ctx);
-  DF_CUDA_TRY(ctx, launch_k(ctx->pdl, vocab_pass2_kernel, dim3(rows), dim3(kVocabThreads), 0, st, K, topk, n_chunks, ctx->vk_part, part_v,
-                                                     part_lse, arg_idx, vec_idx, argmax, margin,
-                                                     topk_ids, topk_logp));
-  DF_LAUNCHED(ctx);
-  return DFLASH_OK;
+  {
+    ProfScope prof__(ctx, kProfVocab, st);
+    dim3 g1(rows, n_chunks);
+    DF_CUDA_TRY(ctx, launch_k(ctx->pdl, vocab_pass1_kernel, dim3(g1), dim3(kVocabThreads), 0, st,
+                              ctx->ws, vocab, K, row_out + ctx->cfg.max_rows, logits_copy,
+                              ctx->vk_part, ctx->vv_part, ctx->vv_part + ctx->vpart_cap,
+                              n_chunks));
+    DF_LAUNCHED(ctx);
+  }
+  return launch_vocab_merge(ctx, rows, n_chunks, K, row_out, topk, argmax, margin, topk_ids,
+                            topk_logp, st);
 }
 
 }  // namespace dflash

@@ -427,9 +427,10 @@ DFLASH_API dflash_status dflash_profile_read(dflash_ctx *ctx, int32_t kind, int6
  * picks, so that a caller (or a test) can see them without a GPU.
  *
  * Tensor-core GEMM of M token rows by an N x K weight (K a multiple of 64)
- * on a GPU with sm_count SMs.  kind: 0 fp32 result (lm_head), 1 QKV, 2 SwiGLU
+ * on a GPU with sm_count SMs.  kind: 0 fp32 result, 1 QKV, 2 SwiGLU
  * (N = gate rows + up rows, a multiple of 128), 3 residual add, 4 store,
- * 5 injected K/V.  max_splits caps the K split.  plan_out[7] receives:
+ * 5 injected K/V, 6 lm_head with the vocabulary reduction in the epilogue.
+ * max_splits caps the K split.  plan_out[7] receives:
  * token rows per tile, token-row tiles, 128-row weight tiles, pipeline stages,
  * K splits (= thread-block cluster size), threads per CTA, dynamic shared
  * memory bytes.  DFLASH_E_INVALID_ARG for sizes the GEMM does not take. */

@@ -11,7 +11,7 @@ import pytest
 
 from block_diffusion_speculative_injection_gb300 import capi
 
-QKV, SWIGLU, RESID, SLAB = 1, 2, 3, 0
+QKV, SWIGLU, RESID, SLAB, VOCAB = 1, 2, 3, 0, 6
 GB300_SMS = 152
 
 
@@ -34,6 +34,9 @@ def test_qwen3_8b_one_sequence_grids(lib):
     assert grid(capi.dflash_plan_gemm(GB300_SMS, 16, 4096, 12288, RESID)) == (32, 1, 8)
     assert grid(capi.dflash_plan_gemm(GB300_SMS, 16, 2 * 12288, 4096, SWIGLU)) == (192, 1, 1)
     assert grid(capi.dflash_plan_gemm(GB300_SMS, 16, 151936, 4096, SLAB)) == (1187, 1, 1)
+    # the lm_head with its vocabulary reduction: one CTA per 128 ids, no K split
+    assert grid(capi.dflash_plan_gemm(GB300_SMS, 16, 151936, 4096, VOCAB)) == (1187, 1, 1)
+    assert grid(capi.dflash_plan_gemm(GB300_SMS, 512, 151936, 4096, VOCAB)) == (1187, 2, 1)
     p = capi.dflash_plan_gemm(GB300_SMS, 16, 6144, 4096, QKV)
     assert (p["BN"], p["threads"]) == (16, 128)
 
@@ -49,7 +52,8 @@ def test_qwen3_8b_32_sequences_qkv(lib):
 @pytest.mark.parametrize("sms", [GB300_SMS, 132, 20])
 def test_gemm_plan_rules(lib, sms):
     shapes = [(6144, 4096, QKV), (4096, 4096, RESID), (4096, 12288, RESID),
-              (24576, 4096, SWIGLU), (151936, 4096, SLAB), (2048, 8192, 4), (10240, 4096, 5)]
+              (24576, 4096, SWIGLU), (151936, 4096, SLAB), (2048, 8192, 4), (10240, 4096, 5),
+              (151936, 4096, VOCAB)]
     for M, (N, K, kind) in itertools.product(list(range(1, 80)) + [96, 128, 129, 200, 256, 257,
                                                                   300, 512, 777, 1024, 2048],
                                              shapes):
@@ -69,7 +73,7 @@ def test_gemm_plan_rules(lib, sms):
         if sp > 1:
             assert BN * 128 * 4 <= stage_mem
         assert 1 <= sp <= 8 and sp <= K // 64 // 4 or sp == 1
-        if kind in (SWIGLU, SLAB):
+        if kind in (SWIGLU, SLAB, VOCAB):
             assert sp == 1
         if sp > 1:
             slots = (2 if BN <= 32 else 1) * sms
@@ -78,7 +82,7 @@ def test_gemm_plan_rules(lib, sms):
 
 def test_gemm_plan_refuses_bad_sizes(lib):
     for args in [(152, 0, 4096, 4096, 1), (152, 16, 4096, 100, 1), (152, 16, 4096, 0, 1),
-                 (0, 16, 4096, 4096, 1), (152, 16, 4096, 4096, 9), (152, 16, 4160, 4096, SWIGLU)]:
+                 (0, 16, 4096, 4096, 1), (152, 16, 4096, 4096, 7), (152, 16, 4160, 4096, SWIGLU)]:
         with pytest.raises(capi.DFlashError):
             capi.dflash_plan_gemm(*args)
 
