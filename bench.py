@@ -500,7 +500,7 @@ KERNEL_REV = "gemm-v5"
 ATTN_KERNELS = "attn_tc_kernel (+ attn_combine_kernel)"
 
 
-def attn_op_points(steps: int, warmup: int, local: int):
+def attn_op_points(steps: int, warmup: int, local: int, only=None):
     """Block attention op (dflash_block_attention) over the grid of context
     lengths x batches: Q [b,16,32,128], K/V [b,8,ctx+16,128] bf16, block
     visible without mask.  Each point: `warmup` calls, then `steps` calls
@@ -523,33 +523,33 @@ def attn_op_points(steps: int, warmup: int, local: int):
     sampler = ClockSampler(local)
     points = []
     sampler.start()
-    for ctx in wl.ATTN_OP_CTX:
-        for b in wl.ATTN_OP_BATCH:
-            q = device_operand("q", b * BLK * H).view(b, BLK, H, HD)
-            k = device_operand("k", b * HKV * (ctx + BLK)).view(b, HKV, ctx + BLK, HD)
-            v = device_operand("v", b * HKV * (ctx + BLK)).view(b, HKV, ctx + BLK, HD)
-            out = torch.empty_like(q)
-            need = capi.dflash_block_attention_workspace(b, H, HKV, ctx, BLK)
-            ws = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
-            for _ in range(warmup):
-                capi.dflash_block_attention(b, H, HKV, ctx, BLK, 0, q, k, v, out, ws)
-            times = []
-            for _ in range(steps):
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                flush.fill_(1)
-                torch.cuda._sleep(200000)  # ~0.1 ms: covers the host side of the call
-                e0.record(stream)
-                capi.dflash_block_attention(b, H, HKV, ctx, BLK, 0, q, k, v, out, ws)
-                e1.record(stream)
-                e1.synchronize()
-                times.append(e0.elapsed_time(e1) * 1e3)
-            us = statistics.median(times)
-            nbytes = b * (4096 * ctx + 327680)  # ctx + block K/V, Q and O per sequence
-            gbs = nbytes / (us * 1e-6) / 1e9
-            points.append({"ctx": ctx, "batch": b, "us": us, "bytes": nbytes, "gbs": gbs,
-                           "frac": gbs / hbm, "roofline_us": nbytes / (hbm * 1e9) * 1e6})
-            del q, k, v, out, ws
+    grid = [only] if only else [(c, b) for c in wl.ATTN_OP_CTX for b in wl.ATTN_OP_BATCH]
+    for ctx, b in grid:
+        q = device_operand("q", b * BLK * H).view(b, BLK, H, HD)
+        k = device_operand("k", b * HKV * (ctx + BLK)).view(b, HKV, ctx + BLK, HD)
+        v = device_operand("v", b * HKV * (ctx + BLK)).view(b, HKV, ctx + BLK, HD)
+        out = torch.empty_like(q)
+        need = capi.dflash_block_attention_workspace(b, H, HKV, ctx, BLK)
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
+        for _ in range(warmup):
+            capi.dflash_block_attention(b, H, HKV, ctx, BLK, 0, q, k, v, out, ws)
+        times = []
+        for _ in range(steps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            flush.fill_(1)
+            torch.cuda._sleep(200000)  # ~0.1 ms: covers the host side of the call
+            e0.record(stream)
+            capi.dflash_block_attention(b, H, HKV, ctx, BLK, 0, q, k, v, out, ws)
+            e1.record(stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e3)
+        us = statistics.median(times)
+        nbytes = b * (4096 * ctx + 327680)  # ctx + block K/V, Q and O per sequence
+        gbs = nbytes / (us * 1e-6) / 1e9
+        points.append({"ctx": ctx, "batch": b, "us": us, "bytes": nbytes, "gbs": gbs,
+                       "frac": gbs / hbm, "roofline_us": nbytes / (hbm * 1e9) * 1e6})
+        del q, k, v, out, ws
     clocks = sampler.stop()
     del flush
     torch.cuda.empty_cache()
@@ -564,8 +564,13 @@ def run_attn_op(args) -> None:
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     hbm, _, src = peaks()
-    points, clocks = attn_op_points(args.steps, args.warmup, local)
-    head = next(pt for pt in points if pt["ctx"] == max(wl.ATTN_OP_CTX) and pt["batch"] == max(wl.ATTN_OP_BATCH))
+    only = None
+    if args.attn_point:  # one point of the grid, e.g. for a profiler capture
+        c, b = args.attn_point.lower().split("x")
+        only = (int(c), int(b))
+    points, clocks = attn_op_points(args.steps, args.warmup, local, only)
+    head = points[0] if only else next(
+        pt for pt in points if pt["ctx"] == max(wl.ATTN_OP_CTX) and pt["batch"] == max(wl.ATTN_OP_BATCH))
     line = {
         "metric": "block attention op: achieved HBM bandwidth (Q [b,16,32,128] over ctx+16 keys, GQA 4:1)",
         "value": head["gbs"], "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
@@ -643,6 +648,16 @@ def workload_steps(w: wl.Workload, steps: int, warmup: int, prof_steps: int, loc
     t_sus, t_src = sustained_tflops()
     flops_step = gflops / max(prof_steps, 1)
     gemm_ms_live = gms / max(prof_steps, 1)
+    # GEMM launches grouped by their work (one group per projection shape)
+    by_shape = {}
+    for lms, lfl in capi.dflash_profile_list(eng.ctx, capi.PROF_GEMM):
+        g = by_shape.setdefault(round(lfl / 1e9, 3), [0, 0.0])
+        g[0] += 1
+        g[1] += lms
+    shapes = [{"gflop": k, "launches_per_step": v[0] / max(prof_steps, 1),
+               "ms_per_step": v[1] / max(prof_steps, 1),
+               "tflops": k * v[0] / v[1] if v[1] else None}
+              for k, v in sorted(by_shape.items(), key=lambda kv: -kv[1][1])]
     out = {
         "workload": w.name, "batch": b, "block": B, "steps": steps, "warmup": warmup,
         "prompt_len": [min(lens), max(lens)], "tree_nodes": nmax or None,
@@ -653,7 +668,8 @@ def workload_steps(w: wl.Workload, steps: int, warmup: int, prof_steps: int, loc
                  "frac_live": (flops_step / (gemm_ms_live / 1e3) / 1e12 / t_sus) if gemm_ms_live else None,
                  "tflops_over_step": flops_step / (step_ms / 1e3) / 1e12,
                  "frac_over_step": flops_step / (step_ms / 1e3) / 1e12 / t_sus,
-                 "peak_tflops": t_sus, "peak_source": t_src + " (sustained bf16)"},
+                 "peak_tflops": t_sus, "peak_source": t_src + " (sustained bf16)",
+                 "by_shape_live": shapes},
         "attention_ms_per_step_live": ams / max(prof_steps, 1),
         "clocks": clocks,
         "timing": "CUDA-graph replays, CUDA events on the launching stream; live per-launch "
@@ -758,7 +774,24 @@ def run_concurrency(args) -> None:
     nb = max(batches)
     prompts = [wl.prompt_tokens(w, s, P) for s in range(nb)]
     steps_total = len(batches) * (args.warmup + args.steps) * 2 + 8
-    eng = DFlashEngine(w.shape, B, nb, P + B * steps_total + 64, max_rows=max(P, nb * B), seed=w.seed)
+    used = P + B * steps_total + 64  # cache slots a sequence reaches in this sweep
+    s_ = w.shape
+    page_bytes = (s_.n_layers + s_.n_draft_layers) * 2 * s_.n_kv_heads * capi.PAGE_SLOTS * s_.head_dim * 2
+    if args.kv_pages:
+        # serving configuration: slots admit requests of up to 32K tokens, and
+        # pages come from one pool sized for what the sequences use
+        max_ctx = max(32768, used)
+        pages = nb * -(-used // capi.PAGE_SLOTS)
+    else:
+        max_ctx, pages = used, 0
+    eng = DFlashEngine(w.shape, B, nb, max_ctx, max_rows=max(P, nb * B), seed=w.seed, kv_pages=pages)
+    if args.kv_pages:
+        for q in range(nb):  # the graph replays below map nothing
+            eng.reserve(q, used)
+    kv = {"mode": "paged" if args.kv_pages else "fixed regions", "max_ctx": max_ctx,
+          "pages": pages if args.kv_pages else nb * -(-max_ctx // capi.PAGE_SLOTS),
+          "bytes": (pages if args.kv_pages else nb * -(-max_ctx // capi.PAGE_SLOTS)) * page_bytes,
+          "fixed_regions_bytes_at_max_ctx": nb * -(-max_ctx // capi.PAGE_SLOTS) * page_bytes}
     eng.prefill(prompts)
     stream = torch.cuda.current_stream()
     sampler = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
@@ -803,7 +836,7 @@ def run_concurrency(args) -> None:
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded random-init weights, uniform random prompt tokens)",
         "config": {"workload": "concurrency", "batches": list(batches), "block": B, "prompt_len": P,
-                   "expected_accept_len": PAGES_ACCEPT_LEN,
+                   "expected_accept_len": PAGES_ACCEPT_LEN, "kv_cache": kv,
                    "l2": "no flush: every step streams ~19 GB of weights"},
         "points": points, "clocks": clocks}))
 
@@ -823,6 +856,10 @@ def main() -> None:
     ap.add_argument("--ar-steps", type=int, default=50)
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--attn-point", default="",
+                    help="attn_op workload: only the point CTXxBATCH (e.g. 8192x8)")
+    ap.add_argument("--kv-pages", action="store_true",
+                    help="concurrency workload: paged KV cache (32K-slot sequences, shared page pool)")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the attention-op grid, batch-32 and DDTree measurements that the "
                          "default single-GPU run adds to its line")

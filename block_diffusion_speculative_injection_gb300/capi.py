@@ -40,7 +40,11 @@ class Config(ctypes.Structure):
         ("block_size", ctypes.c_int32), ("max_batch", ctypes.c_int32),
         ("max_ctx", ctypes.c_int32), ("max_rows", ctypes.c_int32),
         ("max_tree_nodes", ctypes.c_int32), ("dtype", ctypes.c_int32),
+        ("kv_pages", ctypes.c_int32),
     ]
+
+
+PAGE_SLOTS = 128  # DFLASH_PAGE_SLOTS: cache slots per KV page
 
 
 class DTree(ctypes.Structure):
@@ -57,6 +61,15 @@ _SIGS = {
     "dflash_create": ([ctypes.POINTER(Config), ctypes.POINTER(_P)], _I),
     "dflash_set_weight": ([_P, ctypes.c_char_p, _P, _I, ctypes.POINTER(ctypes.c_int64), _I], _I),
     "dflash_reset_seq": ([_P, _I, _P], _I),
+    "dflash_kv_reserve": ([_P, _I, _I, _P], _I),
+    "dflash_kv_release": ([_P, _I, _P], _I),
+    "dflash_kv_free_pages": ([_P], _I),
+    "dflash_kv_pool_create": ([_I, _I, _I], _P),
+    "dflash_kv_pool_destroy": ([_P], None),
+    "dflash_kv_pool_reserve": ([_P, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)], _I),
+    "dflash_kv_pool_release": ([_P, _I], _I),
+    "dflash_kv_pool_pages": ([_P, _I, _P, _I], _I),
+    "dflash_kv_pool_free": ([_P], _I),
     "dflash_verify": ([_P, _I, _P, _P, _I, _P, _I, _P, _P, _P, _P], _I),
     "dflash_draft_block": ([_P, _I, _P, _P, _P, _I, _P, _P, _P, _P], _I),
     "dflash_set_block_size": ([_P, _I], _I),
@@ -85,6 +98,7 @@ _SIGS = {
     "dflash_debug_trace": ([_P, _P, ctypes.c_int64], _I),
     "dflash_debug_trace_draft": ([_P, _P, ctypes.c_int64], _I),
     "dflash_debug_trace_draft_attn": ([_P, _P, _P, ctypes.c_int64], _I),
+    "dflash_profile_list": ([_P, _I, _P, _P, ctypes.c_int64], ctypes.c_int64),
     "dflash_profile_read": ([_P, _I, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double),
                              ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)], _I),
 }
@@ -164,6 +178,60 @@ def dflash_set_weight(ctx: int, name: str, tensor, dtype: int) -> None:
 
 def dflash_reset_seq(ctx: int, seq_id: int, stream=None) -> None:
     _check(ctx, load().dflash_reset_seq(ctx, seq_id, _stream(stream)))
+
+
+def dflash_kv_reserve(ctx, seq_id: int, n_slots: int, stream=None) -> None:
+    _check(ctx, load().dflash_kv_reserve(ctx, seq_id, n_slots, _stream(stream)))
+
+
+def dflash_kv_release(ctx, seq_id: int, stream=None) -> None:
+    _check(ctx, load().dflash_kv_release(ctx, seq_id, _stream(stream)))
+
+
+def dflash_kv_free_pages(ctx) -> int:
+    return load().dflash_kv_free_pages(ctx)
+
+
+class KvPool:
+    """The host page allocator (dflash_kv_pool_*), no GPU needed."""
+
+    def __init__(self, n_pages: int, max_seqs: int, max_pages: int):
+        self.h = load().dflash_kv_pool_create(n_pages, max_seqs, max_pages)
+        if not self.h:
+            raise DFlashError(1, "dflash_kv_pool_create")
+
+    def reserve(self, seq: int, n_slots: int):
+        """(first new table index, pages added); raises DFlashError when refused."""
+        f, n = _I(), _I()
+        st = load().dflash_kv_pool_reserve(self.h, seq, n_slots, ctypes.byref(f), ctypes.byref(n))
+        if st != 0:
+            raise DFlashError(st, "dflash_kv_pool_reserve")
+        return f.value, n.value
+
+    def release(self, seq: int) -> int:
+        return load().dflash_kv_pool_release(self.h, seq)
+
+    def pages(self, seq: int) -> list:
+        n = load().dflash_kv_pool_pages(self.h, seq, None, 0)
+        if n < 0:
+            raise DFlashError(1, "dflash_kv_pool_pages")
+        buf = (_I * max(n, 1))()
+        load().dflash_kv_pool_pages(self.h, seq, ctypes.addressof(buf), n)
+        return list(buf)[:n]
+
+    def free(self) -> int:
+        return load().dflash_kv_pool_free(self.h)
+
+    def close(self) -> None:
+        if self.h:
+            load().dflash_kv_pool_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def dflash_verify(ctx, batch, seq_ids, tokens, q, q_lens, flags, argmax, margin=None, logits=None,
@@ -271,6 +339,17 @@ def dflash_profile(ctx, enable: bool) -> None:
 
 
 PROF_GEMM, PROF_ATTN, PROF_ROW, PROF_VOCAB, PROF_SPEC, PROF_ALL = 0, 1, 2, 3, 4, -1
+
+
+def dflash_profile_list(ctx, kind: int):
+    """Per-launch (ms, flops) of the recorded launches of one class."""
+    n = load().dflash_profile_list(ctx, kind, None, None, 0)
+    if n < 0:
+        raise DFlashError(4, "dflash_profile_list")
+    ms = (ctypes.c_double * max(n, 1))()
+    fl = (ctypes.c_double * max(n, 1))()
+    load().dflash_profile_list(ctx, kind, ctypes.addressof(ms), ctypes.addressof(fl), n)
+    return list(zip(list(ms)[:n], list(fl)[:n]))
 
 
 def dflash_profile_read(ctx, kind: int):

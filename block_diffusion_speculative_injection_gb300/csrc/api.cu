@@ -73,6 +73,7 @@ static dflash_status validate_config(const dflash_config* c, std::string* why) {
       c->max_rows < c->max_batch * c->max_tree_nodes)
     return bad("max_rows must cover max_batch * max(block_size, max_tree_nodes)");
   if (!(c->rms_eps > 0.f) || !(c->rope_theta > 0.f)) return bad("rms_eps and rope_theta must be > 0");
+  if (c->kv_pages < 0) return bad("kv_pages must be >= 0");
   if (c->d_model > 8192) return bad("d_model must be <= 8192");
   if (c->dtype == DFLASH_F32) {
     if (c->head_dim % 32) return bad("fp32 path needs head_dim a multiple of 32");
@@ -164,9 +165,6 @@ static dflash_status resolve_weights(dflash_ctx* ctx) {
   return DFLASH_OK;
 }
 
-static size_t cache_bytes_per_layer(const dflash_config& c, int esize) {
-  return (size_t)c.max_batch * c.n_kv_heads * c.max_ctx * c.head_dim * esize;
-}
 
 // ---------------------------------------------------------------------------
 // one transformer layer (target or draft) over the rows of the current pass
@@ -187,6 +185,7 @@ static EpiArgs epi_base(dflash_ctx* ctx, int kind) {
   e.max_ctx = c.max_ctx;
   e.max_batch = c.max_batch;
   e.layer_elems = ctx->layer_cache_elems;
+  e.kp = ctx_pages(ctx);
   e.F = c.ffn_dim;
   e.n_inject = c.n_inject;
   e.resid = ctx->resid;
@@ -296,7 +295,7 @@ static dflash_status target_pass(dflash_ctx* ctx, int batch, int q, int mask,
   ab.mask = mask;
   ab.anc = anc;
   ab.anc_words = anc_words;
-  ab.max_keys_ub = c.max_ctx;
+  ab.max_keys_ub = pages_key_bound(ctx);
   DF_TRY(launch_norm(ctx, rows, nullptr, ctx->tl[0].attn_norm, ctx->xn, st));
   int inj = 0;
   for (int l = 0; l < c.n_target_layers; ++l) {
@@ -367,7 +366,11 @@ dflash_status dflash_create(const dflash_config* cfg, dflash_ctx** out) {
   const size_t es = ctx->esize;
   const size_t R = c.max_rows, d = c.d_model, F = c.ffn_dim;
   const size_t qd = (size_t)c.n_heads * c.head_dim;
-  ctx->layer_cache_elems = (size_t)c.max_batch * c.n_kv_heads * c.max_ctx * c.head_dim;
+  if (pages_init(ctx) != DFLASH_OK) {
+    delete ctx;
+    return DFLASH_E_INVALID_ARG;
+  }
+  ctx->layer_cache_elems = (size_t)ctx->n_pages * c.n_kv_heads * kPageSlots * c.head_dim;
   // GEMM workspace: the widest non-lm_head GEMM over max_rows rows, or the
   // lm_head over the rows of one decode pass, whichever is larger
   size_t wsn = R * std::max<size_t>({(size_t)target_layer_qkv_rows(c), 2 * F, d,
@@ -390,7 +393,7 @@ dflash_status dflash_create(const dflash_config* cfg, dflash_ctx** out) {
     if (!ok) return;
     if (cudaMalloc(p, bytes ? bytes : 16) != cudaSuccess) ok = false;
   };
-  const size_t cache_layer_bytes = cache_bytes_per_layer(c, ctx->esize);
+  const size_t cache_layer_bytes = ctx->layer_cache_elems * ctx->esize;
   alloc((void**)&ctx->seq_len, sizeof(int32_t) * c.max_batch);
   alloc((void**)&ctx->gen_count, sizeof(int32_t) * c.max_batch);
   alloc((void**)&ctx->dev_status, sizeof(int32_t) * 4);
@@ -419,6 +422,7 @@ dflash_status dflash_create(const dflash_config* cfg, dflash_ctx** out) {
   alloc((void**)&ctx->inj_seq, sizeof(int32_t) * R);
   alloc((void**)&ctx->inj_pos, sizeof(int32_t) * R);
   alloc((void**)&ctx->path, sizeof(int32_t) * c.max_batch * 34);
+  alloc((void**)&ctx->page_tab, sizeof(int32_t) * c.max_batch * ctx->pps);
   alloc((void**)&ctx->rope_cos, sizeof(float) * ctx->rope_len * (c.head_dim / 2));
   alloc((void**)&ctx->rope_sin, sizeof(float) * ctx->rope_len * (c.head_dim / 2));
   DraftMeta dm{nullptr, nullptr, nullptr};
@@ -433,7 +437,8 @@ dflash_status dflash_create(const dflash_config* cfg, dflash_ctx** out) {
   ctx->pass_ctx = ctx->pass_seq + c.max_batch;
   ctx->pass_blk = ctx->pass_seq + 2 * c.max_batch;
   // caches start at zero so that stale slots always hold finite values
-  bool mok = cudaMemset(ctx->kc, 0, cache_layer_bytes * c.n_target_layers) == cudaSuccess &&
+  bool mok = pages_fill_table(ctx) == DFLASH_OK &&
+             cudaMemset(ctx->kc, 0, cache_layer_bytes * c.n_target_layers) == cudaSuccess &&
              cudaMemset(ctx->vc, 0, cache_layer_bytes * c.n_target_layers) == cudaSuccess &&
              cudaMemset(ctx->dkc, 0, cache_layer_bytes * c.n_draft_layers) == cudaSuccess &&
              cudaMemset(ctx->dvc, 0, cache_layer_bytes * c.n_draft_layers) == cudaSuccess &&
@@ -471,9 +476,10 @@ void dflash_destroy(dflash_ctx* ctx) {
                   ctx->ao,      ctx->act,        ctx->fb,      ctx->lm_in,   ctx->ws,
                   ctx->part_o,  ctx->part_ml,    ctx->vk_part, ctx->vv_part, ctx->pass_seq,
                   ctx->row_pos, ctx->row_slot,   ctx->row_seq, ctx->lm_rows, ctx->inj_seq,
-                  ctx->inj_pos, ctx->path,       ctx->rope_cos, ctx->rope_sin};
+                  ctx->inj_pos, ctx->path,       ctx->rope_cos, ctx->rope_sin, ctx->page_tab};
   for (void* p : ptrs)
     if (p) cudaFree(p);
+  pages_destroy(ctx);
   for (cudaEvent_t e : ctx->prof_ev) cudaEventDestroy(e);
   auto it = g_draft_meta.find(ctx);
   if (it != g_draft_meta.end()) {
@@ -586,7 +592,7 @@ dflash_status dflash_draft_block(dflash_ctx* ctx, int32_t batch, const int32_t* 
   ab.batch = batch;
   ab.q_stride = B;
   ab.mask = kMaskNone;
-  ab.max_keys_ub = c.max_ctx;
+  ab.max_keys_ub = pages_key_bound(ctx);
   // the attention kernels read per-sequence metadata from the pass arrays;
   // point them at the draft's copy for the duration of this pass
   int32_t* save[3] = {ctx->pass_seq, ctx->pass_ctx, ctx->pass_blk};
@@ -761,7 +767,8 @@ dflash_status dflash_check(dflash_ctx* ctx) {
   cudaMemset(ctx->dev_status, 0, sizeof(int32_t));
   switch (s) {
     case kDevOk: return DFLASH_OK;
-    case kDevCapacity: return fail(ctx, DFLASH_E_CAPACITY, "device: sequence exceeded max_ctx");
+    case kDevCapacity:
+      return fail(ctx, DFLASH_E_CAPACITY, "device: sequence exceeded max_ctx or its mapped KV pages");
     case kDevTimeout: return fail(ctx, DFLASH_E_TIMEOUT, "device: bounded wait expired");
     default: return fail(ctx, DFLASH_E_DEVICE_CHECK, "device: argument check failed");
   }
@@ -860,6 +867,27 @@ dflash_status dflash_profile_read(dflash_ctx* ctx, int32_t kind, int64_t* launch
   return DFLASH_OK;
 }
 
+int64_t dflash_profile_list(dflash_ctx* ctx, int32_t kind, double* ms, double* flops,
+                            int64_t max_out) {
+  if (!ctx || max_out < 0) return -1;
+  if (!ctx->prof_recs.empty() &&
+      cudaEventSynchronize(ctx->prof_ev[ctx->prof_recs.back().ev + 1]) != cudaSuccess)
+    return -1;
+  int64_t n = 0;
+  for (const ProfRec& r : ctx->prof_recs) {
+    if (kind >= 0 && r.kind != kind) continue;
+    if (n < max_out) {
+      float t = 0.f;
+      if (cudaEventElapsedTime(&t, ctx->prof_ev[r.ev], ctx->prof_ev[r.ev + 1]) != cudaSuccess)
+        return -1;
+      if (ms) ms[n] = t;
+      if (flops) flops[n] = r.flops;
+    }
+    ++n;
+  }
+  return n;
+}
+
 const char* dflash_last_error(const dflash_ctx* ctx) {
   return ctx ? ctx->last_error.c_str() : "null context";
 }
@@ -884,6 +912,11 @@ dflash_status dflash_debug_view(const dflash_ctx* ctx, const char* name, int32_t
     if (layer < 0 || layer >= c.n_draft_layers) return DFLASH_E_INVALID_ARG;
     *dev_ptr = static_cast<const uint8_t*>(n[1] == 'k' ? ctx->dkc : ctx->dvc) + layer * lb;
     *bytes = (int64_t)lb;
+    return DFLASH_OK;
+  }
+  if (n == "page_table") {
+    *dev_ptr = ctx->page_tab;
+    *bytes = (int64_t)c.max_batch * ctx->pps * sizeof(int32_t);
     return DFLASH_OK;
   }
   if (n == "gen_count") {

@@ -32,7 +32,8 @@ struct AttnK {
   const int32_t* pass_seq;
   const int32_t* pass_ctx;
   const int32_t* pass_blk;
-  int q_stride, H, Hkv, G, hd, max_ctx;
+  int q_stride, H, Hkv, G, hd;
+  KvPages kp;  // cache slot -> row of the K/V tensors
   int mask;
   const uint64_t* anc;
   int anc_words;
@@ -150,12 +151,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int key_end = (p.mask == kMaskCausal) ? ctx_len + jmax : ctx_len + blk;
   // causal and draft passes: this sequence's keys in equal whole-tile shares
   // over the splits (the launch is sized for the longest context); tree
-  // verify keeps the plan's fixed share
-  const int kps =
-      p.mask == kMaskTree
-          ? p.keys_per_split
-          : min(p.keys_per_split,
-                max(kTK, (key_end + p.n_splits * kTK - 1) / (p.n_splits * kTK) * kTK));
+  // verify keeps the plan's fixed share unless its keys need more (the plan
+  // is sized from a host bound on the length; the splits always cover every
+  // key, whatever that bound was when a graph of this launch was captured)
+  const int share = max(kTK, (key_end + p.n_splits * kTK - 1) / (p.n_splits * kTK) * kTK);
+  const int kps = p.mask == kMaskTree ? max(p.keys_per_split, share) : share;
   const int k_begin = split * kps;
   const int k_stop = min(key_end, k_begin + kps);
 
@@ -228,30 +228,53 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const int qz = b * p.q_stride + j0;
       tma_load_3d(qs, &maps.q, 0, kvh * G, qz, q_full);
       tma_load_3d(qs + kQBox, &maps.q, 64, kvh * G, qz, q_full);
-      const int row0 = (seq * p.Hkv + kvh) * p.max_ctx + k_begin;
+      // a tile is one page (k_begin and the tile stride are multiples of the
+      // page size); pass setup has checked that every page is mapped
+      static_assert(kTK == kPageSlots, "one key tile per KV page");
       int k_issued = 0, v_issued = 0;
-      auto load = [&](int t, bool is_v) -> bool {
+      // page of tile t (a raw table read, consumed only when the tile is
+      // loaded), and the tile's first row in the K/V tensors; an unmapped
+      // page, which pass setup rules out, loads page 0 and flags the pass
+      auto tile_page = [&](int t) -> int {
+        return p.kp.tab ? p.kp.tab[seq * p.kp.pps + (k_begin + t * kTK) / kPageSlots] : 0;
+      };
+      auto load = [&](int t, bool is_v, int pg) -> bool {
+        long long row;
+        if (!p.kp.tab) {
+          row = kv_row(p.kp, p.Hkv, seq, kvh, k_begin + t * kTK);
+        } else if (pg < 0 || pg >= p.kp.n_pages) {
+          set_dev_status(status, kDevCapacity);
+          row = 0;
+        } else {
+          row = ((long long)pg * p.Hkv + kvh) * kPageSlots;
+        }
+        const int y = (int)row;
         const int st = t & 1;
         uint64_t* empty = is_v ? &v_empty[st] : &k_empty[st];
         uint64_t* full = is_v ? &v_full[st] : &k_full[st];
         if (t >= 2 && !mbar_wait(empty, ((t >> 1) - 1) & 1, status)) return false;
         uint8_t* dst = kvs + st * 2 * kKBytes + (is_v ? kKBytes : 0);
         const CUtensorMap* map = is_v ? &maps.v : &maps.k;
-        const int y = row0 + t * kTK;
         mbar_arrive_expect_tx(full, kKBytes);
         tma_load_2d(dst, map, 0, y, full);
         tma_load_2d(dst + kKBox, map, 64, y, full);
         return true;
       };
+      // pages are read one tile ahead, so that the table read's latency
+      // hides behind the wait for a free ring stage
+      int pg_k = tile_page(0), pg_v = 0;
       for (int t = 0; t <= n_tiles; ++t) {
+        const int pg_next = t + 1 < n_tiles ? tile_page(t + 1) : 0;
         if (t < n_tiles) {
-          if (!load(t, false)) break;
+          if (!load(t, false, pg_k)) break;
           k_issued = t + 1;
         }
         if (t >= 1) {
-          if (!load(t - 1, true)) break;
+          if (!load(t - 1, true, pg_v)) break;
           v_issued = t;
         }
+        pg_v = pg_k;
+        pg_k = pg_next;
       }
       // every issued copy has landed before this thread leaves
       mbar_wait(q_full, 0, status);
@@ -614,25 +637,30 @@ __global__ void attn_simt_f32_kernel(const AttnK p) {
   const float* qv = static_cast<const float*>(p.q) + ((size_t)row * p.H + h) * p.hd;
   float qr[4], acc[4] = {0.f, 0.f, 0.f, 0.f};
   for (int i = 0; i < per; ++i) qr[i] = qv[lane + 32 * i];
-  const size_t head_base = ((size_t)seq * p.Hkv + kvh) * (size_t)p.max_ctx;
-  const float* kg = static_cast<const float*>(p.kc) + head_base * p.hd;
-  const float* vg = static_cast<const float*>(p.vc) + head_base * p.hd;
+  const float* const kc = static_cast<const float*>(p.kc);
+  const float* const vc = static_cast<const float*>(p.vc);
   const uint64_t* anc = p.mask == kMaskTree ? p.anc + (size_t)row * p.anc_words : nullptr;
   const int key_end = (p.mask == kMaskCausal) ? ctx_len + j + 1 : ctx_len + blk;
   const float scale = p.scale_log2;  // log2 domain
   float m = -INFINITY, l = 0.f;
   for (int k = 0; k < key_end; ++k) {
     if (!key_visible(p.mask, k, ctx_len, blk, j, anc)) continue;
+    const long long kr = kv_row(p.kp, p.Hkv, seq, kvh, k);
+    if (kr < 0) {
+      if (lane == 0) set_dev_status(p.status, kDevCapacity);
+      continue;
+    }
+    const float* kg = kc + (size_t)kr * p.hd;
+    const float* vg = vc + (size_t)kr * p.hd;
     float dot = 0.f;
-    for (int i = 0; i < per; ++i) dot += qr[i] * kg[(size_t)k * p.hd + lane + 32 * i];
+    for (int i = 0; i < per; ++i) dot += qr[i] * kg[lane + 32 * i];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
     const float sc = dot * scale;
     const float mn = fmaxf(m, sc);
     const float corr = exp2f(m - mn), pk = exp2f(sc - mn);
     l = l * corr + pk;
-    for (int i = 0; i < per; ++i)
-      acc[i] = acc[i] * corr + pk * vg[(size_t)k * p.hd + lane + 32 * i];
+    for (int i = 0; i < per; ++i) acc[i] = acc[i] * corr + pk * vg[lane + 32 * i];
     m = mn;
   }
   float* og = static_cast<float*>(p.out) + ((size_t)row * p.H + h) * p.hd;
@@ -740,7 +768,8 @@ dflash_status attention(dflash_ctx* ctx, const AttnArgs& a, cudaStream_t st) {
   p.Hkv = c.n_kv_heads;
   p.G = c.n_heads / c.n_kv_heads;
   p.hd = c.head_dim;
-  p.max_ctx = c.max_ctx;
+  p.kp = ctx_pages(ctx);
+  p.status = ctx->dev_status;
   p.mask = a.mask;
   p.anc = a.anc;
   p.anc_words = a.anc_words;
@@ -762,11 +791,10 @@ dflash_status attention(dflash_ctx* ctx, const AttnArgs& a, cudaStream_t st) {
     set_error(ctx, "bf16 attention needs head_dim 128 and a GQA group dividing 64");
     return DFLASH_E_UNSUPPORTED;
   }
-  p.status = ctx->dev_status;
   AttnMaps maps;
-  const int64_t kv_rows = (int64_t)c.max_batch * c.n_kv_heads * c.max_ctx;
+  const int64_t kv_rows = (int64_t)ctx->n_pages * c.n_kv_heads * kPageSlots;
   if (kv_rows >= (int64_t)1 << 31) {
-    set_error(ctx, "bf16 attention needs max_batch * n_kv_heads * max_ctx < 2^31");
+    set_error(ctx, "bf16 attention needs pages * n_kv_heads * %d < 2^31", kPageSlots);
     return DFLASH_E_UNSUPPORTED;
   }
   {
@@ -852,7 +880,7 @@ dflash_status block_attention(int batch, int H, int Hkv, int hd, int ctx_len, in
   p.Hkv = Hkv;
   p.G = H / Hkv;
   p.hd = hd;
-  p.max_ctx = ctx_len + block;
+  p.kp = KvPages{nullptr, 0, 0, ctx_len + block};
   p.mask = causal ? kMaskCausal : kMaskNone;
   p.rows_total = batch * block;
   p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)hd));
@@ -865,7 +893,7 @@ dflash_status block_attention(int batch, int H, int Hkv, int hd, int ctx_len, in
   const size_t per_split = (size_t)p.rows_total * H * (kHd + 2) * sizeof(float);
   const size_t cap_units = workspace ? (size_t)workspace_bytes / per_split * p.rows_total * H : 0;
   int splits = 1;
-  plan_splits(device_sms(), ctas, p.max_ctx, cap_units, p.rows_total * H, &splits,
+  plan_splits(device_sms(), ctas, (int64_t)ctx_len + block, cap_units, p.rows_total * H, &splits,
               &p.keys_per_split);
   if (splits > 1) {
     p.part_o = static_cast<float*>(workspace);

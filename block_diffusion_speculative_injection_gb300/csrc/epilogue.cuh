@@ -35,6 +35,7 @@ struct EpiArgs {
   void* kc;  // QKV: this layer's cache base; INJECT: draft cache base (all layers)
   void* vc;
   int H, Hkv, hd, max_ctx, max_batch;
+  KvPages kp;  // cache slot -> page row
   size_t layer_elems;
   int layer0;
   // SWIGLU
@@ -100,10 +101,17 @@ __device__ void epi_rotate_head(const EpiArgs& e, int n0, int m0, int m1, T* dst
       seq = e.row_seq[t];
       slot = e.row_slot[t];
     }
+    long long row = (long long)t * e.H + head;
+    if (!is_q) {
+      row = kv_row(e.kp, e.Hkv, seq, head, slot);
+      if (row < 0) {
+        set_dev_status(e.status, kDevCapacity);
+        continue;
+      }
+    }
     const float lo = slab_sum<T>(e, t, n0 + i), hi = slab_sum<T>(e, t, n0 + i + half);
     const float c = e.rcos[(size_t)pos * half + i], s = e.rsin[(size_t)pos * half + i];
-    T* dst = is_q ? dst_base + ((size_t)t * e.H + head) * e.hd
-                  : dst_base + (((size_t)seq * e.Hkv + head) * e.max_ctx + slot) * e.hd;
+    T* dst = dst_base + (size_t)row * e.hd;
     st_f(dst + i, lo * c - hi * s);
     st_f(dst + i + half, hi * c + lo * s);
   }
@@ -123,8 +131,12 @@ __device__ void epi_copy_head(const EpiArgs& e, int n0, int m0, int m1, T* dst_b
       seq = e.row_seq[t];
       slot = e.row_slot[t];
     }
-    st_f(dst_base + (((size_t)seq * e.Hkv + head) * e.max_ctx + slot) * e.hd + c,
-         slab_sum<T>(e, t, n0 + c));
+    const long long row = kv_row(e.kp, e.Hkv, seq, head, slot);
+    if (row < 0) {
+      set_dev_status(e.status, kDevCapacity);
+      continue;
+    }
+    st_f(dst_base + (size_t)row * e.hd + c, slab_sum<T>(e, t, n0 + c));
   }
 }
 
@@ -326,9 +338,13 @@ __device__ void run_epilogue_direct(const EpiArgs& e, uint32_t tmem, int n0, int
               set_dev_status(e.status, kDevCheck);
             } else {
               const int slot = inject ? pos : e.row_slot[t];
-              dst = is_q ? ((long long)t * H + head) * 128
-                         : (((long long)seq * Hkv + head) * max_ctx + slot) * 128;
-              if (pos < max_ctx) rope = pos * 64;  // the tables hold max_ctx positions
+              const long long row = is_q ? (long long)t * H + head : kv_row(e.kp, Hkv, seq, head, slot);
+              if (row < 0) {
+                set_dev_status(e.status, kDevCapacity);
+              } else {
+                dst = row * 128;
+                if (pos < max_ctx) rope = pos * 64;  // the tables hold max_ctx positions
+              }
             }
           }
         }
@@ -464,8 +480,12 @@ __device__ void run_epilogue_cluster(const EpiArgs& e, int n0, int m0, int BN, c
           set_dev_status(e.status, kDevCheck);
           continue;
         }
-        T* dst = is_q ? base + ((size_t)t * e.H + head) * 128
-                      : base + (((size_t)seq * e.Hkv + head) * e.max_ctx + slot) * 128;
+        const long long row = is_q ? (long long)t * e.H + head : kv_row(e.kp, e.Hkv, seq, head, slot);
+        if (row < 0) {
+          set_dev_status(e.status, kDevCapacity);
+          continue;
+        }
+        T* dst = base + (size_t)row * 128;
         if (is_v) {
           st_f(dst + c, val(u, c));
         } else {

@@ -46,6 +46,36 @@ struct WeightRef {
 
 enum PassKind { kPassNone = 0, kPassLinear = 1, kPassTree = 2, kPassDraft = 3 };
 
+// ---------------------------------------------------------------------------
+// KV cache addressing.  A layer's cache is a pool of pages
+// [page][n_kv][kPageSlots][hd]; slot s of sequence q is row s % kPageSlots of
+// page tab[q * pps + s / kPageSlots].  With tab == nullptr the cache is one
+// contiguous region per sequence, [seq][n_kv][ctx_cap][hd] (the op-level
+// attention over caller tensors).
+// ---------------------------------------------------------------------------
+constexpr int kPageSlots = DFLASH_PAGE_SLOTS;
+static_assert((kPageSlots & (kPageSlots - 1)) == 0, "page slots: a power of two");
+
+struct KvPages {
+  const int32_t* tab;  // [max_batch][pps] page ids, -1 unmapped (nullptr: contiguous)
+  int pps;             // table entries per sequence
+  int n_pages;         // pool size (bounds of a page id)
+  int ctx_cap;         // contiguous layout: slots per (sequence, head)
+};
+
+// Row (in units of head_dim elements) of cache slot `slot` of sequence `seq`,
+// KV head `head`, within one layer; -1 when its page is not mapped.
+__device__ __forceinline__ long long kv_row(const KvPages& kp, int Hkv, int seq, int head,
+                                            int slot) {
+  if (!kp.tab) return ((long long)seq * Hkv + head) * kp.ctx_cap + slot;
+  const int pg = kp.tab[seq * kp.pps + slot / kPageSlots];
+  if (pg < 0 || pg >= kp.n_pages) return -1;
+  return ((long long)pg * Hkv + head) * kPageSlots + (slot & (kPageSlots - 1));
+}
+
+// host-side page allocator (csrc/pages.cu)
+struct PagePool;
+
 struct LayerW {
   const void *attn_norm, *wq, *wk, *wv, *wo, *ffn_norm, *w_gate, *w_up, *w_down;
 };
@@ -78,12 +108,15 @@ struct dflash_ctx {
   // per-sequence state
   int32_t* seq_len = nullptr;        // [max_batch] committed length
   int32_t* gen_count = nullptr;      // [max_batch] tokens emitted since reset
-  std::vector<int64_t> host_len_ub;  // host upper bound of each slot's length
   int32_t* dev_status = nullptr;     // [1]
 
-  // caches: [layers][max_batch][n_kv][max_ctx][hd]
+  // caches: [layers][pages][n_kv][kPageSlots][hd], one page table for all
   void *kc = nullptr, *vc = nullptr, *dkc = nullptr, *dvc = nullptr;
   size_t layer_cache_elems = 0;
+  int32_t* page_tab = nullptr;     // [max_batch][pps]
+  int pps = 0, n_pages = 0;        // table entries per sequence, pool pages
+  bool paged = false;              // kv_pages > 0: pages come from the pool on demand
+  dflash::PagePool* pool = nullptr;
 
   // activations (rows = max_rows)
   void* capture = nullptr;  // [max_rows][n_inject][d]
@@ -148,6 +181,17 @@ struct GemmSegs {
   int rows[12];
   int n;
 };
+
+// paged KV cache (csrc/pages.cu): sizes from the config, the initial table,
+// teardown of the host allocator
+dflash_status pages_init(dflash_ctx* ctx);
+dflash_status pages_fill_table(dflash_ctx* ctx);
+void pages_destroy(dflash_ctx* ctx);
+int64_t pages_key_bound(const dflash_ctx* ctx);
+
+inline KvPages ctx_pages(const dflash_ctx* ctx) {
+  return KvPages{ctx->page_tab, ctx->pps, ctx->n_pages, 0};
+}
 
 struct EpiArgs;
 // X[M][K] . W^T with W the vertical stack of the segments, then the fused

@@ -23,6 +23,7 @@ struct PassSetupArgs {
   int32_t *row_pos, *row_slot, *row_seq;
   int32_t *lm_in, *lm_arg, *lm_vec;
   int batch, q, kind, last_only, max_batch, max_ctx;
+  KvPages kp;  // every slot a pass touches must sit in a mapped page
   int32_t* status;
 };
 
@@ -48,6 +49,15 @@ __global__ void pass_setup_kernel(PassSetupArgs a) {
       if (ctx + blk > a.max_ctx) {
         set_dev_status(a.status, kDevCapacity);
         blk = 0;
+      }
+      // the pass reads slots 0 .. ctx + blk - 1 (keys) and writes ctx ..
+      // ctx + blk - 1: all of their pages must be mapped
+      for (int pg = 0; blk > 0 && pg * kPageSlots < ctx + blk; ++pg) {
+        const int id = a.kp.tab[seq * a.kp.pps + pg];
+        if (id < 0 || id >= a.kp.n_pages) {
+          set_dev_status(a.status, kDevCapacity);
+          blk = 0;
+        }
       }
     }
     a.pass_seq[b] = seq < 0 || seq >= a.max_batch ? 0 : seq;
@@ -129,6 +139,7 @@ dflash_status launch_pass_setup_full(dflash_ctx* ctx, int batch, const int32_t* 
   a.last_only = last_only;
   a.max_batch = ctx->cfg.max_batch;
   a.max_ctx = ctx->cfg.max_ctx;
+  a.kp = ctx_pages(ctx);
   a.status = ctx->dev_status;
   DF_CUDA_TRY(ctx, launch_k(ctx->pdl, pass_setup_kernel, dim3(1), dim3(1024), 0, st, a));
   DF_LAUNCHED(ctx);

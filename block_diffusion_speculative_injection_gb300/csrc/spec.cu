@@ -296,7 +296,8 @@ template <typename T>
 __global__ void tree_compact_kernel(const int32_t* __restrict__ path,
                                     const int32_t* __restrict__ pass_seq,
                                     const int32_t* __restrict__ pass_blk, T* kc, T* vc,
-                                    size_t layer_elems, int batch, int Hkv, int hd, int max_ctx) {
+                                    size_t layer_elems, int batch, int Hkv, int hd,
+                                    const KvPages kp, int32_t* status) {
   pdl_wait();
   pdl_trigger();
   extern __shared__ uint8_t buf[];
@@ -308,17 +309,26 @@ __global__ void tree_compact_kernel(const int32_t* __restrict__ path,
   if (a <= 0) return;
   T* ks = reinterpret_cast<T*>(buf);
   T* vs = ks + (size_t)a * hd;
-  const size_t head = (size_t)l * layer_elems + ((size_t)seq * Hkv + kh) * max_ctx * hd;
+  const size_t layer = (size_t)l * layer_elems;
+  // the pages of every slot of the pass were checked at pass setup; an
+  // unmapped one is flagged and its row skipped
   for (int i = threadIdx.x; i < a * hd; i += blockDim.x) {
     const int r = i / hd + 1, e = i % hd;
-    const size_t src = head + (size_t)(ctx + pb[2 + r]) * hd + e;
+    const long long row = kv_row(kp, Hkv, seq, kh, ctx + pb[2 + r]);
+    if (row < 0) {
+      set_dev_status(status, kDevCapacity);
+      continue;
+    }
+    const size_t src = layer + (size_t)row * hd + e;
     ks[i] = kc[src];
     vs[i] = vc[src];
   }
   __syncthreads();
   for (int i = threadIdx.x; i < a * hd; i += blockDim.x) {
     const int r = i / hd + 1, e = i % hd;
-    const size_t dst = head + (size_t)(ctx + r) * hd + e;
+    const long long row = kv_row(kp, Hkv, seq, kh, ctx + r);
+    if (row < 0) continue;
+    const size_t dst = layer + (size_t)row * hd + e;
     kc[dst] = ks[i];
     vc[dst] = vs[i];
   }
@@ -342,12 +352,12 @@ dflash_status launch_tree_accept(dflash_ctx* ctx, int batch, const int32_t* seq_
     DF_CUDA_TRY(ctx, launch_k(ctx->pdl, tree_compact_kernel<bf16>, dim3(grid), dim3(128), smem, st, 
         ctx->path, ctx->pass_seq, ctx->pass_blk, static_cast<bf16*>(ctx->kc),
         static_cast<bf16*>(ctx->vc), ctx->layer_cache_elems, batch, c.n_kv_heads, c.head_dim,
-        c.max_ctx));
+        ctx_pages(ctx), ctx->dev_status));
   else
     DF_CUDA_TRY(ctx, launch_k(ctx->pdl, tree_compact_kernel<float>, dim3(grid), dim3(128), smem, st, 
         ctx->path, ctx->pass_seq, ctx->pass_blk, static_cast<float*>(ctx->kc),
         static_cast<float*>(ctx->vc), ctx->layer_cache_elems, batch, c.n_kv_heads, c.head_dim,
-        c.max_ctx));
+        ctx_pages(ctx), ctx->dev_status));
   DF_LAUNCHED(ctx);
   return DFLASH_OK;
 }

@@ -22,7 +22,7 @@ from .adaptive import AdaptiveBlock
 
 
 def config_for(shape: wl.ModelShape, block_size: int, max_batch: int, max_ctx: int,
-               max_rows: int, max_tree_nodes: int = 0) -> capi.Config:
+               max_rows: int, max_tree_nodes: int = 0, kv_pages: int = 0) -> capi.Config:
     c = capi.Config()
     c.d_model = shape.d_model
     c.n_heads = shape.n_heads
@@ -43,6 +43,7 @@ def config_for(shape: wl.ModelShape, block_size: int, max_batch: int, max_ctx: i
     c.max_rows = max_rows
     c.max_tree_nodes = max_tree_nodes
     c.dtype = capi.DFLASH_BF16 if shape.dtype == "bf16" else capi.DFLASH_F32
+    c.kv_pages = kv_pages
     return c
 
 
@@ -79,7 +80,7 @@ class DFlashEngine:
 
     def __init__(self, shape: wl.ModelShape, block_size: int, max_batch: int, max_ctx: int,
                  max_rows: Optional[int] = None, max_tree_nodes: int = 0, seed: int = 0,
-                 weights=None, device: str = "cuda"):
+                 weights=None, device: str = "cuda", kv_pages: int = 0):
         capi.load()
         self.shape = shape
         self.B = block_size
@@ -88,7 +89,12 @@ class DFlashEngine:
         self.max_tree_nodes = max_tree_nodes
         self.device = device
         self.max_rows = max_rows or max(max_batch * max(block_size, max_tree_nodes), 1)
-        self.cfg = config_for(shape, block_size, max_batch, max_ctx, self.max_rows, max_tree_nodes)
+        self.cfg = config_for(shape, block_size, max_batch, max_ctx, self.max_rows, max_tree_nodes,
+                              kv_pages)
+        # paged KV cache: pages are mapped on demand from a shared pool; the
+        # engine keeps a host upper bound of every slot's length for that
+        self.paged = kv_pages > 0
+        self.len_ub = [0] * max_batch
         self.dtype_code = self.cfg.dtype
         self.ctx = capi.dflash_create(self.cfg)
         self.weights = weights if weights is not None else device_weights(shape, seed, device)
@@ -156,8 +162,16 @@ class DFlashEngine:
         return device_view(capi.dflash_debug_view(self.ctx, "gen_count")[0], (self.max_batch,),
                            torch.int32)
 
+    def page_table(self) -> torch.Tensor:
+        """Live device view of the page table [max_batch][pages per slot]."""
+        ptr, nbytes = capi.dflash_debug_view(self.ctx, "page_table")
+        return device_view(ptr, (self.max_batch, nbytes // 4 // self.max_batch), torch.int32)
+
     def debug_view(self, name: str, layer: int = 0) -> torch.Tensor:
-        """Zero-copy view of an internal buffer (see dflash_debug_view)."""
+        """A view of an internal buffer (see dflash_debug_view).  The caches
+        come back as [max_batch][n_kv_heads][max_ctx][head_dim], gathered
+        through the page table (a copy; slots of unmapped pages read as page
+        0's); every other buffer is a zero-copy view."""
         ptr, nbytes = capi.dflash_debug_view(self.ctx, name, layer)
         es = 2 if self.shape.dtype == "bf16" else 4
         t = device_view(ptr, (nbytes // es,), torch.bfloat16 if es == 2 else torch.float32)
@@ -166,7 +180,41 @@ class DFlashEngine:
             return t.view(self.max_rows, s.n_inject, s.d_model)
         if name == "fused":
             return t.view(self.max_rows, s.d_model)
-        return t.view(self.max_batch, s.n_kv_heads, self.cfg.max_ctx, s.head_dim)
+        pool = t.view(-1, s.n_kv_heads, capi.PAGE_SLOTS, s.head_dim)
+        g = pool[self.page_table().long().clamp(min=0)]  # [slot][page][kv][row][hd]
+        g = g.permute(0, 2, 1, 3, 4).reshape(self.max_batch, s.n_kv_heads, -1, s.head_dim)
+        return g[:, :, : self.cfg.max_ctx]
+
+    # -- paged KV cache ------------------------------------------------------
+    def reserve(self, seq: int, n_slots: int) -> None:
+        """Maps pages so that slot `seq` covers cache slots 0..n_slots-1."""
+        capi.dflash_kv_reserve(self.ctx, seq, n_slots)
+
+    def release(self, seq: int) -> None:
+        """Returns slot `seq`'s pages to the pool (after its last pass)."""
+        capi.dflash_kv_release(self.ctx, seq)
+        self.len_ub[seq] = 0
+
+    def free_pages(self) -> int:
+        return capi.dflash_kv_free_pages(self.ctx)
+
+    def reserve_ahead(self, seq_ids, steps: int, rows: int) -> None:
+        """Paged mode: pages for `steps` more steps of at most self.B committed
+        tokens each, plus one pass of `rows` rows (e.g. before capturing a
+        step graph, whose replays map nothing)."""
+        if not self.paged:
+            return
+        for s in _host_ids(seq_ids):
+            self.reserve(s, min(self.len_ub[s] + steps * self.B_max + rows, self.cfg.max_ctx))
+
+    def _pages_for_pass(self, seq_ids, rows: int, advance: int):
+        """Paged mode: maps the pages a pass of `rows` rows per sequence touches
+        and moves the length bound on by `advance` (the most a step commits)."""
+        if not self.paged or torch.cuda.is_current_stream_capturing():
+            return  # a captured step maps nothing: reserve_ahead before capturing
+        for s in _host_ids(seq_ids):
+            self.reserve(s, min(self.len_ub[s] + rows, self.cfg.max_ctx))
+            self.len_ub[s] += advance
 
     def prefill(self, prompts: Sequence[np.ndarray], chunk: Optional[int] = None) -> torch.Tensor:
         """Target prefill of each sequence (slot = its index); returns the
@@ -176,6 +224,9 @@ class DFlashEngine:
         chunk = chunk or self.max_rows
         for s, p in enumerate(prompts):
             capi.dflash_reset_seq(self.ctx, s)
+            if self.paged:
+                self.reserve(s, len(p))
+                self.len_ub[s] = len(p)
             sid = torch.tensor([s], dtype=torch.int32, device=self.device)
             toks = torch.from_numpy(np.asarray(p, dtype=np.int32)).to(self.device)
             for c0 in range(0, len(p), chunk):
@@ -195,6 +246,7 @@ class DFlashEngine:
              draft_override: Optional[torch.Tensor] = None):
         b = seq_ids.numel()
         B = self.B
+        self._pages_for_pass(seq_ids, B, B)
         block = self.block[: b * B]
         dlog = vlog = None
         if want_logits:
@@ -229,6 +281,7 @@ class DFlashEngine:
         b = seq_ids.numel()
         B = self.B
         V = self.shape.vocab
+        self._pages_for_pass(seq_ids, B, B)
         if not hasattr(self, "_samp"):
             rows = self.max_batch * max(self.B_max - 1, 1)
             self._samp = {
@@ -264,6 +317,7 @@ class DFlashEngine:
     def ar_step(self, seq_ids: torch.Tensor, anchors: torch.Tensor):
         """Plain greedy decoding step: verify the anchor alone, commit it."""
         b = seq_ids.numel()
+        self._pages_for_pass(seq_ids, 1, 1)
         toks = anchors.contiguous()
         argmax = self.argmax[:b]
         capi.dflash_verify(self.ctx, b, seq_ids, toks, 1, None, 0, argmax)
@@ -288,6 +342,7 @@ class DFlashEngine:
         B = self.B
         m = self.tree_mem
         n = self.max_tree_nodes
+        self._pages_for_pass(seq_ids, max(B, n), B)
         ids = m["topk_ids"][: b * (B - 1) * topk]
         lps = m["topk_logp"][: b * (B - 1) * topk]
         block = self.block[: b * B]
@@ -376,6 +431,10 @@ class _CudaArray:
     def __init__(self, ptr: int, shape, typestr: str):
         self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr,
                                          "data": (ptr, False), "version": 2, "strides": None}
+
+
+def _host_ids(seq_ids) -> List[int]:
+    return seq_ids.tolist() if isinstance(seq_ids, torch.Tensor) else list(seq_ids)
 
 
 def device_view(ptr: int, shape, dtype: torch.dtype) -> torch.Tensor:

@@ -84,7 +84,13 @@ typedef struct {
   int32_t max_rows;            /* rows of one target pass (batch*q), >= max_batch*block */
   int32_t max_tree_nodes;      /* 0 or >= 2 (root + drafted nodes), <= 128 */
   int32_t dtype;               /* storage type of weights, caches, capture: DFLASH_F32 | DFLASH_BF16 */
+  int32_t kv_pages;            /* paged KV cache: pages of DFLASH_PAGE_SLOTS slots in each
+                                  layer's pool, shared by all slots (dflash_kv_reserve);
+                                  0: every slot owns max_ctx slots of its own */
 } dflash_config;
+
+/* Cache slots per KV page (one attention key tile). */
+#define DFLASH_PAGE_SLOTS 128
 
 typedef struct dflash_ctx dflash_ctx;
 
@@ -132,8 +138,61 @@ DFLASH_API dflash_status dflash_create(const dflash_config *cfg, dflash_ctx **ou
 DFLASH_API dflash_status dflash_set_weight(dflash_ctx *ctx, const char *name, const void *dev_ptr,
                                 int32_t dtype, const int64_t *shape, int32_t ndim);
 
-/* Marks sequence slot `seq_id` empty (committed length 0). */
+/* Marks sequence slot `seq_id` empty (committed length 0).  Its KV pages stay
+ * mapped (dflash_kv_release returns them). */
 DFLASH_API dflash_status dflash_reset_seq(dflash_ctx *ctx, int32_t seq_id, dflash_stream_t stream);
+
+/* ---- paged KV cache --------------------------------------------------------
+ * The serving-side cache behind concurrency measurements like the SGLang line
+ * of "DFlash, Diffusion LLMs, dLLM, MTP and Speculative Decoding: A Deep
+ * Research Report", section "DFlash benchmark results"; the report gives no
+ * layout, so this one is the library's own.
+ * Every target and draft layer keeps its K and V in a pool of pages
+ * [page][n_kv_heads][DFLASH_PAGE_SLOTS][head_dim]; cache slot s of sequence
+ * slot q lives in page table[q][s / DFLASH_PAGE_SLOTS] at row
+ * s % DFLASH_PAGE_SLOTS.  One page table serves all layers and both models
+ * (a slot holds the same position in each).
+ * With kv_pages = 0 at create, the pool has max_batch * ceil(max_ctx / 128)
+ * pages and slot q owns pages q * ceil(max_ctx / 128) + i for good.
+ * With kv_pages > 0, the pool has kv_pages pages, no slot owns any, and a
+ * pass over a sequence whose slots 0 .. length + rows - 1 are not all mapped
+ * sets the sticky device status DFLASH_E_CAPACITY and skips that sequence.
+ *
+ * dflash_kv_reserve maps pages so that slot seq_id covers slots
+ * 0 .. n_slots - 1, taking free pages lowest id first, and writes the new
+ * table entries on `stream` (host-to-device copy; not for use inside a
+ * stream capture).  Returns DFLASH_E_CAPACITY, and maps nothing, when
+ * n_slots > max_ctx or the free pages do not suffice.  With kv_pages = 0 it
+ * only checks n_slots <= max_ctx.
+ * dflash_kv_release returns every page of seq_id to the free list and
+ * unmaps it (on `stream`); with kv_pages = 0 it does nothing.  The caller
+ * orders it after the last pass over that sequence.
+ * dflash_kv_free_pages: pages in the free list (-1 on a null context). */
+DFLASH_API dflash_status dflash_kv_reserve(dflash_ctx *ctx, int32_t seq_id, int32_t n_slots,
+                                           dflash_stream_t stream);
+DFLASH_API dflash_status dflash_kv_release(dflash_ctx *ctx, int32_t seq_id, dflash_stream_t stream);
+DFLASH_API int32_t dflash_kv_free_pages(const dflash_ctx *ctx);
+
+/* The page allocator behind dflash_kv_reserve on its own (host memory only,
+ * no GPU): n_pages pages, max_seqs sequence slots of at most max_pages pages.
+ * dflash_kv_pool_reserve grows seq's list to need ceil(n_slots / 128) pages,
+ * lowest free ids first; *first_new / *n_new receive the table index of the
+ * first page added and the count (0 when nothing was needed).  It returns
+ * DFLASH_E_CAPACITY and changes nothing when the pages do not suffice or
+ * exceed max_pages; DFLASH_E_INVALID_ARG for a bad slot or a negative count.
+ * dflash_kv_pool_release frees seq's pages and returns how many it held.
+ * dflash_kv_pool_pages copies seq's page ids into out[0..max_out) and returns
+ * their count.  dflash_kv_pool_free: pages in the free list. */
+typedef struct dflash_kv_pool dflash_kv_pool;
+DFLASH_API dflash_kv_pool *dflash_kv_pool_create(int32_t n_pages, int32_t max_seqs,
+                                                 int32_t max_pages);
+DFLASH_API void dflash_kv_pool_destroy(dflash_kv_pool *pool);
+DFLASH_API dflash_status dflash_kv_pool_reserve(dflash_kv_pool *pool, int32_t seq, int32_t n_slots,
+                                                int32_t *first_new, int32_t *n_new);
+DFLASH_API int32_t dflash_kv_pool_release(dflash_kv_pool *pool, int32_t seq);
+DFLASH_API int32_t dflash_kv_pool_pages(const dflash_kv_pool *pool, int32_t seq, int32_t *out,
+                                        int32_t max_out);
+DFLASH_API int32_t dflash_kv_pool_free(const dflash_kv_pool *pool);
 
 /* Target pass ("verify", also used for prompt prefill and plain AR steps).
  * For every b < batch, rows j < q_len[b] hold tokens[b][j] at position
@@ -256,8 +315,10 @@ DFLASH_API const int32_t *dflash_seq_lengths(const dflash_ctx *ctx);
 DFLASH_API int64_t dflash_launch_count(const dflash_ctx *ctx);
 
 /* Read-only views of internal buffers for tests and tooling.
- *   "k_cache"/"v_cache"   target layer `layer`: [max_batch][n_kv_heads][max_ctx][head_dim]
+ *   "k_cache"/"v_cache"   target layer `layer`: its page pool
+ *                         [pages][n_kv_heads][DFLASH_PAGE_SLOTS][head_dim]
  *   "dk_cache"/"dv_cache" draft layer `layer`: same layout
+ *   "page_table"          [max_batch][ceil(max_ctx / 128)] int32 page ids (-1: unmapped)
  *   "capture"             [max_rows][n_inject][d_model] (row = b*q + j of the last pass)
  *   "fused"               [max_rows][d_model]: the fused feature F = W_fuse h_cat of the
  *                         rows of the last dflash_inject_kv (row order of that call)
@@ -421,6 +482,13 @@ DFLASH_API dflash_status dflash_profile(dflash_ctx *ctx, int32_t enable);
  * classes report 0).  Waits for the recorded events. */
 DFLASH_API dflash_status dflash_profile_read(dflash_ctx *ctx, int32_t kind, int64_t *launches,
                                              double *ms, double *bytes, double *flops);
+
+/* The recorded launches of one kernel class (-1: all) one by one, in launch
+ * order: device milliseconds and flops of the first max_out go to ms[] and
+ * flops[] (either may be NULL).  Returns how many launches were recorded, or
+ * -1 on a null context or a failed event query.  Waits for the events. */
+DFLASH_API int64_t dflash_profile_list(dflash_ctx *ctx, int32_t kind, double *ms, double *flops,
+                                       int64_t max_out);
 
 /* ---- launch plans (host arithmetic only: no GPU, no context) -----------------
  * The pages prescribe no kernel design; these report the shapes this library

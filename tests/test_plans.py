@@ -47,6 +47,9 @@ def test_qwen3_8b_32_sequences_qkv(lib):
     p = capi.dflash_plan_gemm(GB300_SMS, 512, 6144, 4096, QKV)
     assert grid(p) == (48, 2, 1)
     assert (p["BN"], p["threads"], p["smem_bytes"]) == (256, 256, 197720)
+    # O and down (32 feature tiles) would fill 64 SMs: four tiles of 128 rows
+    assert grid(capi.dflash_plan_gemm(GB300_SMS, 512, 4096, 4096, RESID)) == (32, 4, 1)
+    assert grid(capi.dflash_plan_gemm(GB300_SMS, 512, 4096, 12288, RESID)) == (32, 4, 1)
 
 
 @pytest.mark.parametrize("sms", [GB300_SMS, 132, 20])
@@ -60,7 +63,10 @@ def test_gemm_plan_rules(lib, sms):
         p = capi.dflash_plan_gemm(sms, M, N, K, kind)
         BN, mt, nt, st, sp, th, smem = (p[k] for k in ("BN", "m_tiles", "n_tiles", "stages",
                                                        "splits", "threads", "smem_bytes"))
-        assert BN % 16 == 0 and 16 <= BN <= 256 and BN * mt >= M and mt == (M + 255) // 256
+        mt0 = (M + 255) // 256
+        # several token tiles that would fill under half the SMs: twice as many
+        want = 2 * mt0 if mt0 > 1 and nt * mt0 * 2 <= sms else mt0
+        assert BN % 16 == 0 and 16 <= BN <= 256 and BN * mt >= M and mt == want
         assert nt == (N + 127) // 128
         assert 2 <= st <= 8
         assert th == (256 if BN > 32 else 128)
