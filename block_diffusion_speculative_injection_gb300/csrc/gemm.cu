@@ -58,7 +58,7 @@ __device__ __forceinline__ void vocab_tile_reduce(const EpiArgs& e, const float*
     for (int u = threadIdx.x; u < BN; u += blockDim.x) {
       const int t = m0 + u;
       if (t >= M) break;
-      const size_t pb = (size_t)t * gridDim.x + blockIdx.x;
+      const size_t pb = (size_t)t * gridDim.y + blockIdx.y;
       const float* col = tile + u;
       float v1 = -INFINITY, v2 = -INFINITY;
       int i1 = INT_MAX, i2 = INT_MAX;
@@ -92,7 +92,7 @@ __device__ __forceinline__ void vocab_tile_reduce(const EpiArgs& e, const float*
   for (int u = warp; u < BN; u += nw) {
     const int t = m0 + u;
     if (t >= M) break;
-    const size_t pb = (size_t)t * gridDim.x + blockIdx.x;
+    const size_t pb = (size_t)t * gridDim.y + blockIdx.y;
     float x[4], v[4];
     int id[4];
 #pragma unroll
@@ -166,7 +166,12 @@ __global__ void __launch_bounds__(256, 1)
   // segment; its 128-row weight tile is gate rows f0..f0+63 over up rows
   // f0..f0+63 (two 64-row TMA boxes), so SiLU(gate) * up forms in one CTA
   const bool swiglu = p.epi.kind == kEpiSwiGLU;
-  const int n0 = swiglu ? (int)blockIdx.x * 64 : (int)blockIdx.x * 128, m0 = blockIdx.y * BN;
+  // grid: x = token tile, y = weight tile, z = K split.  The token tiles of
+  // one weight tile are neighbours in launch order, so they run together and
+  // the second reads the weight tile from L2 (weights carry an evict-first
+  // hint: a token tile a wave later would find them gone from L2 and fetch
+  // them from HBM again)
+  const int n0 = swiglu ? (int)blockIdx.y * 64 : (int)blockIdx.y * 128, m0 = blockIdx.x * BN;
   const int kb0 = blockIdx.z * p.kb_per_split;
   const int kb1 = min(p.n_kb, kb0 + p.kb_per_split);
   const int nkb = kb1 - kb0;
@@ -703,7 +708,7 @@ dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs&
   p.epi.status = ctx->dev_status;
 
   DF_CUDA_TRY(ctx, ensure_tc_smem());
-  dim3 grid(n_tiles, m_tiles, splits);
+  dim3 grid(m_tiles, n_tiles, splits);
   const size_t smem_bytes = plan.smem_bytes;
   const dim3 cluster(1, 1, splits);
   const dim3 block(plan.threads);
