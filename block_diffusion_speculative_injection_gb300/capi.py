@@ -315,11 +315,11 @@ def dflash_block_attention_workspace(batch, n_heads, n_kv_heads, ctx_len, block)
 
 def dflash_plan_gemm(sm_count, M, N, K, kind, max_splits=8) -> dict:
     """Launch plan of the tensor-core GEMM (host arithmetic; no GPU needed)."""
-    out = (ctypes.c_int32 * 7)()
+    out = (ctypes.c_int32 * 8)()
     st = load().dflash_plan_gemm(sm_count, M, N, K, kind, max_splits, ctypes.addressof(out))
     if st != 0:
         raise DFlashError(st, "dflash_plan_gemm")
-    keys = ("BN", "m_tiles", "n_tiles", "stages", "splits", "threads", "smem_bytes")
+    keys = ("BN", "m_tiles", "n_tiles", "stages", "splits", "threads", "smem_bytes", "persistent")
     return dict(zip(keys, list(out)))
 
 

@@ -219,11 +219,21 @@ __device__ __forceinline__ void group_bar_sync(int grp) {
   else asm volatile("bar.sync 2, 128;" ::: "memory");
 }
 
+// All threads that run the epilogue: the whole CTA (ep_threads == blockDim.x)
+// or, in the persistent kernel, its ep_threads epilogue warps (named barrier 3).
+__device__ __forceinline__ void epi_sync_all(int ep_threads) {
+  if (ep_threads == (int)blockDim.x) __syncthreads();
+  else asm volatile("bar.sync 3, %0;" ::"r"(ep_threads) : "memory");
+}
+
+// ep_tid / ep_threads: this thread's index among the threads that run the
+// epilogue, and their count (a multiple of 128); a warp reads the TMEM lane
+// quarter of its hardware warp index.
 template <typename T>
 __device__ void run_epilogue_direct(const EpiArgs& e, uint32_t tmem, int n0, int m0, int BN,
-                                    float* xbuf) {
-  const int warp = (int)threadIdx.x >> 5, lane = (int)threadIdx.x & 31;
-  const int quarter = warp & 3, grp = warp >> 2, ngrp = (int)blockDim.x >> 7;
+                                    float* xbuf, int ep_tid, int ep_threads) {
+  const int warp = ep_tid >> 5, lane = ep_tid & 31;
+  const int quarter = ((int)threadIdx.x >> 5) & 3, grp = warp >> 2, ngrp = ep_threads >> 7;
   const int f = quarter * 32 + lane;
   const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16);
   const int c0 = grp * 16, cstep = ngrp * 16;
@@ -327,7 +337,8 @@ __device__ void run_epilogue_direct(const EpiArgs& e, uint32_t tmem, int n0, int
       // nothing to write) and of its cos/sin table row (-1: no rotation)
       long long* const s_dst = reinterpret_cast<long long*>(xbuf + 2 * 16 * 128);
       int* const s_rope = reinterpret_cast<int*>(s_dst + 256);
-      for (int u = (int)threadIdx.x; u < BN; u += (int)blockDim.x) {
+      epi_sync_all(ep_threads);  // the previous tile's readers are done with s_dst / s_rope
+      for (int u = ep_tid; u < BN; u += ep_threads) {
         const int t = m0 + u;
         long long dst = -1;
         int rope = -1;
@@ -351,7 +362,7 @@ __device__ void run_epilogue_direct(const EpiArgs& e, uint32_t tmem, int n0, int
         s_dst[u] = dst;
         s_rope[u] = rope;
       }
-      __syncthreads();
+      epi_sync_all(ep_threads);
       const float* const rcos = e.rcos;
       const float* const rsin = e.rsin;
       const int j = f & 63;

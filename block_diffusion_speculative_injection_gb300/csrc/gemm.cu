@@ -37,6 +37,7 @@ struct TcParams {
   int n_seg;
   int seg_begin[kMaxSeg + 1];
   int BN, stages, kb_per_split, n_kb;
+  int m_tiles, n_tiles;  // the persistent form walks m_tiles * n_tiles tiles
   float* out;
   long long split_stride;
   int32_t* status;
@@ -319,7 +320,8 @@ __global__ void __launch_bounds__(256, 1)
     return;
   }
   if (p.epi.splits == 1) {  // no K split: straight from TMEM
-    run_epilogue_direct<bf16>(p.epi, tmem, n0, m0, BN, reinterpret_cast<float*>(smem));
+    run_epilogue_direct<bf16>(p.epi, tmem, n0, m0, BN, reinterpret_cast<float*>(smem),
+                              (int)threadIdx.x, (int)blockDim.x);
     tc_fence_before();
     __syncthreads();
     if (warp == 1) tmem_dealloc(tmem, tmem_cols);
@@ -354,6 +356,172 @@ __global__ void __launch_bounds__(256, 1)
   cluster_sync();
   run_epilogue_cluster<bf16>(p.epi, n0, m0, BN, part, s_meta);
   cluster_sync();  // peers may still be reading this CTA's partial tile
+}
+
+// ---------------------------------------------------------------------------
+// Persistent form for passes of more tiles than SMs (wide token tiles, no K
+// split): one CTA per SM walks the tiles t = blockIdx.x, + gridDim.x, ...
+// (token tile fastest, as in the grid above).  Warp 0 issues TMA through the
+// stage ring continuously across tiles, warp 1 issues the MMAs into one of
+// two accumulators in tensor memory (columns 0 and 256), and warps 2..9 run
+// the epilogue of tile i from one accumulator while the MMAs of tile i + 1
+// fill the other, so the epilogue no longer idles the tensor pipe.  The
+// epilogue's scratch (two 16 x 128 fp32 exchange buffers, 256 row offsets)
+// has its own shared memory after the ring.
+// ---------------------------------------------------------------------------
+constexpr int kPersistThreads = 320;
+constexpr uint32_t kPersistScratch = 2 * 16 * 128 * 4 + 256 * 8 + 256 * 4;
+constexpr size_t kPersistSmemMax = 227 * 1024;  // the opt-in limit per CTA
+
+__global__ void __launch_bounds__(kPersistThreads, 1)
+    gemm_tc_persistent_kernel(const __grid_constant__ TmapSet wmaps,
+                              const __grid_constant__ CUtensorMap xmap, const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int BN = p.BN, S = p.stages;
+  const uint32_t a_bytes = 128 * 64 * 2;
+  const uint32_t b_bytes = (uint32_t)BN * 64 * 2;
+  uint8_t* a_s = smem;
+  uint8_t* b_s = smem + S * a_bytes;
+  float* scratch = reinterpret_cast<float*>(b_s + S * b_bytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(scratch) + kPersistScratch);
+  uint64_t* empty = full + S;
+  uint64_t* acc_full = empty + S;   // [2] accumulator ready for the epilogue
+  uint64_t* acc_empty = acc_full + 2;  // [2] accumulator read out (8 epilogue warps)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool swiglu = p.epi.kind == kEpiSwiGLU;
+  const int n_tiles_total = p.m_tiles * p.n_tiles;
+  const int nkb = p.n_kb;
+  // tile -> (first output feature, first token row, weight segment and row)
+  auto tile_geo = [&](int tile, int& n0, int& m0, int& seg, int& wrow0) {
+    const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+    n0 = swiglu ? nt * 64 : nt * 128;
+    m0 = mt * BN;
+    seg = 0;
+    if (!swiglu)
+      while (seg + 1 < p.n_seg && p.seg_begin[seg + 1] <= n0) ++seg;
+    wrow0 = swiglu ? n0 : n0 - p.seg_begin[seg];
+  };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 8);
+    }
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_trigger();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // TMA producer: k-block g of this CTA's stream goes to stage g % S
+      tma_prefetch_desc(&xmap);
+      const uint64_t wpol = l2_policy_evict_first();
+      uint32_t g = 0;
+      bool ok = true, waited = false;
+      for (int tile = blockIdx.x; ok && tile < n_tiles_total; tile += gridDim.x) {
+        int n0, m0, seg, wrow0;
+        tile_geo(tile, n0, m0, seg, wrow0);
+        for (int kb = 0; kb < nkb; ++kb, ++g) {
+          const int s = (int)(g % (uint32_t)S);
+          const uint32_t ph = (g / (uint32_t)S) & 1u;
+          if (g >= (uint32_t)S && !mbar_wait(&empty[s], ph ^ 1u, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], a_bytes + b_bytes);
+          const int kx = kb * 64;
+          if (swiglu) {
+            tma_load_2d_hint(a_s + s * a_bytes, &wmaps.m[0], kx, wrow0, &full[s], wpol);
+            tma_load_2d_hint(a_s + s * a_bytes + a_bytes / 2, &wmaps.m[1], kx, wrow0, &full[s], wpol);
+          } else {
+            tma_load_2d_hint(a_s + s * a_bytes, &wmaps.m[seg], kx, wrow0, &full[s], wpol);
+          }
+          // the activations are the preceding kernel's output: wait for it
+          // once, after the first weight tiles are on their way
+          if (!waited) {
+            pdl_wait();
+            waited = true;
+          }
+          tma_load_2d(b_s + s * b_bytes, &xmap, kx, m0, &full[s]);
+        }
+      }
+      // drain: every issued copy has landed before this thread leaves
+      for (uint32_t i = g > (uint32_t)S ? g - (uint32_t)S : 0u; i < g; ++i)
+        mbar_wait(&full[i % (uint32_t)S], (i / (uint32_t)S) & 1u, p.status);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // MMA issuer: tile i accumulates into buffer i & 1
+      const uint32_t idesc = idesc_bf16_f32(128, BN);
+      uint32_t g = 0;
+      int i = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < n_tiles_total; tile += gridDim.x, ++i) {
+        const int buf = i & 1;
+        if (i >= 2 && !mbar_wait(&acc_empty[buf], ((i >> 1) - 1) & 1, p.status)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(buf * 256);
+        for (int kb = 0; kb < nkb; ++kb, ++g) {
+          const int s = (int)(g % (uint32_t)S);
+          if (!mbar_wait(&full[s], (g / (uint32_t)S) & 1u, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sw128_desc(smem_u32(a_s + s * a_bytes));
+          const uint64_t bd = sw128_desc(smem_u32(b_s + s * b_bytes));
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(&empty[s]);
+        }
+        if (ok) tc_commit(&acc_full[buf]);
+      }
+    }
+    __syncwarp();
+  } else {
+    // epilogue warps 2..9 (ordered after the preceding kernel before they
+    // read the residual or write anything)
+    pdl_wait();
+    const int ep_tid = (int)threadIdx.x - 64;
+    int i = 0;
+    for (int tile = blockIdx.x; tile < n_tiles_total; tile += gridDim.x, ++i) {
+      const int buf = i & 1;
+      // a wait that gives up has set the status word; the warps go on
+      // together regardless (one warp leaving alone would strand the others
+      // at the epilogue's named barriers, which have no time limit)
+      mbar_wait_sleep(&acc_full[buf], (i >> 1) & 1, p.status);
+      __syncwarp();
+      tc_fence_after();
+      int n0, m0, seg, wrow0;
+      tile_geo(tile, n0, m0, seg, wrow0);
+      run_epilogue_direct<bf16>(p.epi, tmem + (uint32_t)(buf * 256), n0, m0, BN, scratch, ep_tid,
+                                kPersistThreads - 64);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
 // fp32 storage: the epilogue runs as its own kernel over the slab (splits = 1)
@@ -519,11 +687,21 @@ static size_t tc_smem_bytes(int BN, int stages) {
 struct TcPlan {
   int BN, m_tiles, n_tiles, stages, n_kb, splits, kb_per, threads;
   size_t smem_bytes;
+  int persistent;  // CTAs of the persistent form (0: one CTA per tile)
 };
+
+static size_t persist_smem_bytes(int BN, int stages) {
+  return 1024 + (size_t)stages * (128 * 64 * 2 + BN * 64 * 2) + kPersistScratch +
+         (2 * stages + 4) * 8 + 16;
+}
 
 static cudaError_t ensure_tc_smem() {
   static std::atomic<bool> done[kMaxDevices];
   return ensure_smem_attr(done, gemm_tc_kernel, 210 * 1024);
+}
+static cudaError_t ensure_persist_smem() {
+  static std::atomic<bool> done[kMaxDevices];
+  return ensure_smem_attr(done, gemm_tc_persistent_kernel, (int)kPersistSmemMax);
 }
 
 static TcPlan plan_tc(int sm_count, int M, int N, int K, int kind, int max_splits) {
@@ -571,6 +749,22 @@ static TcPlan plan_tc(int sm_count, int M, int N, int K, int kind, int max_split
   // second group of 4 warps then shares the epilogue at no occupancy cost
   t.threads = t.BN > 32 ? 256 : 128;
   t.smem_bytes = tc_smem_bytes(t.BN, t.stages);
+  // More tiles than SMs, wide token tiles and no K split: the persistent
+  // form (one CTA per SM, the epilogue of a tile overlapping the next tile's
+  // main loop).  The lm_head's vocabulary epilogue stages its tile in the
+  // ring's memory, so it keeps one CTA per tile.
+  t.persistent = 0;
+  if (t.splits == 1 && t.BN > 64 && kind != kEpiSlab && kind != kEpiVocab &&
+      (int64_t)t.n_tiles * t.m_tiles > sm_count) {
+    t.persistent = sm_count;
+    t.threads = kPersistThreads;
+    const int per = 128 * 64 * 2 + t.BN * 64 * 2;
+    const size_t fixed = persist_smem_bytes(t.BN, 0);
+    int st = (int)((kPersistSmemMax - fixed) / (per + 16));
+    if (st > 8) st = 8;
+    t.stages = st;
+    t.smem_bytes = persist_smem_bytes(t.BN, st);
+  }
   return t;
 }
 
@@ -586,6 +780,7 @@ dflash_status plan_gemm(int sm_count, int M, int N, int K, int kind, int max_spl
   out[4] = t.splits;
   out[5] = t.threads;
   out[6] = (int32_t)t.smem_bytes;
+  out[7] = t.persistent;
   return DFLASH_OK;
 }
 
@@ -707,6 +902,17 @@ dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs&
   p.epi.slab = out;
   p.epi.status = ctx->dev_status;
 
+  p.m_tiles = m_tiles;
+  p.n_tiles = n_tiles;
+  if (plan.persistent > 0) {
+    DF_CUDA_TRY(ctx, ensure_persist_smem());
+    const int ctas = (int)std::min<int64_t>((int64_t)m_tiles * n_tiles, plan.persistent);
+    DF_CUDA_TRY(ctx, launch_k(ctx->pdl, gemm_tc_persistent_kernel, dim3(ctas), dim3(kPersistThreads),
+                              plan.smem_bytes, st, maps, *xm, p));
+    DF_LAUNCHED(ctx);
+    *splits_used = 1;
+    return DFLASH_OK;
+  }
   DF_CUDA_TRY(ctx, ensure_tc_smem());
   dim3 grid(m_tiles, n_tiles, splits);
   const size_t smem_bytes = plan.smem_bytes;

@@ -160,18 +160,41 @@ __global__ void embed_kernel(const int32_t* __restrict__ tokens, const T* __rest
   const int r = blockIdx.x;
   float* out = resid + (size_t)r * d;
   const T* src = nullptr;
-  if (row_pos[r] >= 0) {
-    int tok;
-    if (draft_block) {
-      const int b = r / block, j = r % block;
-      if (j == 0) tok = tokens[b];
-      else tok = -2;
-    } else {
-      tok = tokens[r];
-    }
+  // the row's position and token are independent loads (both in flight)
+  const int pos = row_pos[r];
+  int tok;
+  if (draft_block) {
+    const int b = r / block, j = r % block;
+    tok = j == 0 ? tokens[b] : -2;
+  } else {
+    tok = tokens[r];
+  }
+  if (pos >= 0) {
     if (tok == -2) src = mask_emb;
     else if (tok >= 0 && tok < vocab) src = emb + (size_t)tok * d;
     else set_dev_status(status, kDevCheck);
+  }
+  // 16-byte loads and stores when the row and the (borrowed) tables allow
+  constexpr int V = 16 / (int)sizeof(T);
+  const bool aligned = ((reinterpret_cast<uintptr_t>(emb) | reinterpret_cast<uintptr_t>(mask_emb)) &
+                        15u) == 0;
+  if (aligned && d % V == 0 && d % 4 == 0) {
+    for (int i = threadIdx.x * V; i < d; i += blockDim.x * V) {
+      float x[V];
+      if (src) {
+        const uint4 u = *reinterpret_cast<const uint4*>(src + i);
+        const T* e = reinterpret_cast<const T*>(&u);
+#pragma unroll
+        for (int k = 0; k < V; ++k) x[k] = ld_f(e + k);
+      } else {
+#pragma unroll
+        for (int k = 0; k < V; ++k) x[k] = 0.f;
+      }
+#pragma unroll
+      for (int k = 0; k < V; k += 4)
+        *reinterpret_cast<float4*>(out + i + k) = make_float4(x[k], x[k + 1], x[k + 2], x[k + 3]);
+    }
+    return;
   }
   for (int i = threadIdx.x; i < d; i += blockDim.x) out[i] = src ? ld_f(src + i) : 0.f;
 }
@@ -266,17 +289,20 @@ __global__ void __launch_bounds__(kNormThreads)
     norm_vec_kernel(const float* __restrict__ resid, const int32_t* __restrict__ rows_in, int d,
                     const T* __restrict__ gain, T* __restrict__ out, float eps) {
   pdl_trigger();
-  pdl_wait();
   __shared__ float red[32];
+  float4 x[VPT], g[VPT];
+  // the gains are weights (no kernel writes them): load them before waiting
+  // on the preceding kernel
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) g[v] = ld4(gain + (threadIdx.x + v * kNormThreads) * 4);
+  pdl_wait();
   const int i_out = blockIdx.x;
   const int r = rows_in ? rows_in[i_out] : i_out;
-  float4 x[VPT], g[VPT];
   float ss = 0.f;
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
     const int i = (threadIdx.x + v * kNormThreads) * 4;
     x[v] = r >= 0 ? ld4(resid + (size_t)r * d + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-    g[v] = ld4(gain + i);
   }
 #pragma unroll
   for (int v = 0; v < VPT; ++v) ss += x[v].x * x[v].x + x[v].y * x[v].y + x[v].z * x[v].z + x[v].w * x[v].w;

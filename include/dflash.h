@@ -498,10 +498,14 @@ DFLASH_API int64_t dflash_profile_list(dflash_ctx *ctx, int32_t kind, double *ms
  * on a GPU with sm_count SMs.  kind: 0 fp32 result, 1 QKV, 2 SwiGLU
  * (N = gate rows + up rows, a multiple of 128), 3 residual add, 4 store,
  * 5 injected K/V, 6 lm_head with the vocabulary reduction in the epilogue.
- * max_splits caps the K split.  plan_out[7] receives:
+ * max_splits caps the K split.  plan_out[8] receives:
  * token rows per tile, token-row tiles, 128-row weight tiles, pipeline stages,
  * K splits (= thread-block cluster size), threads per CTA, dynamic shared
- * memory bytes.  DFLASH_E_INVALID_ARG for sizes the GEMM does not take. */
+ * memory bytes, and the CTAs of the persistent form (0 when every tile has a
+ * CTA of its own; else one CTA per SM walks the tiles, with the epilogue of a
+ * tile overlapping the next tile's main loop: passes of more tiles than SMs
+ * with tiles wider than 64 token rows, no K split, and any epilogue but the
+ * lm_head's).  DFLASH_E_INVALID_ARG for sizes the GEMM does not take. */
 DFLASH_API dflash_status dflash_plan_gemm(int32_t sm_count, int32_t M, int32_t N, int32_t K,
                                           int32_t kind, int32_t max_splits, int32_t *plan_out);
 

@@ -69,12 +69,22 @@ def test_gemm_plan_rules(lib, sms):
         assert BN % 16 == 0 and 16 <= BN <= 256 and BN * mt >= M and mt == want
         assert nt == (N + 127) // 128
         assert 2 <= st <= 8
-        assert th == (256 if BN > 32 else 128)
-        assert smem <= 210 * 1024  # the kernel's shared-memory attribute
+        pers = p["persistent"]
+        # persistent form: more tiles than SMs, wide tiles, no K split, not the lm_head
+        want_pers = sp == 1 and BN > 64 and kind not in (SLAB, VOCAB) and nt * mt > sms
+        assert pers == (sms if want_pers else 0)
+        if pers:
+            assert th == 320 and smem <= 227 * 1024
+            # ring + the epilogue's own scratch (two 16 x 128 fp32 buffers, 256 x 12 B)
+            assert smem >= st * (128 * 64 * 2 + BN * 64 * 2) + 2 * 16 * 128 * 4 + 256 * 12
+        else:
+            assert th == (256 if BN > 32 else 128)
+            assert smem <= 210 * 1024  # the kernel's shared-memory attribute
         stage_mem = st * (128 * 64 * 2 + BN * 64 * 2)
         # direct epilogue: two 16 x 128 fp32 exchange buffers, then 256 x 8 B
-        # destination offsets and 256 x 4 B RoPE offsets, all in stage memory
-        assert 2 * 16 * 128 * 4 + 256 * 8 + 256 * 4 <= stage_mem
+        # destination offsets and 256 x 4 B RoPE offsets, in stage memory
+        # (or, persistent, in memory of their own)
+        assert 2 * 16 * 128 * 4 + 256 * 8 + 256 * 4 <= stage_mem or pers
         # a split tile's fp32 partial [BN][128] sits in its own stage memory
         if sp > 1:
             assert BN * 128 * 4 <= stage_mem
