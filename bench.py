@@ -496,7 +496,7 @@ def run_ours(args, w: wl.Workload) -> None:
     print(json.dumps(line))
 
 
-KERNEL_REV = "gemm-v5"
+KERNEL_REV = "gemm-v6"  # vocabulary epilogue, token-tile-first grid, persistent form
 ATTN_KERNELS = "attn_tc_kernel (+ attn_combine_kernel)"
 
 
