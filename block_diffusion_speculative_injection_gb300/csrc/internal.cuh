@@ -1,5 +1,5 @@
 // Internal declarations of the DFlash GB300 library: context layout,
-// kernel launchers and small PTX wrappers (mbarrier, TMA, tcgen05, mma.sync).
+// kernel launchers and small PTX wrappers (mbarrier, TMA, tcgen05).
 #pragma once
 
 #include <cuda.h>
