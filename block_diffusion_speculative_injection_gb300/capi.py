@@ -62,6 +62,9 @@ _SIGS = {
     "dflash_set_weight": ([_P, ctypes.c_char_p, _P, _I, ctypes.POINTER(ctypes.c_int64), _I], _I),
     "dflash_reset_seq": ([_P, _I, _P], _I),
     "dflash_kv_reserve": ([_P, _I, _I, _P], _I),
+    "dflash_injection_rows": ([_P, ctypes.POINTER(_P), ctypes.POINTER(_P), ctypes.POINTER(_P),
+                               ctypes.POINTER(_I)], _I),
+    "dflash_advance_lengths": ([_P, _I, _P, _P, _P], _I),
     "dflash_kv_release": ([_P, _I, _P], _I),
     "dflash_kv_free_pages": ([_P], _I),
     "dflash_kv_pool_create": ([_I, _I, _I], _P),
@@ -178,6 +181,19 @@ def dflash_set_weight(ctx: int, name: str, tensor, dtype: int) -> None:
 
 def dflash_reset_seq(ctx: int, seq_id: int, stream=None) -> None:
     _check(ctx, load().dflash_reset_seq(ctx, seq_id, _stream(stream)))
+
+
+def dflash_injection_rows(ctx):
+    """(hidden, row_seq, row_pos device pointers, rows) of the pending injection queue."""
+    h, rs, rp, n = _P(), _P(), _P(), _I()
+    _check(ctx, load().dflash_injection_rows(ctx, ctypes.byref(h), ctypes.byref(rs), ctypes.byref(rp),
+                                             ctypes.byref(n)))
+    return h.value, rs.value, rp.value, n.value
+
+
+def dflash_advance_lengths(ctx, batch: int, seq_ids, counts, stream=None) -> None:
+    _check(ctx, load().dflash_advance_lengths(ctx, batch, _ptr(seq_ids), _ptr(counts),
+                                              _stream(stream)))
 
 
 def dflash_kv_reserve(ctx, seq_id: int, n_slots: int, stream=None) -> None:

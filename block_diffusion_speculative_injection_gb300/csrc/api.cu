@@ -34,6 +34,14 @@ static dflash_status fail(dflash_ctx* ctx, dflash_status s, const char* fmt, ...
   return s;
 }
 
+// refuses a call made while another device than the context's is current
+#define DF_ON_DEVICE(ctx)                                                              \
+  do {                                                                                 \
+    if (!ctx_on_current_device(ctx))                                                   \
+      return fail(ctx, DFLASH_E_STATE, "called with another device current than the " \
+                                       "context's (device %d)", (ctx)->device);         \
+  } while (0)
+
 // draft pass keeps its own per-sequence metadata so that a draft issued
 // between a verify and its accept never disturbs the verify's record
 struct DraftMeta {
@@ -515,6 +523,7 @@ dflash_status dflash_set_weight(dflash_ctx* ctx, const char* name, const void* d
 
 dflash_status dflash_reset_seq(dflash_ctx* ctx, int32_t seq_id, dflash_stream_t stream) {
   if (!ctx) return DFLASH_E_INVALID_ARG;
+  DF_ON_DEVICE(ctx);
   if (seq_id < 0 || seq_id >= ctx->cfg.max_batch)
     return fail(ctx, DFLASH_E_INVALID_ARG, "seq_id %d out of range", seq_id);
   DF_CUDA_TRY(ctx, cudaMemsetAsync(ctx->seq_len + seq_id, 0, sizeof(int32_t),
@@ -529,6 +538,7 @@ dflash_status dflash_verify(dflash_ctx* ctx, int32_t batch, const int32_t* seq_i
                             int32_t flags, int32_t* argmax_dev, float* margin_dev,
                             float* logits_dev, dflash_stream_t stream) {
   if (!ctx) return DFLASH_E_INVALID_ARG;
+  DF_ON_DEVICE(ctx);
   if (!seq_ids_dev || !tokens_dev || !argmax_dev)
     return fail(ctx, DFLASH_E_INVALID_ARG, "null pointer argument");
   if (batch < 1 || batch > ctx->cfg.max_batch || q < 1)
@@ -568,6 +578,7 @@ dflash_status dflash_draft_block(dflash_ctx* ctx, int32_t batch, const int32_t* 
                                  int32_t* topk_ids_dev, float* topk_logp_dev, float* logits_dev,
                                  dflash_stream_t stream) {
   if (!ctx) return DFLASH_E_INVALID_ARG;
+  DF_ON_DEVICE(ctx);
   const dflash_config& c = ctx->cfg;
   if (!seq_ids_dev || !anchor_dev || !block_dev)
     return fail(ctx, DFLASH_E_INVALID_ARG, "null pointer argument");
@@ -628,6 +639,7 @@ dflash_status dflash_accept_commit(dflash_ctx* ctx, int32_t batch, const int32_t
                                    int32_t* accept_len_dev, int32_t* next_anchor_dev,
                                    int32_t* emitted_dev, dflash_stream_t stream) {
   if (!ctx) return DFLASH_E_INVALID_ARG;
+  DF_ON_DEVICE(ctx);
   if (!argmax_dev || !accept_len_dev || !next_anchor_dev || !emitted_dev)
     return fail(ctx, DFLASH_E_INVALID_ARG, "null pointer argument");
   if (mode != DFLASH_ACCEPT_GREEDY && mode != DFLASH_ACCEPT_ALL && mode != DFLASH_ACCEPT_GIVEN)
@@ -655,10 +667,33 @@ dflash_status dflash_accept_commit(dflash_ctx* ctx, int32_t batch, const int32_t
   return DFLASH_OK;
 }
 
+dflash_status dflash_advance_lengths(dflash_ctx* ctx, int32_t batch, const int32_t* seq_ids_dev,
+                                    const int32_t* counts_dev, dflash_stream_t stream) {
+  if (!ctx) return DFLASH_E_INVALID_ARG;
+  DF_ON_DEVICE(ctx);
+  if (!seq_ids_dev || !counts_dev) return fail(ctx, DFLASH_E_INVALID_ARG, "null pointer argument");
+  if (batch < 0 || batch > ctx->cfg.max_batch)
+    return fail(ctx, DFLASH_E_INVALID_ARG, "batch %d outside 0..max_batch", batch);
+  if (batch == 0) return DFLASH_OK;
+  return launch_advance_lengths(ctx, batch, seq_ids_dev, counts_dev, (cudaStream_t)stream);
+}
+
+dflash_status dflash_injection_rows(const dflash_ctx* ctx, const void** hidden_dev,
+                                    const int32_t** row_seq_dev, const int32_t** row_pos_dev,
+                                    int32_t* n_rows) {
+  if (!ctx || !hidden_dev || !row_seq_dev || !row_pos_dev || !n_rows) return DFLASH_E_INVALID_ARG;
+  *hidden_dev = ctx->capture;
+  *row_seq_dev = ctx->inj_seq;
+  *row_pos_dev = ctx->inj_pos;
+  *n_rows = ctx->pending_rows;
+  return DFLASH_OK;
+}
+
 dflash_status dflash_inject_kv(dflash_ctx* ctx, int32_t n_rows, const int32_t* row_seq_dev,
                                const int32_t* row_pos_dev, const void* hidden_dev,
                                dflash_stream_t stream) {
   if (!ctx) return DFLASH_E_INVALID_ARG;
+  DF_ON_DEVICE(ctx);
   const dflash_config& c = ctx->cfg;
   DF_TRY(resolve_weights(ctx));
   cudaStream_t st = (cudaStream_t)stream;
@@ -711,6 +746,7 @@ dflash_status dtree_build(dflash_ctx* ctx, int32_t batch, const int32_t* anchor_
                           const int32_t* topk_ids_dev, const float* topk_logp_dev, int32_t topk,
                           int32_t budget, const dtree_buffers* tree, dflash_stream_t stream) {
   if (!ctx) return DFLASH_E_INVALID_ARG;
+  DF_ON_DEVICE(ctx);
   const dflash_config& c = ctx->cfg;
   if (!anchor_dev || !topk_ids_dev || !topk_logp_dev || !tree || !tree->tok || !tree->parent ||
       !tree->depth || !tree->anc || !tree->n_nodes)
@@ -732,6 +768,7 @@ dflash_status dtree_verify(dflash_ctx* ctx, int32_t batch, const int32_t* seq_id
                            const dtree_buffers* tree, int32_t* node_argmax_dev, float* margin_dev,
                            float* logits_dev, dflash_stream_t stream) {
   if (!ctx) return DFLASH_E_INVALID_ARG;
+  DF_ON_DEVICE(ctx);
   const dflash_config& c = ctx->cfg;
   if (!seq_ids_dev || !tree || !node_argmax_dev || !tree->tok || !tree->depth || !tree->anc ||
       !tree->n_nodes)
@@ -759,6 +796,7 @@ dflash_status dtree_verify(dflash_ctx* ctx, int32_t batch, const int32_t* seq_id
 
 dflash_status dflash_check(dflash_ctx* ctx) {
   if (!ctx) return DFLASH_E_INVALID_ARG;
+  DF_ON_DEVICE(ctx);
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return fail(ctx, DFLASH_E_CUDA, "device: %s", cudaGetErrorString(e));
   int32_t s = 0;

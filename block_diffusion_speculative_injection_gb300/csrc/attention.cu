@@ -373,9 +373,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const bool need_mask = tile_start + kTK > mask_from || tile_start + kTK > k_stop;
-      // pass 1: tile max of the visible scores (scaled after the max: scale > 0),
-      // in four independent chains
-      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      // pass 1: tile max of the visible scores (scaled after the max: scale > 0)
+      float mx = -INFINITY;
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
         uint32_t v[32];
@@ -385,13 +384,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           const uint32_t vis = visible32(kb0 + 32 * c);
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            m4[i & 3] = fmaxf(m4[i & 3], ((vis >> i) & 1u) ? __uint_as_float(v[i]) : -INFINITY);
+            mx = fmaxf(mx, ((vis >> i) & 1u) ? __uint_as_float(v[i]) : -INFINITY);
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(v[i]));
+          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(v[i]));
         }
       }
-      float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16)) * scale;
       // raise the running max only when it would otherwise grow by > 2^8
       const bool resc = mx > m_used + kRescaleLog2;
@@ -428,7 +426,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       // bf16 residual, stored in the K-major layout of the P.V MMA's A
       // operand (this half's 64 keys are box h)
       uint8_t* const pb = ps + st * kPBytes + h * kPBox;
-      float rs4[4] = {0.f, 0.f, 0.f, 0.f};  // the row sum in four chains
+      float rs = 0.f;
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
         uint32_t v[32];
@@ -443,7 +441,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const int k = q8 * 8 + i;
             e[i] = ex2_approx(fmaf(__uint_as_float(v[k]), scale, nbase));
             if (need_mask && !((vis >> k) & 1u)) e[i] = 0.f;
-            rs4[i & 3] += e[i];
+            rs += e[i];
           }
           uint4 hi, lo;
           split_bf16(e[0], e[1], hi.x, lo.x);
@@ -459,7 +457,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_free[st]);
-      l += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
+      l += rs;
       // a partial last tile: the V rows past the split's keys may hold any
       // bits (another sequence's rows, or a caller's tensor); zero them so
       // that P = 0 never meets a non-finite value

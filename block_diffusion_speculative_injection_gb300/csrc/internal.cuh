@@ -189,6 +189,14 @@ dflash_status pages_fill_table(dflash_ctx* ctx);
 void pages_destroy(dflash_ctx* ctx);
 int64_t pages_key_bound(const dflash_ctx* ctx);
 
+// A context's calls launch on the current device: it must be the device the
+// context was created on (a context on another GPU would be handed foreign
+// pointers).  Entry points that launch refuse the call otherwise.
+inline bool ctx_on_current_device(const dflash_ctx* ctx) {
+  int d = -1;
+  return cudaGetDevice(&d) == cudaSuccess && d == ctx->device;
+}
+
 inline KvPages ctx_pages(const dflash_ctx* ctx) {
   return KvPages{ctx->page_tab, ctx->pps, ctx->n_pages, 0};
 }
@@ -242,6 +250,8 @@ dflash_status launch_accept_linear(dflash_ctx* ctx, int batch, const int32_t* se
                                    const int32_t* block, const int32_t* argmax, int q, int mode,
                                    int32_t* accept_len, int32_t* next_anchor, int32_t* emitted,
                                    cudaStream_t st);
+dflash_status launch_advance_lengths(dflash_ctx* ctx, int batch, const int32_t* seq_ids,
+                                     const int32_t* counts, cudaStream_t st);
 dflash_status launch_tree_build(dflash_ctx* ctx, int batch, const int32_t* anchor,
                                 const int32_t* ids, const float* logp, int topk, int depth,
                                 int budget, const dtree_buffers* t, cudaStream_t st);

@@ -153,6 +153,10 @@ int32_t dflash_kv_pool_free(const dflash_kv_pool* pool) {
 dflash_status dflash_kv_reserve(dflash_ctx* ctx, int32_t seq_id, int32_t n_slots,
                                 dflash_stream_t stream) {
   if (!ctx) return DFLASH_E_INVALID_ARG;
+  if (!ctx_on_current_device(ctx)) {
+    ctx->last_error = "called with another device current than the context's";
+    return DFLASH_E_STATE;
+  }
   const dflash_config& c = ctx->cfg;
   if (seq_id < 0 || seq_id >= c.max_batch || n_slots < 0) {
     ctx->last_error = "dflash_kv_reserve: bad slot or slot count";
@@ -183,6 +187,10 @@ dflash_status dflash_kv_reserve(dflash_ctx* ctx, int32_t seq_id, int32_t n_slots
 
 dflash_status dflash_kv_release(dflash_ctx* ctx, int32_t seq_id, dflash_stream_t stream) {
   if (!ctx) return DFLASH_E_INVALID_ARG;
+  if (!ctx_on_current_device(ctx)) {
+    ctx->last_error = "called with another device current than the context's";
+    return DFLASH_E_STATE;
+  }
   if (seq_id < 0 || seq_id >= ctx->cfg.max_batch) {
     ctx->last_error = "dflash_kv_release: bad slot";
     return DFLASH_E_INVALID_ARG;

@@ -87,6 +87,40 @@ dflash_status launch_accept_linear(dflash_ctx* ctx, int batch, const int32_t* se
   return DFLASH_OK;
 }
 
+// Committed lengths moved on by counts decided elsewhere (a drafter-side
+// context mirroring the commits of a verifier-side one).  A count that would
+// pass max_ctx leaves the length and flags the capacity status.
+__global__ void advance_lengths_kernel(int batch, const int32_t* __restrict__ seq_ids,
+                                       const int32_t* __restrict__ counts,
+                                       int32_t* __restrict__ seq_len, int max_batch, int max_ctx,
+                                       int32_t* status) {
+  pdl_wait();
+  pdl_trigger();
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= batch) return;
+  const int seq = seq_ids[b], n = counts[b];
+  if (seq < 0 || seq >= max_batch) {
+    set_dev_status(status, kDevCheck);
+    return;
+  }
+  if (n <= 0) return;
+  if (seq_len[seq] + n > max_ctx) {
+    set_dev_status(status, kDevCapacity);
+    return;
+  }
+  seq_len[seq] += n;
+}
+
+dflash_status launch_advance_lengths(dflash_ctx* ctx, int batch, const int32_t* seq_ids,
+                                     const int32_t* counts, cudaStream_t st) {
+  ProfScope prof__(ctx, kProfSpec, st);
+  DF_CUDA_TRY(ctx, launch_k(ctx->pdl, advance_lengths_kernel, dim3((batch + 127) / 128), dim3(128),
+                            0, st, batch, seq_ids, counts, ctx->seq_len, ctx->cfg.max_batch,
+                            ctx->cfg.max_ctx, ctx->dev_status));
+  DF_LAUNCHED(ctx);
+  return DFLASH_OK;
+}
+
 // ---------------------------------------------------------------------------
 // DDTree best-first builder (one CTA per sequence; thread 0 runs the heap)
 // ---------------------------------------------------------------------------

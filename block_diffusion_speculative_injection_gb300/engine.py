@@ -96,10 +96,12 @@ class DFlashEngine:
         self.paged = kv_pages > 0
         self.len_ub = [0] * max_batch
         self.dtype_code = self.cfg.dtype
-        self.ctx = capi.dflash_create(self.cfg)
-        self.weights = weights if weights is not None else device_weights(shape, seed, device)
-        for name, t in self.weights.items():
-            capi.dflash_set_weight(self.ctx, name, t, self.dtype_code)
+        # the context belongs to this engine's device: create it there
+        with torch.cuda.device(torch.device(device)):
+            self.ctx = capi.dflash_create(self.cfg)
+            self.weights = weights if weights is not None else device_weights(shape, seed, device)
+            for name, t in self.weights.items():
+                capi.dflash_set_weight(self.ctx, name, t, self.dtype_code)
         i32 = dict(dtype=torch.int32, device=device)
         mb = max_batch
         q = max(block_size, max_tree_nodes, 1)

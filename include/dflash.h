@@ -25,6 +25,9 @@
  *    Weights are BORROWED: they must stay valid until dflash_destroy.
  *    KV caches, the hidden-state capture buffer and all scratch belong to the
  *    context and are allocated once, in dflash_create.
+ *  - A context belongs to the device that was current at dflash_create; its
+ *    calls must be made with that device current (else DFLASH_E_STATE and
+ *    nothing is launched).
  *  - Every call only enqueues work on `stream` and returns without waiting
  *    for the GPU.  A context keeps scratch between calls, so all calls on one
  *    context must be issued on one stream (or otherwise ordered); one
@@ -281,6 +284,33 @@ DFLASH_API dflash_status dflash_accept_commit(dflash_ctx *ctx, int32_t batch, co
 DFLASH_API dflash_status dflash_inject_kv(dflash_ctx *ctx, int32_t n_rows, const int32_t *row_seq_dev,
                                const int32_t *row_pos_dev, const void *hidden_dev,
                                dflash_stream_t stream);
+
+/* ---- drafter and verifier in separate contexts ------------------------------
+ * The glossary "DFlash speculative decoding" (section "Practical meaning and
+ * deployment behaviour") notes that the drafter and the verifier may run on
+ * different devices to overlap their work.  One context then runs the target
+ * passes and commits (the verifier side), another the draft passes and the
+ * injection (the drafter side); these two calls carry a commit across.
+ *
+ * dflash_injection_rows: device pointers to the rows the last
+ * dflash_accept_commit queued for injection -- the capture buffer
+ * [max_rows][n_inject][d_model], and per row its sequence slot (< 0: not
+ * committed) and position -- and the row count.  They stay valid until the
+ * next pass, commit or injection on this context.  Passing them (copied to
+ * the drafter's device) to dflash_inject_kv's explicit-row form injects
+ * exactly what dflash_inject_kv(ctx, 0, NULL, NULL, NULL) would here.
+ *
+ * dflash_advance_lengths: committed length of slot seq_ids_dev[b] += counts
+ * (counts_dev[b] > 0; the verifier's accept_len + 1, or a prompt chunk's
+ * length), so that the drafter-side context drafts at the same positions.
+ * A count that would pass max_ctx leaves that length and sets the sticky
+ * status DFLASH_E_CAPACITY; a bad slot sets DFLASH_E_DEVICE_CHECK. */
+DFLASH_API dflash_status dflash_injection_rows(const dflash_ctx *ctx, const void **hidden_dev,
+                                               const int32_t **row_seq_dev,
+                                               const int32_t **row_pos_dev, int32_t *n_rows);
+DFLASH_API dflash_status dflash_advance_lengths(dflash_ctx *ctx, int32_t batch,
+                                                const int32_t *seq_ids_dev, const int32_t *counts_dev,
+                                                dflash_stream_t stream);
 
 /* DDTree build: per sequence, a best-first heap over prefixes of the per-slot
  * top-k lists (score = fp32 sum of log-probs in depth order; ties: shallower
