@@ -96,6 +96,28 @@ class VerifierSide:
                     self._handoff(counts))
 
 
+    def verify_tree(self, sid: torch.Tensor, tree: dict):
+        """Verify drafted trees (the dtree_buffers arrays, already on this
+        device) with the ancestor-only mask and commit the accepted paths:
+        (accept_len, next_anchor, emitted [b][n], argmax [b][n], hand-off)."""
+        e = self.eng
+        with torch.cuda.device(self.device):
+            b, n, m = sid.numel(), e.max_tree_nodes, e.tree_mem
+            w = e.tree.anc_words
+            for k in ("tok", "parent", "depth"):
+                m[k][: b * n].copy_(tree[k].reshape(-1))
+            m["anc"][: b * n * w].copy_(tree["anc"].reshape(-1))
+            m["n_nodes"][:b].copy_(tree["n_nodes"].reshape(-1))
+            argmax = e.argmax[: b * n]
+            capi.dtree_verify(e.ctx, b, sid, e.tree, argmax, e.margin[: b * n], None)
+            acc, nxt, emitted = e.accept_len[:b], e.next_anchor[:b], e.emitted[: b * n]
+            capi.dflash_accept_commit(e.ctx, b, sid, None, argmax, e.tree, capi.DFLASH_ACCEPT_GREEDY,
+                                      acc, nxt, emitted)
+            counts = acc + 1
+            return (acc.clone(), nxt.clone(), emitted.view(b, n).clone(), argmax.view(b, n).clone(),
+                    self._handoff(counts))
+
+
 class DrafterSide:
     """The draft passes and the KV injection of one context."""
 
@@ -133,6 +155,23 @@ class DrafterSide:
                 return block, dlog.view(b, max(B - 1, 1), -1)
             return block
 
+    def draft_tree(self, sid: torch.Tensor, anchors: torch.Tensor, topk: int, budget: int) -> dict:
+        """The draft pass with per-slot top-k, then the best-first tree
+        (dtree_build): copies of the dtree_buffers arrays of the batch."""
+        e = self.eng
+        with torch.cuda.device(self.device):
+            b, B, n, m = sid.numel(), e.B, e.max_tree_nodes, e.tree_mem
+            ids = m["topk_ids"][: b * (B - 1) * topk]
+            lps = m["topk_logp"][: b * (B - 1) * topk]
+            capi.dflash_draft_block(e.ctx, b, sid, anchors, e.block[: b * B], topk, ids, lps, None)
+            capi.dtree_build(e.ctx, b, anchors, ids, lps, topk, budget, e.tree)
+            w = e.tree.anc_words
+            return {"tok": m["tok"][: b * n].view(b, n).clone(),
+                    "parent": m["parent"][: b * n].view(b, n).clone(),
+                    "depth": m["depth"][: b * n].view(b, n).clone(),
+                    "anc": m["anc"][: b * n * w].view(b, n, w).clone(),
+                    "n_nodes": m["n_nodes"][:b].clone()}
+
 
 @dataclass
 class SplitStep:
@@ -152,9 +191,9 @@ class SplitDFlash:
 
     def __init__(self, shape, block_size: int, max_batch: int, max_ctx: int,
                  draft_device="cuda:0", target_device="cuda:0", max_rows: Optional[int] = None,
-                 seed: int = 0):
+                 seed: int = 0, max_tree_nodes: int = 0):
         self.B = block_size
-        mk = dict(max_rows=max_rows, seed=seed)
+        mk = dict(max_rows=max_rows, seed=seed, max_tree_nodes=max_tree_nodes)
         self.verifier = VerifierSide(DFlashEngine(shape, block_size, max_batch, max_ctx,
                                                   device=str(target_device), **mk))
         self.drafter = DrafterSide(DFlashEngine(shape, block_size, max_batch, max_ctx,
@@ -199,6 +238,20 @@ class SplitDFlash:
         acc, nxt, emitted, argmax, h = self.verifier.verify_block(seq_ids.to(self.vdev), block)
         self.drafter.absorb(sid_d, h.detach_to(self.ddev))
         return SplitStep(block, argmax, acc, nxt, emitted)
+
+    def tree_step(self, seq_ids: torch.Tensor, anchors: torch.Tensor, topk: int, budget: int,
+                  tree_override: Optional[dict] = None) -> SplitStep:
+        """One DDTree step of one group: draft + tree build (drafter), the
+        tree arrays to the verifier, ancestor-masked verify + commit of the
+        accepted path (verifier), hand-off (drafter).  tree_override (tests)
+        replaces the built tree's arrays before the verify pass.  The
+        returned block is the tree's tokens [b][max_nodes]."""
+        sid_d = seq_ids.to(self.ddev)
+        tree = self.drafter.draft_tree(sid_d, anchors.to(self.ddev), topk, budget)
+        tree = {k: (tree_override or tree)[k].to(self.vdev, non_blocking=True) for k in tree}
+        acc, nxt, emitted, argmax, h = self.verifier.verify_tree(seq_ids.to(self.vdev), tree)
+        self.drafter.absorb(sid_d, h.detach_to(self.ddev))
+        return SplitStep(tree["tok"], argmax, acc, nxt, emitted)
 
     def generate(self, prompts: Sequence[np.ndarray], n_new: int, groups: int = 1) -> List[List[int]]:
         """Greedy generation of n_new tokens per prompt.  With groups > 1 the

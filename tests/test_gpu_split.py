@@ -91,3 +91,42 @@ def test_calls_with_another_device_current_are_refused(setup):
         with pytest.raises(capi.DFlashError) as e:
             capi.dflash_reset_seq(eng.ctx, 0)
     assert e.value.status == 8
+
+
+def test_split_tree_steps_match_one_context():
+    """The DDTree step split the same way: the drafter drafts top-k and
+    builds the tree, the tree arrays cross to the verifier, which runs the
+    ancestor-masked verify and commits the accepted path (compaction of the
+    target K/V in its own caches); the path rows' hidden states cross back
+    for injection.  The first step is teacher-forced onto a tree whose path
+    is the target's greedy continuation at slots s_j > j (accept length 6)."""
+    from block_diffusion_speculative_injection_gb300.engine import DFlashEngine
+    from block_diffusion_speculative_injection_gb300.split import SplitDFlash
+    from gpu_replay import forced_tree, tree_arrays
+    w = wl.WORKLOADS["mini_bf16_ddtree"]
+    s, B = w.shape, w.block_size
+    b, nmax = len(LENS), w.tree_budget + 1
+    prompts = _prompts(s.vocab)
+    mr = max(max(LENS), b * nmax)
+    eng = DFlashEngine(s, B, b, 640, max_rows=mr, max_tree_nodes=nmax)
+    ar = eng.generate(prompts, 9, mode="ar")
+    sp = SplitDFlash(s, B, b, 640, max_rows=mr, max_tree_nodes=nmax)
+    sid = eng.seq_ids(b)
+    a1, a2 = eng.prefill(prompts), sp.prefill(prompts)
+    assert torch.equal(a1, a2)
+    forced = tree_arrays([forced_tree(ar[q][0], ar[q][1:7], ar[q][7], nmax, s.vocab, B - 1)
+                          for q in range(b)], nmax)
+    for k in range(3):
+        ov = forced if k == 0 else None
+        r1 = eng.tree_step(sid, a1, w.topk, w.tree_budget, tree_override=ov)
+        r2 = sp.tree_step(sid, a2, w.topk, w.tree_budget, tree_override=ov)
+        for n1, n2 in (("tok", "block"), ("argmax", "argmax"), ("accept_len", "accept_len"),
+                       ("next_anchor", "next_anchor"), ("emitted", "emitted")):
+            assert torch.equal(r1[n1].view(getattr(r2, n2).shape), getattr(r2, n2)), (k, n1)
+        if k == 0:
+            assert (r2.accept_len == 6).all()
+        a1, a2 = r1["next_anchor"].clone(), r2.next_anchor.clone()
+        torch.cuda.synchronize()
+        assert sp.verifier.eng.lengths(b) == sp.drafter.eng.lengths(b) == eng.lengths(b), k
+    sp.close()
+    eng.close()
