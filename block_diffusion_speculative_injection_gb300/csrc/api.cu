@@ -845,6 +845,8 @@ dflash_status dflash_debug_trace(dflash_ctx* ctx, float* dst_dev, int64_t bytes)
   const dflash_config& c = ctx->cfg;
   if (dst_dev && bytes < (int64_t)c.n_target_layers * c.max_rows * c.d_model * (int64_t)sizeof(float))
     return fail(ctx, DFLASH_E_CAPACITY, "trace buffer needs n_target_layers*max_rows*d_model floats");
+  if (reinterpret_cast<uintptr_t>(dst_dev) % 16 != 0)
+    return fail(ctx, DFLASH_E_INVALID_ARG, "trace buffer must be 16-byte aligned");
   ctx->trace = dst_dev;
   return DFLASH_OK;
 }
@@ -854,6 +856,8 @@ dflash_status dflash_debug_trace_draft(dflash_ctx* ctx, float* dst_dev, int64_t 
   const dflash_config& c = ctx->cfg;
   if (dst_dev && bytes < (int64_t)c.n_draft_layers * c.max_rows * c.d_model * (int64_t)sizeof(float))
     return fail(ctx, DFLASH_E_CAPACITY, "trace buffer needs n_draft_layers*max_rows*d_model floats");
+  if (reinterpret_cast<uintptr_t>(dst_dev) % 16 != 0)
+    return fail(ctx, DFLASH_E_INVALID_ARG, "trace buffer must be 16-byte aligned");
   ctx->dtrace = dst_dev;
   return DFLASH_OK;
 }

@@ -422,9 +422,13 @@ __device__ void run_epilogue_direct(const EpiArgs& e, uint32_t tmem, int n0, int
 // Epilogue of a tile whose K splits form a thread-block cluster (residual,
 // store, QKV and injection projections): each CTA has its fp32 partial tile
 // in its own shared memory as part[token][feature]; after a cluster barrier,
-// CTA `rank` takes every S-th work item of the tile, sums the partials of all
-// splits in split order through distributed shared memory, and applies the
-// epilogue operation.  meta[u] = (position, sequence, slot) of tile row u.
+// CTA `rank` takes every S-th work item of the tile (four consecutive
+// features of one tile row), sums the partials of all splits in split order
+// through distributed shared memory, and applies the epilogue operation.
+// A work item issues its global loads (residual, rotary table) and then every
+// split's partial loads before the first add, so that it waits for one round
+// trip of each kind rather than one per split.  meta[u] = (position,
+// sequence, slot) of tile row u.
 template <typename T>
 __device__ void run_epilogue_cluster(const EpiArgs& e, int n0, int m0, int BN, const float* part,
                                      const int32_t* meta) {
@@ -432,32 +436,65 @@ __device__ void run_epilogue_cluster(const EpiArgs& e, int n0, int m0, int BN, c
   const int rank = (int)cluster_ctarank();
   const int cn = min(BN, e.M - m0);
   const uint32_t local = smem_u32(part);
-  auto val = [&](int u, int c) {
-    const uint32_t addr = local + (uint32_t)((u * 128 + c) * 4);
-    float v = 0.f;
+  // features c .. c + 3 of tile row u summed over the splits, from 0 in
+  // split order; with c2 >= 0 also features c2 .. c2 + 3 (into w)
+  auto sum4 = [&](int u, int c, int c2, float4& v, float4& w) {
+    float4 x[8], y[8];
+    const uint32_t a = local + (uint32_t)((u * 128 + c) * 4);
+    const uint32_t a2 = local + (uint32_t)((u * 128 + (c2 < 0 ? c : c2)) * 4);
 #pragma unroll
     for (int s = 0; s < 8; ++s)
-      if (s < S) v += ld_peer_f32(map_peer(addr, (uint32_t)s));
-    return v;
+      if (s < S) x[s] = ld_peer_f32x4(map_peer(a, (uint32_t)s));
+    if (c2 >= 0) {
+#pragma unroll
+      for (int s = 0; s < 8; ++s)
+        if (s < S) y[s] = ld_peer_f32x4(map_peer(a2, (uint32_t)s));
+    }
+    v = make_float4(0.f, 0.f, 0.f, 0.f);
+    w = v;
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+      if (s < S) {
+        v.x += x[s].x;
+        v.y += x[s].y;
+        v.z += x[s].z;
+        v.w += x[s].w;
+      }
+    if (c2 >= 0) {
+#pragma unroll
+      for (int s = 0; s < 8; ++s)
+        if (s < S) {
+          w.x += y[s].x;
+          w.y += y[s].y;
+          w.z += y[s].z;
+          w.w += y[s].w;
+        }
+    }
   };
   const int first = rank * (int)blockDim.x + (int)threadIdx.x;
   const int step = S * (int)blockDim.x;
   switch (e.kind) {
     case kEpiResid: {
       T* cap = static_cast<T*>(e.capture);
-      for (int i = first; i < cn * 128; i += step) {
-        const int u = i >> 7, c = i & 127, t = m0 + u, n = n0 + c;
-        const float r = e.resid[(size_t)t * e.N + n] + val(u, c);
-        e.resid[(size_t)t * e.N + n] = r;
-        if (cap) st_f(cap + ((size_t)t * e.n_inject + e.cap_slot) * e.N + n, r);
-        if (e.trace) e.trace[(size_t)t * e.N + n] = r;
+      for (int i = first; i < cn * 32; i += step) {
+        const int u = i >> 5, c = (i & 31) * 4, t = m0 + u, n = n0 + c;
+        float* rp = e.resid + (size_t)t * e.N + n;
+        const float4 r0 = *reinterpret_cast<const float4*>(rp);
+        float4 v, unused;
+        sum4(u, c, -1, v, unused);
+        const float4 r = make_float4(r0.x + v.x, r0.y + v.y, r0.z + v.z, r0.w + v.w);
+        *reinterpret_cast<float4*>(rp) = r;
+        if (cap) st_f4(cap + ((size_t)t * e.n_inject + e.cap_slot) * e.N + n, r);
+        if (e.trace) *reinterpret_cast<float4*>(e.trace + (size_t)t * e.N + n) = r;
       }
       break;
     }
     case kEpiStore: {
-      for (int i = first; i < cn * 128; i += step) {
-        const int u = i >> 7, c = i & 127;
-        st_f(static_cast<T*>(e.out) + (size_t)(m0 + u) * e.N + n0 + c, val(u, c));
+      for (int i = first; i < cn * 32; i += step) {
+        const int u = i >> 5, c = (i & 31) * 4;
+        float4 v, unused;
+        sum4(u, c, -1, v, unused);
+        st_f4(static_cast<T*>(e.out) + (size_t)(m0 + u) * e.N + n0 + c, v);
       }
       break;
     }
@@ -482,9 +519,11 @@ __device__ void run_epilogue_cluster(const EpiArgs& e, int n0, int m0, int BN, c
       if (is_q) base = static_cast<T*>(e.q_out);
       else base = static_cast<T*>(is_v ? e.vc : e.kc) +
                   (inject ? (size_t)(e.layer0 + layer) * e.layer_elems : 0);
-      const int per = is_v ? 128 : 64;
+      // V: 32 items of 4 features per row; Q, K: 16 items, each with the
+      // rotary partner features 64 further on
+      const int per = is_v ? 32 : 16;
       for (int i = first; i < cn * per; i += step) {
-        const int u = i / per, c = i % per, t = m0 + u;
+        const int u = i / per, c = (i % per) * 4, t = m0 + u;
         const int pos = meta[u * 3], seq = meta[u * 3 + 1], slot = meta[u * 3 + 2];
         if (pos < 0 || seq < 0) continue;
         if (inject && (seq >= e.max_batch || pos >= e.max_ctx)) {
@@ -498,12 +537,18 @@ __device__ void run_epilogue_cluster(const EpiArgs& e, int n0, int m0, int BN, c
         }
         T* dst = base + (size_t)row * 128;
         if (is_v) {
-          st_f(dst + c, val(u, c));
+          float4 v, unused;
+          sum4(u, c, -1, v, unused);
+          st_f4(dst + c, v);
         } else {
-          const float lo = val(u, c), hi = val(u, c + 64);
-          const float cs = e.rcos[(size_t)pos * 64 + c], sn = e.rsin[(size_t)pos * 64 + c];
-          st_f(dst + c, lo * cs - hi * sn);
-          st_f(dst + c + 64, hi * cs + lo * sn);
+          const float4 cs = *reinterpret_cast<const float4*>(e.rcos + (size_t)pos * 64 + c);
+          const float4 sn = *reinterpret_cast<const float4*>(e.rsin + (size_t)pos * 64 + c);
+          float4 lo, hi;
+          sum4(u, c, c + 64, lo, hi);
+          st_f4(dst + c, make_float4(lo.x * cs.x - hi.x * sn.x, lo.y * cs.y - hi.y * sn.y,
+                                     lo.z * cs.z - hi.z * sn.z, lo.w * cs.w - hi.w * sn.w));
+          st_f4(dst + c + 64, make_float4(hi.x * cs.x + lo.x * sn.x, hi.y * cs.y + lo.y * sn.y,
+                                          hi.z * cs.z + lo.z * sn.z, hi.w * cs.w + lo.w * sn.w));
         }
       }
       break;

@@ -363,6 +363,19 @@ template <>
 __device__ __forceinline__ void st_f<float>(float* p, float v) { *p = v; }
 template <>
 __device__ __forceinline__ void st_f<bf16>(bf16* p, float v) { *p = __float2bfloat16_rn(v); }
+// four consecutive elements (address aligned to four elements)
+template <typename T>
+__device__ __forceinline__ void st_f4(T* p, float4 v);
+template <>
+__device__ __forceinline__ void st_f4<float>(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+template <>
+__device__ __forceinline__ void st_f4<bf16>(bf16* p, float4 v) {
+  const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<const uint32_t*>(&a);
+  u.y = *reinterpret_cast<const uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = u;
+}
 
 // ---------------------------------------------------------------------------
 // programmatic dependent launch: a kernel may start while its predecessor
@@ -445,6 +458,15 @@ __device__ __forceinline__ uint32_t map_peer(uint32_t smem_addr, uint32_t rank) 
 __device__ __forceinline__ float ld_peer_f32(uint32_t addr) {
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+// four consecutive fp32 (16-byte aligned address)
+__device__ __forceinline__ float4 ld_peer_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
   return v;
 }
 

@@ -362,14 +362,15 @@ DFLASH_API dflash_status dflash_debug_view(const dflash_ctx *ctx, const char *na
  * residual stream after each target layer, fp32, to
  * dst_dev[layer][row][d_model] (row = b*q + j of the pass; rows past a
  * sequence's block are left as they were).  bytes must cover
- * n_target_layers * max_rows * d_model floats.  NULL switches it off. */
+ * n_target_layers * max_rows * d_model floats, and dst_dev must be 16-byte
+ * aligned (DFLASH_E_INVALID_ARG otherwise).  NULL switches it off. */
 DFLASH_API dflash_status dflash_debug_trace(dflash_ctx *ctx, float *dst_dev, int64_t bytes);
 
 /* Debug: the same trace for draft passes: while dst_dev is set, every
  * dflash_draft_block also writes the residual stream after each draft layer,
  * fp32, to dst_dev[layer][row][d_model] (row = b*B + j of the pass).  bytes
- * must cover n_draft_layers * max_rows * d_model floats.  NULL switches it
- * off. */
+ * must cover n_draft_layers * max_rows * d_model floats, and dst_dev must be
+ * 16-byte aligned.  NULL switches it off. */
 DFLASH_API dflash_status dflash_debug_trace_draft(dflash_ctx *ctx, float *dst_dev, int64_t bytes);
 
 /* Debug: while set, every dflash_draft_block also copies, per draft layer, the
