@@ -706,11 +706,10 @@ static cudaError_t ensure_persist_smem() {
 
 static TcPlan plan_tc(int sm_count, int M, int N, int K, int kind, int max_splits) {
   TcPlan t;
+  // Token tiles as wide as the MMA allows: a 64-column K block takes about
+  // the same time at 80, 128, 144 or 256 token rows, so a pass that leaves
+  // SMs idle is split along K (below) rather than cut into narrower tiles.
   t.m_tiles = (M + 255) / 256;
-  // A pass of several token tiles whose grid would fill fewer than half of
-  // the SMs takes twice as many, half as wide tiles (measured at 512 rows:
-  // O 1.74 -> 1.61 ms and down 3.41 -> 3.30 ms per 32-sequence step).
-  if (t.m_tiles > 1 && (int64_t)((N + 127) / 128) * t.m_tiles * 2 <= sm_count) t.m_tiles *= 2;
   int BN = (M + t.m_tiles - 1) / t.m_tiles;
   BN = ((BN + 15) / 16) * 16;
   t.BN = BN < 16 ? 16 : BN;
@@ -723,13 +722,6 @@ static TcPlan plan_tc(int sm_count, int M, int N, int K, int kind, int max_split
   const int per_sm = (t.BN <= 32) ? 2 : 1;
   const int slots = per_sm * sm_count;
   int splits = ctas >= slots ? 1 : slots / ctas;
-  // Tiles wider than 128 token rows take the whole K range when the unsplit
-  // grid already covers a third of the SMs: their epilogue then runs
-  // straight from tensor memory, while a cluster reduction of such a wide
-  // tile costs more than the parallelism it adds.  Measured on the
-  // concurrency sweep (b = 4, 8, 16, 32 at block 16): splitting pays up to
-  // 128 rows, and above that only for grids of a few dozen CTAs.
-  if (t.BN > 128 && 3 * ctas >= sm_count) splits = 1;
   // the K splits of a tile form one thread-block cluster (portable size <= 8);
   // a SwiGLU tile holds gate and up rows in one CTA and is never split
   const int max_cluster_splits = kind == kEpiSwiGLU ? 1 : 8;  // SwiGLU: direct epilogue only
@@ -743,6 +735,10 @@ static TcPlan plan_tc(int sm_count, int M, int N, int K, int kind, int max_split
   // SM) between 0.875 and 0.97 of that number were resident for cluster
   // sizes 2..8, so the plan counts on 7/8 of it.
   while (splits > 1 && (int64_t)ctas * splits * 8 > (int64_t)slots * 7) --splits;
+  // the cluster epilogue stages each split's fp32 partial tile (BN x 128) in
+  // the CTA's ring memory: a tile whose partial does not fit is not split
+  if (splits > 1 && (size_t)t.BN * 128 * 4 > (size_t)t.stages * (128 * 64 * 2 + t.BN * 64 * 2))
+    splits = 1;
   t.kb_per = (t.n_kb + splits - 1) / splits;
   t.splits = (t.n_kb + t.kb_per - 1) / t.kb_per;
   // tiles of more than 32 token rows hold an SM alone (shared memory): a

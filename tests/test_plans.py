@@ -47,9 +47,12 @@ def test_qwen3_8b_32_sequences_qkv(lib):
     p = capi.dflash_plan_gemm(GB300_SMS, 512, 6144, 4096, QKV)
     assert grid(p) == (48, 2, 1)
     assert (p["BN"], p["threads"], p["smem_bytes"]) == (256, 256, 197720)
-    # O and down (32 feature tiles) would fill 64 SMs: four tiles of 128 rows
-    assert grid(capi.dflash_plan_gemm(GB300_SMS, 512, 4096, 4096, RESID)) == (32, 4, 1)
-    assert grid(capi.dflash_plan_gemm(GB300_SMS, 512, 4096, 12288, RESID)) == (32, 4, 1)
+    # O and down (32 feature tiles) would fill 64 SMs: two K splits per tile
+    assert grid(capi.dflash_plan_gemm(GB300_SMS, 512, 4096, 4096, RESID)) == (32, 2, 2)
+    assert grid(capi.dflash_plan_gemm(GB300_SMS, 512, 4096, 12288, RESID)) == (32, 2, 2)
+    # a DDTree pass of 4 x 65 rows: two 144-row token tiles, O and down split
+    assert grid(capi.dflash_plan_gemm(GB300_SMS, 260, 4096, 14336, RESID)) == (32, 2, 2)
+    assert capi.dflash_plan_gemm(GB300_SMS, 260, 4096, 14336, RESID)["BN"] == 144
 
 
 @pytest.mark.parametrize("sms", [GB300_SMS, 132, 20])
@@ -63,10 +66,8 @@ def test_gemm_plan_rules(lib, sms):
         p = capi.dflash_plan_gemm(sms, M, N, K, kind)
         BN, mt, nt, st, sp, th, smem = (p[k] for k in ("BN", "m_tiles", "n_tiles", "stages",
                                                        "splits", "threads", "smem_bytes"))
-        mt0 = (M + 255) // 256
-        # several token tiles that would fill under half the SMs: twice as many
-        want = 2 * mt0 if mt0 > 1 and nt * mt0 * 2 <= sms else mt0
-        assert BN % 16 == 0 and 16 <= BN <= 256 and BN * mt >= M and mt == want
+        # token tiles as wide as the MMA allows
+        assert BN % 16 == 0 and 16 <= BN <= 256 and BN * mt >= M and mt == (M + 255) // 256
         assert nt == (N + 127) // 128
         assert 2 <= st <= 8
         pers = p["persistent"]
@@ -91,9 +92,14 @@ def test_gemm_plan_rules(lib, sms):
         assert 1 <= sp <= 8 and sp <= K // 64 // 4 or sp == 1
         if kind in (SWIGLU, SLAB, VOCAB):
             assert sp == 1
+        slots = (2 if BN <= 32 else 1) * sms
         if sp > 1:
-            slots = (2 if BN <= 32 else 1) * sms
             assert nt * mt * sp * 8 <= 7 * slots  # every cluster resident at once
+        # a grid that fills under half of the CTA slots is split along K when
+        # two splits are allowed (kind, K, partial tile, cluster residency)
+        if (kind not in (SWIGLU, SLAB, VOCAB) and nt * mt * 2 <= slots and K // 64 // 4 >= 2
+                and BN * 128 * 4 <= stage_mem and nt * mt * 16 <= 7 * slots):
+            assert sp >= 2
 
 
 def test_gemm_plan_refuses_bad_sizes(lib):
