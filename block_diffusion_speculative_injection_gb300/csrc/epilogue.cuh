@@ -419,82 +419,88 @@ __device__ void run_epilogue_direct(const EpiArgs& e, uint32_t tmem, int n0, int
   }
 }
 
-// Epilogue of a tile whose K splits form a thread-block cluster (residual,
-// store, QKV and injection projections): each CTA has its fp32 partial tile
-// in its own shared memory as part[token][feature]; after a cluster barrier,
-// CTA `rank` takes every S-th work item of the tile (four consecutive
-// features of one tile row), sums the partials of all splits in split order
-// through distributed shared memory, and applies the epilogue operation.
-// A work item issues its global loads (residual, rotary table) and then every
-// split's partial loads before the first add, so that it waits for one round
-// trip of each kind rather than one per split.  meta[u] = (position,
-// sequence, slot) of tile row u.
-template <typename T>
-__device__ void run_epilogue_cluster(const EpiArgs& e, int n0, int m0, int BN, const float* part,
-                                     const int32_t* meta) {
-  const int S = e.splits;
-  const int rank = (int)cluster_ctarank();
-  const int cn = min(BN, e.M - m0);
-  const uint32_t local = smem_u32(part);
-  // features c .. c + 3 of tile row u summed over the splits, from 0 in
-  // split order; with c2 >= 0 also features c2 .. c2 + 3 (into w)
-  auto sum4 = [&](int u, int c, int c2, float4& v, float4& w) {
-    float4 x[8], y[8];
-    const uint32_t a = local + (uint32_t)((u * 128 + c) * 4);
-    const uint32_t a2 = local + (uint32_t)((u * 128 + (c2 < 0 ? c : c2)) * 4);
+// Partial sums of NI work items over the S splits of a cluster: item k is
+// features c[k] .. c[k] + 3 of tile row u[k].  Every load (S per item) is
+// issued before the first add; each item's sum starts from 0 and runs in
+// split order.
+template <int S, int NI>
+__device__ __forceinline__ void cluster_sums(uint32_t local, const int (&u)[NI], const int (&c)[NI],
+                                             const bool (&ok)[NI], float4 (&v)[NI]) {
+  float4 x[NI][S];
 #pragma unroll
-    for (int s = 0; s < 8; ++s)
-      if (s < S) x[s] = ld_peer_f32x4(map_peer(a, (uint32_t)s));
-    if (c2 >= 0) {
+  for (int k = 0; k < NI; ++k)
 #pragma unroll
-      for (int s = 0; s < 8; ++s)
-        if (s < S) y[s] = ld_peer_f32x4(map_peer(a2, (uint32_t)s));
-    }
-    v = make_float4(0.f, 0.f, 0.f, 0.f);
-    w = v;
+    for (int s = 0; s < S; ++s)
+      if (ok[k]) x[k][s] = ld_peer_f32x4(map_peer(local + (uint32_t)((u[k] * 128 + c[k]) * 4), (uint32_t)s));
 #pragma unroll
-    for (int s = 0; s < 8; ++s)
-      if (s < S) {
-        v.x += x[s].x;
-        v.y += x[s].y;
-        v.z += x[s].z;
-        v.w += x[s].w;
+  for (int k = 0; k < NI; ++k) {
+    v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int s = 0; s < S; ++s)
+      if (ok[k]) {
+        v[k].x += x[k][s].x;
+        v[k].y += x[k][s].y;
+        v[k].z += x[k][s].z;
+        v[k].w += x[k][s].w;
       }
-    if (c2 >= 0) {
-#pragma unroll
-      for (int s = 0; s < 8; ++s)
-        if (s < S) {
-          w.x += y[s].x;
-          w.y += y[s].y;
-          w.z += y[s].z;
-          w.w += y[s].w;
-        }
-    }
-  };
+  }
+}
+
+// Epilogue of a tile whose K splits form a thread-block cluster (residual,
+// store, QKV and injection projections): each CTA has its fp32 partial tile in
+// its own shared memory as part[token][feature]; after a cluster barrier, CTA
+// `rank` takes every S-th work item of the tile (four consecutive features of
+// one tile row), sums the partials of all splits in split order through
+// distributed shared memory, and applies the epilogue operation.  A thread
+// keeps U = 8 / S work items in flight (4 / S for the rotary projections,
+// whose items carry a partner feature group and table rows): it issues their
+// global loads (residual, rotary table) and every split's partial loads
+// before the first add, so that the whole batch waits for one round trip of
+// each kind.
+// meta[u] = (position, sequence, slot) of tile row u.
+template <typename T, int S>
+__device__ void epilogue_cluster_s(const EpiArgs& e, int n0, int m0, int BN, uint32_t local,
+                                   const int32_t* meta, int rank) {
+  constexpr int U = S >= 8 ? 1 : 8 / S;
+  constexpr int UQ = S >= 4 ? 1 : 4 / S;
+  const int cn = min(BN, e.M - m0);
   const int first = rank * (int)blockDim.x + (int)threadIdx.x;
   const int step = S * (int)blockDim.x;
   switch (e.kind) {
-    case kEpiResid: {
-      T* cap = static_cast<T*>(e.capture);
-      for (int i = first; i < cn * 32; i += step) {
-        const int u = i >> 5, c = (i & 31) * 4, t = m0 + u, n = n0 + c;
-        float* rp = e.resid + (size_t)t * e.N + n;
-        const float4 r0 = *reinterpret_cast<const float4*>(rp);
-        float4 v, unused;
-        sum4(u, c, -1, v, unused);
-        const float4 r = make_float4(r0.x + v.x, r0.y + v.y, r0.z + v.z, r0.w + v.w);
-        *reinterpret_cast<float4*>(rp) = r;
-        if (cap) st_f4(cap + ((size_t)t * e.n_inject + e.cap_slot) * e.N + n, r);
-        if (e.trace) *reinterpret_cast<float4*>(e.trace + (size_t)t * e.N + n) = r;
-      }
-      break;
-    }
+    case kEpiResid:
     case kEpiStore: {
-      for (int i = first; i < cn * 32; i += step) {
-        const int u = i >> 5, c = (i & 31) * 4;
-        float4 v, unused;
-        sum4(u, c, -1, v, unused);
-        st_f4(static_cast<T*>(e.out) + (size_t)(m0 + u) * e.N + n0 + c, v);
+      const bool resid = e.kind == kEpiResid;
+      T* cap = static_cast<T*>(e.capture);
+      const int total = cn * 32;
+      for (int i0 = first; i0 < total; i0 += U * step) {
+        int u[U], c[U];
+        bool ok[U];
+        float4 r0[U], v[U];
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+          const int i = i0 + k * step;
+          ok[k] = i < total;
+          u[k] = ok[k] ? i >> 5 : 0;
+          c[k] = ok[k] ? (i & 31) * 4 : 0;
+          if (resid && ok[k])
+            r0[k] = *reinterpret_cast<const float4*>(e.resid + (size_t)(m0 + u[k]) * e.N + n0 + c[k]);
+        }
+        cluster_sums<S, U>(local, u, c, ok, v);
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+          if (!ok[k]) continue;
+          const size_t t = (size_t)(m0 + u[k]);
+          const int n = n0 + c[k];
+          if (!resid) {
+            st_f4(static_cast<T*>(e.out) + t * e.N + n, v[k]);
+            continue;
+          }
+          const float4 r = make_float4(r0[k].x + v[k].x, r0[k].y + v[k].y, r0[k].z + v[k].z,
+                                       r0[k].w + v[k].w);
+          *reinterpret_cast<float4*>(e.resid + t * e.N + n) = r;
+          if (cap) st_f4(cap + (t * e.n_inject + e.cap_slot) * e.N + n, r);
+          if (e.trace) *reinterpret_cast<float4*>(e.trace + t * e.N + n) = r;
+        }
       }
       break;
     }
@@ -520,41 +526,90 @@ __device__ void run_epilogue_cluster(const EpiArgs& e, int n0, int m0, int BN, c
       else base = static_cast<T*>(is_v ? e.vc : e.kc) +
                   (inject ? (size_t)(e.layer0 + layer) * e.layer_elems : 0);
       // V: 32 items of 4 features per row; Q, K: 16 items, each with the
-      // rotary partner features 64 further on
+      // rotary partner features 64 further on (items UQ .. 2 UQ - 1 below)
       const int per = is_v ? 32 : 16;
-      for (int i = first; i < cn * per; i += step) {
-        const int u = i / per, c = (i % per) * 4, t = m0 + u;
-        const int pos = meta[u * 3], seq = meta[u * 3 + 1], slot = meta[u * 3 + 2];
-        if (pos < 0 || seq < 0) continue;
-        if (inject && (seq >= e.max_batch || pos >= e.max_ctx)) {
-          set_dev_status(e.status, kDevCheck);
-          continue;
+      const int total = cn * per;
+      for (int i0 = first; i0 < total; i0 += UQ * step) {
+        int u[2 * UQ], c[2 * UQ], pos[UQ];
+        bool ok[2 * UQ];
+        T* dst[UQ];
+        float4 cs[UQ], sn[UQ], v[2 * UQ];
+#pragma unroll
+        for (int k = 0; k < UQ; ++k) {
+          const int i = i0 + k * step;
+          bool g = i < total;
+          u[k] = g ? i / per : 0;
+          c[k] = g ? (i % per) * 4 : 0;
+          pos[k] = 0;
+          dst[k] = nullptr;
+          if (g) {
+            const int t = m0 + u[k];
+            const int ps = meta[u[k] * 3], seq = meta[u[k] * 3 + 1], slot = meta[u[k] * 3 + 2];
+            pos[k] = ps;
+            if (ps < 0 || seq < 0) {
+              g = false;
+            } else if (inject && (seq >= e.max_batch || ps >= e.max_ctx)) {
+              set_dev_status(e.status, kDevCheck);
+              g = false;
+            } else {
+              const long long row =
+                  is_q ? (long long)t * e.H + head : kv_row(e.kp, e.Hkv, seq, head, slot);
+              if (row < 0) {
+                set_dev_status(e.status, kDevCapacity);
+                g = false;
+              } else {
+                dst[k] = base + (size_t)row * 128;
+              }
+            }
+          }
+          ok[k] = g;
+          // rotary partner: only for Q and K
+          u[UQ + k] = u[k];
+          c[UQ + k] = c[k] + 64;
+          ok[UQ + k] = g && !is_v;
+          if (g && !is_v) {
+            cs[k] = *reinterpret_cast<const float4*>(e.rcos + (size_t)pos[k] * 64 + c[k]);
+            sn[k] = *reinterpret_cast<const float4*>(e.rsin + (size_t)pos[k] * 64 + c[k]);
+          }
         }
-        const long long row = is_q ? (long long)t * e.H + head : kv_row(e.kp, e.Hkv, seq, head, slot);
-        if (row < 0) {
-          set_dev_status(e.status, kDevCapacity);
-          continue;
-        }
-        T* dst = base + (size_t)row * 128;
-        if (is_v) {
-          float4 v, unused;
-          sum4(u, c, -1, v, unused);
-          st_f4(dst + c, v);
-        } else {
-          const float4 cs = *reinterpret_cast<const float4*>(e.rcos + (size_t)pos * 64 + c);
-          const float4 sn = *reinterpret_cast<const float4*>(e.rsin + (size_t)pos * 64 + c);
-          float4 lo, hi;
-          sum4(u, c, c + 64, lo, hi);
-          st_f4(dst + c, make_float4(lo.x * cs.x - hi.x * sn.x, lo.y * cs.y - hi.y * sn.y,
-                                     lo.z * cs.z - hi.z * sn.z, lo.w * cs.w - hi.w * sn.w));
-          st_f4(dst + c + 64, make_float4(hi.x * cs.x + lo.x * sn.x, hi.y * cs.y + lo.y * sn.y,
-                                          hi.z * cs.z + lo.z * sn.z, hi.w * cs.w + lo.w * sn.w));
+        cluster_sums<S, 2 * UQ>(local, u, c, ok, v);
+#pragma unroll
+        for (int k = 0; k < UQ; ++k) {
+          if (!ok[k]) continue;
+          if (is_v) {
+            st_f4(dst[k] + c[k], v[k]);
+          } else {
+            const float4 lo = v[k], hi = v[UQ + k];
+            st_f4(dst[k] + c[k],
+                  make_float4(lo.x * cs[k].x - hi.x * sn[k].x, lo.y * cs[k].y - hi.y * sn[k].y,
+                              lo.z * cs[k].z - hi.z * sn[k].z, lo.w * cs[k].w - hi.w * sn[k].w));
+            st_f4(dst[k] + c[k] + 64,
+                  make_float4(hi.x * cs[k].x + lo.x * sn[k].x, hi.y * cs[k].y + lo.y * sn[k].y,
+                              hi.z * cs[k].z + lo.z * sn[k].z, hi.w * cs[k].w + lo.w * sn[k].w));
+          }
         }
       }
       break;
     }
     default:
       break;
+  }
+}
+
+template <typename T>
+__device__ void run_epilogue_cluster(const EpiArgs& e, int n0, int m0, int BN, const float* part,
+                                     const int32_t* meta) {
+  const int rank = (int)cluster_ctarank();
+  const uint32_t local = smem_u32(part);
+  switch (e.splits) {
+    case 1: epilogue_cluster_s<T, 1>(e, n0, m0, BN, local, meta, rank); break;
+    case 2: epilogue_cluster_s<T, 2>(e, n0, m0, BN, local, meta, rank); break;
+    case 3: epilogue_cluster_s<T, 3>(e, n0, m0, BN, local, meta, rank); break;
+    case 4: epilogue_cluster_s<T, 4>(e, n0, m0, BN, local, meta, rank); break;
+    case 5: epilogue_cluster_s<T, 5>(e, n0, m0, BN, local, meta, rank); break;
+    case 6: epilogue_cluster_s<T, 6>(e, n0, m0, BN, local, meta, rank); break;
+    case 7: epilogue_cluster_s<T, 7>(e, n0, m0, BN, local, meta, rank); break;
+    default: epilogue_cluster_s<T, 8>(e, n0, m0, BN, local, meta, rank); break;
   }
 }
 
