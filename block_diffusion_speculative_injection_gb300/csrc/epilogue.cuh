@@ -205,18 +205,21 @@ __device__ void run_epilogue(const EpiArgs& e, int n0, int m0, int BN) {
 // Epilogue straight from tensor memory, for a tile without K splits.  The
 // thread of TMEM lane f holds feature n0 + f for 16 token rows per
 // tcgen05.ld.  A warp may only read the TMEM lane quarter warp % 4, so a
-// CTA of 8 warps runs two groups of 4 warps over alternate 16-row chunks
-// (one group: all chunks); each group has its own named barrier and its own
-// exchange buffer.  QKV / INJECT rotate the pairs (f, f + 64) of a head and
+// CTA of 8 or 12 warps runs two or three groups of 4 warps over interleaved
+// 16-row chunks (one group: all chunks); each group has its own named
+// barrier and its own exchange buffer.  QKV / INJECT rotate the pairs (f, f + 64) of a head and
 // SwiGLU multiplies gate row f by up row f + 64: those partners sit in warps
 // w and w ^ 2 and trade through the group's [16][128] fp32 buffer.  Row
 // metadata (destination offset, RoPE table offset) is worked out once per
-// row before the chunks.  All of it lives in the idle stage memory: two
-// 8 KB buffers, then 256 x 8 + 256 x 4 bytes.
+// row before the chunks.  All of it lives in the idle stage memory: one
+// 8 KB buffer per group, then 256 x 8 + 256 x 4 bytes.
 // ---------------------------------------------------------------------------
+// (barrier 3 is the persistent kernel's all-epilogue barrier, so a third
+// group takes 4)
 __device__ __forceinline__ void group_bar_sync(int grp) {
   if (grp == 0) asm volatile("bar.sync 1, 128;" ::: "memory");
-  else asm volatile("bar.sync 2, 128;" ::: "memory");
+  else if (grp == 1) asm volatile("bar.sync 2, 128;" ::: "memory");
+  else asm volatile("bar.sync 4, 128;" ::: "memory");
 }
 
 // All threads that run the epilogue: the whole CTA (ep_threads == blockDim.x)
@@ -335,7 +338,7 @@ __device__ void run_epilogue_direct(const EpiArgs& e, uint32_t tmem, int n0, int
                   (inject ? (size_t)(e.layer0 + layer) * e.layer_elems : 0);
       // per tile row: element offset of its 128-wide destination row (-1:
       // nothing to write) and of its cos/sin table row (-1: no rotation)
-      long long* const s_dst = reinterpret_cast<long long*>(xbuf + 2 * 16 * 128);
+      long long* const s_dst = reinterpret_cast<long long*>(xbuf + ngrp * 16 * 128);
       int* const s_rope = reinterpret_cast<int*>(s_dst + 256);
       epi_sync_all(ep_threads);  // the previous tile's readers are done with s_dst / s_rope
       for (int u = ep_tid; u < BN; u += ep_threads) {

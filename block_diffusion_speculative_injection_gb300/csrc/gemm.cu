@@ -146,7 +146,7 @@ __device__ __forceinline__ void vocab_tile_reduce(const EpiArgs& e, const float*
   }
 }
 
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     gemm_tc_kernel(const __grid_constant__ TmapSet wmaps, const __grid_constant__ CUtensorMap xmap,
                    const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -742,8 +742,9 @@ static TcPlan plan_tc(int sm_count, int M, int N, int K, int kind, int max_split
   t.kb_per = (t.n_kb + splits - 1) / splits;
   t.splits = (t.n_kb + t.kb_per - 1) / t.kb_per;
   // tiles of more than 32 token rows hold an SM alone (shared memory): a
-  // second group of 4 warps then shares the epilogue at no occupancy cost
-  t.threads = t.BN > 32 ? 256 : 128;
+  // second group of 4 warps then shares the epilogue at no occupancy cost,
+  // and a third one for tiles of more than 128 rows
+  t.threads = t.BN > 128 ? 384 : t.BN > 32 ? 256 : 128;
   t.smem_bytes = tc_smem_bytes(t.BN, t.stages);
   // More tiles than SMs, wide token tiles and no K split: the persistent
   // form (one CTA per SM, the epilogue of a tile overlapping the next tile's

@@ -43,10 +43,10 @@ def test_qwen3_8b_one_sequence_grids(lib):
 
 def test_qwen3_8b_32_sequences_qkv(lib):
     # 512 token rows: the launch of the --set full capture (grid 48 x 2 x 1,
-    # 256 threads, 197.72 KB of dynamic shared memory)
+    # 197.72 KB of dynamic shared memory; 12 warps: three epilogue groups)
     p = capi.dflash_plan_gemm(GB300_SMS, 512, 6144, 4096, QKV)
     assert grid(p) == (48, 2, 1)
-    assert (p["BN"], p["threads"], p["smem_bytes"]) == (256, 256, 197720)
+    assert (p["BN"], p["threads"], p["smem_bytes"]) == (256, 384, 197720)
     # O and down (32 feature tiles) would fill 64 SMs: two K splits per tile
     assert grid(capi.dflash_plan_gemm(GB300_SMS, 512, 4096, 4096, RESID)) == (32, 2, 2)
     assert grid(capi.dflash_plan_gemm(GB300_SMS, 512, 4096, 12288, RESID)) == (32, 2, 2)
@@ -79,13 +79,13 @@ def test_gemm_plan_rules(lib, sms):
             # ring + the epilogue's own scratch (two 16 x 128 fp32 buffers, 256 x 12 B)
             assert smem >= st * (128 * 64 * 2 + BN * 64 * 2) + 2 * 16 * 128 * 4 + 256 * 12
         else:
-            assert th == (256 if BN > 32 else 128)
+            assert th == (384 if BN > 128 else 256 if BN > 32 else 128)
             assert smem <= 210 * 1024  # the kernel's shared-memory attribute
         stage_mem = st * (128 * 64 * 2 + BN * 64 * 2)
-        # direct epilogue: two 16 x 128 fp32 exchange buffers, then 256 x 8 B
-        # destination offsets and 256 x 4 B RoPE offsets, in stage memory
-        # (or, persistent, in memory of their own)
-        assert 2 * 16 * 128 * 4 + 256 * 8 + 256 * 4 <= stage_mem or pers
+        # direct epilogue: one 16 x 128 fp32 exchange buffer per group of 128
+        # threads, then 256 x 8 B destination offsets and 256 x 4 B RoPE
+        # offsets, in stage memory (or, persistent, in memory of their own)
+        assert (th // 128) * 16 * 128 * 4 + 256 * 8 + 256 * 4 <= stage_mem or pers
         # a split tile's fp32 partial [BN][128] sits in its own stage memory
         if sp > 1:
             assert BN * 128 * 4 <= stage_mem
