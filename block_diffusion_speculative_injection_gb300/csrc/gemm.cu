@@ -913,10 +913,14 @@ dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs&
   DF_CUDA_TRY(ctx, ensure_tc_smem());
   dim3 grid(m_tiles, n_tiles, splits);
   const size_t smem_bytes = plan.smem_bytes;
-  const dim3 cluster(1, 1, splits);
   const dim3 block(plan.threads);
-  DF_CUDA_TRY(ctx, launch_k_cluster(ctx->pdl, cluster, gemm_tc_kernel, grid, block, smem_bytes,
-                                    st, maps, *xm, p));
+  // the K splits of a tile form a cluster; an unsplit launch needs none
+  if (splits > 1) {
+    DF_CUDA_TRY(ctx, launch_k_cluster(ctx->pdl, dim3(1, 1, splits), gemm_tc_kernel, grid, block,
+                                      smem_bytes, st, maps, *xm, p));
+  } else {
+    DF_CUDA_TRY(ctx, launch_k(ctx->pdl, gemm_tc_kernel, grid, block, smem_bytes, st, maps, *xm, p));
+  }
   DF_LAUNCHED(ctx);
   *splits_used = splits;
   return DFLASH_OK;
