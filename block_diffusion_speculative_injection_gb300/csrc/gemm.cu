@@ -704,12 +704,10 @@ static cudaError_t ensure_persist_smem() {
   return ensure_smem_attr(done, gemm_tc_persistent_kernel, (int)kPersistSmemMax);
 }
 
-static TcPlan plan_tc(int sm_count, int M, int N, int K, int kind, int max_splits) {
+// the plan for a given number of token tiles
+static TcPlan plan_tiles(int sm_count, int M, int N, int K, int kind, int max_splits, int m_tiles) {
   TcPlan t;
-  // Token tiles as wide as the MMA allows: a 64-column K block takes about
-  // the same time at 80, 128, 144 or 256 token rows, so a pass that leaves
-  // SMs idle is split along K (below) rather than cut into narrower tiles.
-  t.m_tiles = (M + 255) / 256;
+  t.m_tiles = m_tiles;
   int BN = (M + t.m_tiles - 1) / t.m_tiles;
   BN = ((BN + 15) / 16) * 16;
   t.BN = BN < 16 ? 16 : BN;
@@ -761,6 +759,23 @@ static TcPlan plan_tc(int sm_count, int M, int N, int K, int kind, int max_split
     if (st > 8) st = 8;
     t.stages = st;
     t.smem_bytes = persist_smem_bytes(t.BN, st);
+  }
+  return t;
+}
+
+static TcPlan plan_tc(int sm_count, int M, int N, int K, int kind, int max_splits) {
+  // Token tiles as wide as the MMA allows: a 64-column K block takes about
+  // the same time at 80, 128, 144 or 256 token rows, so a pass that leaves
+  // SMs idle is split along K rather than cut into narrower tiles.  A pass
+  // that K splits cannot spread within one wave (a single split) takes more,
+  // narrower token tiles while they still fit one wave: each CTA keeps its
+  // main loop and gets a shorter epilogue (QKV at 512 rows: three tiles of
+  // 176 rows on 144 SMs instead of two of 256 on 96).
+  TcPlan t = plan_tiles(sm_count, M, N, K, kind, max_splits, (M + 255) / 256);
+  if (t.splits == 1 && t.persistent == 0 && t.m_tiles > 1 && kind != kEpiSlab && kind != kEpiVocab) {
+    int m = t.m_tiles;
+    while ((int64_t)t.n_tiles * (m + 1) <= sm_count && (M + m) / (m + 1) > 48) ++m;  // >= 64-row tiles
+    if (m > t.m_tiles) t = plan_tiles(sm_count, M, N, K, kind, max_splits, m);
   }
   return t;
 }

@@ -42,11 +42,11 @@ def test_qwen3_8b_one_sequence_grids(lib):
 
 
 def test_qwen3_8b_32_sequences_qkv(lib):
-    # 512 token rows: the launch of the --set full capture (grid 48 x 2 x 1,
-    # 197.72 KB of dynamic shared memory; 12 warps: three epilogue groups)
+    # 512 token rows: QKV (48 feature tiles, unsplit) takes three 176-row
+    # token tiles on 144 SMs
     p = capi.dflash_plan_gemm(GB300_SMS, 512, 6144, 4096, QKV)
-    assert grid(p) == (48, 2, 1)
-    assert (p["BN"], p["threads"], p["smem_bytes"]) == (256, 384, 197720)
+    assert grid(p) == (48, 3, 1)
+    assert (p["BN"], p["threads"]) == (176, 384)
     # O and down (32 feature tiles) would fill 64 SMs: two K splits per tile
     assert grid(capi.dflash_plan_gemm(GB300_SMS, 512, 4096, 4096, RESID)) == (32, 2, 2)
     assert grid(capi.dflash_plan_gemm(GB300_SMS, 512, 4096, 12288, RESID)) == (32, 2, 2)
@@ -66,8 +66,14 @@ def test_gemm_plan_rules(lib, sms):
         p = capi.dflash_plan_gemm(sms, M, N, K, kind)
         BN, mt, nt, st, sp, th, smem = (p[k] for k in ("BN", "m_tiles", "n_tiles", "stages",
                                                        "splits", "threads", "smem_bytes"))
-        # token tiles as wide as the MMA allows
-        assert BN % 16 == 0 and 16 <= BN <= 256 and BN * mt >= M and mt == (M + 255) // 256
+        # token tiles as wide as the MMA allows; an unsplit pass that leaves
+        # SMs idle takes more (of at least 64 rows) while they fit one wave
+        mt0 = (M + 255) // 256
+        assert BN % 16 == 0 and 16 <= BN <= 256 and BN * mt >= M and mt >= mt0
+        if mt > mt0:
+            assert sp == 1 and not p["persistent"] and kind not in (SLAB, VOCAB) and mt0 > 1
+            assert nt * mt <= sms and BN >= 64
+            assert nt * (mt + 1) > sms or -(-M // (mt + 1)) <= 48
         assert nt == (N + 127) // 128
         assert 2 <= st <= 8
         pers = p["persistent"]
