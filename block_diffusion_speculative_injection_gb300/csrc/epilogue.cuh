@@ -275,29 +275,34 @@ __device__ void run_epilogue_direct(const EpiArgs& e, uint32_t tmem, int n0, int
       break;
     }
     case kEpiSwiGLU: {
-      // lanes 0..63: gate of features n0 + f; lanes 64..127: up of n0 + f - 64
+      // lanes 0..63: gate of features n0 + f; lanes 64..127: up of n0 + f - 64.
+      // Of each 16-row chunk the gate thread finishes rows 0..7 and the up
+      // thread rows 8..15: each hands its partner (lane f ^ 64) the 8 values
+      // the partner needs, through one of two alternating 8 x 128 halves of
+      // the group's buffer (a half is rewritten two chunks later, after the
+      // partner's read has passed the next chunk's barrier).
       T* const act = static_cast<T*>(e.act);
       const int F = e.F;
-      for (int c = c0; c < BN; c += cstep) {
+      const bool is_gate = f < 64;
+      const int keep = is_gate ? 0 : 8;
+      int parity = 0;
+      for (int c = c0; c < BN; c += cstep, parity ^= 1) {
         float v[16];
         tmem_ld16(taddr + (uint32_t)c, v);
+        float* const xh = xb + parity * 8 * 128;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) xb[i * 128 + f] = v[i];
+        for (int i = 0; i < 8; ++i) xh[i * 128 + f] = is_gate ? v[8 + i] : v[i];
         group_bar_sync(grp);
-        if (f < 64) {
-          float up[16];
+        float other[8];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) up[i] = xb[i * 128 + f + 64];
-          group_bar_sync(grp);  // xb may be rewritten by the next chunk
+        for (int i = 0; i < 8; ++i) other[i] = xh[i * 128 + (f ^ 64)];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int t = m0 + c + i;
-            if (t >= M) continue;
-            const float g = v[i];
-            st_f(act + (size_t)t * F + n0 + f, g / (1.f + __expf(-g)) * up[i]);
-          }
-        } else {
-          group_bar_sync(grp);
+        for (int i = 0; i < 8; ++i) {
+          const int t = m0 + c + keep + i;
+          if (t >= M) continue;
+          const float g = is_gate ? v[i] : other[i];
+          const float u = is_gate ? other[i] : v[8 + i];
+          st_f(act + (size_t)t * F + n0 + (f & 63), g / (1.f + __expf(-g)) * u);
         }
       }
       break;
