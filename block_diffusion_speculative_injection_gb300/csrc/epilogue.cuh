@@ -375,49 +375,60 @@ __device__ void run_epilogue_direct(const EpiArgs& e, uint32_t tmem, int n0, int
       const float* const rsin = e.rsin;
       const int j = f & 63;
       const bool low = f < 64;
-      // cos/sin of a chunk's rows, loaded one chunk ahead so that their
-      // latency overlaps the previous chunk's exchange and stores
-      float cs[16], sn[16], cs_n[16], sn_n[16];
+      if (is_v) {
+        for (int c = c0; c < BN; c += cstep) {
+          float v[16];
+          tmem_ld16(taddr + (uint32_t)c, v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const long long off = s_dst[c + i];
+            if (off >= 0) st_f(base + off + f, v[i]);
+          }
+        }
+        break;
+      }
+      // Q and K: of each 16-row chunk the thread of feature j (low) rotates
+      // rows 0..7 and the thread of feature j + 64 rows 8..15, writing both
+      // features of the pair; each hands its partner (lane f ^ 64) the 8
+      // values the partner needs through one of two alternating 8 x 128
+      // halves of the group's buffer (a half is rewritten two chunks later,
+      // after the partner's read has passed the next chunk's barrier).  The
+      // cos/sin of a thread's 8 rows load one chunk ahead.
+      const int keep = low ? 0 : 8;
+      float cs[8], sn[8], cs_n[8], sn_n[8];
       auto load_rope = [&](int c, float* cn, float* snn) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int ro = s_rope[c + i];
+        for (int i = 0; i < 8; ++i) {
+          const int ro = s_rope[c + keep + i];
           cn[i] = ro >= 0 ? rcos[ro + j] : 1.f;
           snn[i] = ro >= 0 ? rsin[ro + j] : 0.f;
         }
       };
-      if (!is_v && c0 < BN) load_rope(c0, cs_n, sn_n);
-      for (int c = c0; c < BN; c += cstep) {
+      if (c0 < BN) load_rope(c0, cs_n, sn_n);
+      int parity = 0;
+      for (int c = c0; c < BN; c += cstep, parity ^= 1) {
         float v[16];
         tmem_ld16(taddr + (uint32_t)c, v);
-        float y[16];
-        if (!is_v) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            cs[i] = cs_n[i];
-            sn[i] = sn_n[i];
-          }
-          if (c + cstep < BN) load_rope(c + cstep, cs_n, sn_n);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) xb[i * 128 + f] = v[i];
-          group_bar_sync(grp);
-          float other[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) other[i] = xb[i * 128 + (f ^ 64)];
-          group_bar_sync(grp);  // xb may be rewritten by the next chunk
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float lo = low ? v[i] : other[i], hi = low ? other[i] : v[i];
-            y[i] = low ? lo * cs[i] - hi * sn[i] : hi * cs[i] + lo * sn[i];
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) y[i] = v[i];
+        for (int i = 0; i < 8; ++i) {
+          cs[i] = cs_n[i];
+          sn[i] = sn_n[i];
         }
+        if (c + cstep < BN) load_rope(c + cstep, cs_n, sn_n);
+        float* const xh = xb + parity * 8 * 128;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const long long off = s_dst[c + i];
-          if (off >= 0) st_f(base + off + f, y[i]);
+        for (int i = 0; i < 8; ++i) xh[i * 128 + f] = low ? v[8 + i] : v[i];
+        group_bar_sync(grp);
+        float other[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) other[i] = xh[i * 128 + (f ^ 64)];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const long long off = s_dst[c + keep + i];
+          if (off < 0) continue;
+          const float lo = low ? v[i] : other[i], hi = low ? other[i] : v[8 + i];
+          st_f(base + off + j, lo * cs[i] - hi * sn[i]);
+          st_f(base + off + j + 64, hi * cs[i] + lo * sn[i]);
         }
       }
       break;
