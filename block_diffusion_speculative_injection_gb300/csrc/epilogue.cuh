@@ -209,7 +209,8 @@ __device__ void run_epilogue(const EpiArgs& e, int n0, int m0, int BN) {
 // 16-row chunks (one group: all chunks); each group has its own named
 // barrier and its own exchange buffer.  QKV / INJECT rotate the pairs (f, f + 64) of a head and
 // SwiGLU multiplies gate row f by up row f + 64: those partners sit in warps
-// w and w ^ 2 and trade through the group's [16][128] fp32 buffer.  Row
+// w and w ^ 2, split each chunk's rows between them and trade through the
+// two [8][128] fp32 halves of the group's buffer.  Row
 // metadata (destination offset, RoPE table offset) is worked out once per
 // row before the chunks.  All of it lives in the idle stage memory: one
 // 8 KB buffer per group, then 256 x 8 + 256 x 4 bytes.
