@@ -515,7 +515,7 @@ def run_ours(args, w: wl.Workload) -> None:
     print(json.dumps(line))
 
 
-KERNEL_REV = "gemm-v8"  # vocabulary epilogue, token-tile-first grid, persistent form, batched cluster epilogue, 12 warps above 128 rows
+KERNEL_REV = "gemm-v9"  # vocabulary epilogue, token-tile-first grid, persistent form, batched cluster epilogue, 12 warps above 128 rows, split-chunk pair epilogues
 ATTN_KERNELS = "attn_tc_kernel (+ attn_combine_kernel)"
 
 
