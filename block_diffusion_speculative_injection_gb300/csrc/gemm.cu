@@ -668,11 +668,19 @@ static dflash_status get_tmap(dflash_ctx* ctx, const void* ptr, int64_t rows, in
 
 static size_t tc_smem_bytes(int BN, int stages);
 
+// Token rows up to which a tile streams weights (about 2 x rows flops per
+// weight byte, far under the machine balance): such tiles run 4 warps, 2
+// CTAs per SM, with a 110 KB ring each.
+constexpr int kSmallTileRows = 64;
+
 static int tc_stages(int BN) {
   const int per = 128 * 64 * 2 + BN * 64 * 2;
-  // small tiles: 2 CTAs per SM (a third, left for the next launch's weight
-  // prefetch, measured slower: its 3 stages per CTA hold too little in flight)
-  int budget = (BN <= 32) ? 110 * 1024 : 200 * 1024;
+  // tiles of up to kSmallTileRows token rows stream weights: 2 CTAs per SM
+  // (a third, left for the next launch's weight prefetch, measured slower:
+  // its 3 stages per CTA hold too little in flight)
+  // (108 KB of ring: two CTAs, each with its alignment pad, barriers, 3 KB
+  // of static shared memory and the 1 KB per-CTA reserve, fit in 228 KB)
+  int budget = (BN <= kSmallTileRows) ? 108 * 1024 : 200 * 1024;
   int s = budget / per;
   if (s > 8) s = 8;
   if (s < 2) s = 2;
@@ -717,7 +725,7 @@ static TcPlan plan_tiles(int sm_count, int M, int N, int K, int kind, int max_sp
   const int ctas = t.n_tiles * t.m_tiles;
   // K splits: as many as fit in ONE wave of resident CTAs (a partial second
   // wave would double the latency of these short, bandwidth-bound launches)
-  const int per_sm = (t.BN <= 32) ? 2 : 1;
+  const int per_sm = (t.BN <= kSmallTileRows) ? 2 : 1;
   const int slots = per_sm * sm_count;
   int splits = ctas >= slots ? 1 : slots / ctas;
   // the K splits of a tile form one thread-block cluster (portable size <= 8);
@@ -739,10 +747,10 @@ static TcPlan plan_tiles(int sm_count, int M, int N, int K, int kind, int max_sp
     splits = 1;
   t.kb_per = (t.n_kb + splits - 1) / splits;
   t.splits = (t.n_kb + t.kb_per - 1) / t.kb_per;
-  // tiles of more than 32 token rows hold an SM alone (shared memory): a
+  // tiles of more than kSmallTileRows token rows hold an SM alone (shared memory): a
   // second group of 4 warps then shares the epilogue at no occupancy cost,
   // and a third one for tiles of more than 128 rows
-  t.threads = t.BN > 128 ? 384 : t.BN > 32 ? 256 : 128;
+  t.threads = t.BN > 128 ? 384 : t.BN > kSmallTileRows ? 256 : 128;
   t.smem_bytes = tc_smem_bytes(t.BN, t.stages);
   // More tiles than SMs, wide token tiles and no K split: the persistent
   // form (one CTA per SM, the epilogue of a tile overlapping the next tile's
