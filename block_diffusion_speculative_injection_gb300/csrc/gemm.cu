@@ -668,10 +668,11 @@ static dflash_status get_tmap(dflash_ctx* ctx, const void* ptr, int64_t rows, in
 
 static size_t tc_smem_bytes(int BN, int stages);
 
-// Token rows up to which a tile streams weights (about 2 x rows flops per
-// weight byte, far under the machine balance): such tiles run 4 warps, 2
-// CTAs per SM, with a 110 KB ring each.
-constexpr int kSmallTileRows = 64;
+// Token rows up to which tiles run 4 warps, 2 CTAs per SM, with a 108 KB
+// ring each (about 2 x rows flops per weight byte: at or under the machine
+// balance; measured at 64 and 128 rows against one CTA per SM with a 200 KB
+// ring and 8 warps).  Wider tiles hold an SM alone with 12 warps.
+constexpr int kSmallTileRows = 128;
 
 static int tc_stages(int BN) {
   const int per = 128 * 64 * 2 + BN * 64 * 2;
@@ -747,10 +748,9 @@ static TcPlan plan_tiles(int sm_count, int M, int N, int K, int kind, int max_sp
     splits = 1;
   t.kb_per = (t.n_kb + splits - 1) / splits;
   t.splits = (t.n_kb + t.kb_per - 1) / t.kb_per;
-  // tiles of more than kSmallTileRows token rows hold an SM alone (shared memory): a
-  // second group of 4 warps then shares the epilogue at no occupancy cost,
-  // and a third one for tiles of more than 128 rows
-  t.threads = t.BN > 128 ? 384 : t.BN > kSmallTileRows ? 256 : 128;
+  // tiles of more than kSmallTileRows token rows hold an SM alone (shared
+  // memory): three groups of 4 warps share the epilogue at no occupancy cost
+  t.threads = t.BN > kSmallTileRows ? 384 : 128;
   t.smem_bytes = tc_smem_bytes(t.BN, t.stages);
   // More tiles than SMs, wide token tiles and no K split: the persistent
   // form (one CTA per SM, the epilogue of a tile overlapping the next tile's

@@ -85,8 +85,8 @@ def test_gemm_plan_rules(lib, sms):
             # ring + the epilogue's own scratch (two 16 x 128 fp32 buffers, 256 x 12 B)
             assert smem >= st * (128 * 64 * 2 + BN * 64 * 2) + 2 * 16 * 128 * 4 + 256 * 12
         else:
-            assert th == (384 if BN > 128 else 256 if BN > 64 else 128)
-            if BN <= 64:  # two CTAs per SM: dynamic + 3 KB static + 1 KB reserve each
+            assert th == (384 if BN > 128 else 128)
+            if BN <= 128:  # two CTAs per SM: dynamic + 3 KB static + 1 KB reserve each
                 assert 2 * (smem + 3072 + 1024) <= 228 * 1024
             assert smem <= 210 * 1024  # the kernel's shared-memory attribute
         stage_mem = st * (128 * 64 * 2 + BN * 64 * 2)
@@ -100,7 +100,7 @@ def test_gemm_plan_rules(lib, sms):
         assert 1 <= sp <= 8 and sp <= K // 64 // 4 or sp == 1
         if kind in (SWIGLU, SLAB, VOCAB):
             assert sp == 1
-        slots = (2 if BN <= 64 else 1) * sms
+        slots = (2 if BN <= 128 else 1) * sms
         if sp > 1:
             assert nt * mt * sp * 8 <= 7 * slots  # every cluster resident at once
         # a grid that fills under half of the CTA slots is split along K when
