@@ -233,6 +233,55 @@ __device__ __forceinline__ void epi_sync_all(int ep_threads) {
 // ep_tid / ep_threads: this thread's index among the threads that run the
 // epilogue, and their count (a multiple of 128); a warp reads the TMEM lane
 // quarter of its hardware warp index.
+// Top-2 lists (value descending, id ascending; empty slots are (-inf,
+// INT_MAX)): merge list B into list A.  The order is total, so the merged
+// list is the top 2 of the union whatever the merge order.
+__device__ __forceinline__ bool top_better(float x, int xi, float y, int yi) {
+  return x > y || (x == y && xi < yi);
+}
+__device__ __forceinline__ void top2_merge(float& a1, int& j1, float& a2, int& j2, float b1, int k1,
+                                           float b2, int k2) {
+  if (top_better(b1, k1, a1, j1)) {
+    if (top_better(a1, j1, b2, k2)) {
+      a2 = a1;
+      j2 = j1;
+    } else {
+      a2 = b2;
+      j2 = k2;
+    }
+    a1 = b1;
+    j1 = k1;
+  } else if (top_better(b1, k1, a2, j2)) {
+    a2 = b1;
+    j2 = k1;
+  }
+}
+
+// One halving round of a warp's top-2 reduce-scatter over R rows: lanes l
+// and l ^ off trade lists; the lane with bit `off` set keeps rows R/2 .. R-1
+// (the other rows 0 .. R/2-1) and merges the partner's lists for them.
+template <int R>
+__device__ __forceinline__ void top2_halve(const float (&a1)[R], const int (&j1)[R],
+                                           const float (&a2)[R], const int (&j2)[R],
+                                           float (&b1)[R / 2], int (&k1)[R / 2],
+                                           float (&b2)[R / 2], int (&k2)[R / 2], int lane, int off) {
+  const bool hi = (lane & off) != 0;
+#pragma unroll
+  for (int i = 0; i < R / 2; ++i) {
+    const float s1 = hi ? a1[i] : a1[R / 2 + i], s2 = hi ? a2[i] : a2[R / 2 + i];
+    const int t1 = hi ? j1[i] : j1[R / 2 + i], t2 = hi ? j2[i] : j2[R / 2 + i];
+    const float r1 = __shfl_xor_sync(0xffffffffu, s1, off);
+    const int q1 = __shfl_xor_sync(0xffffffffu, t1, off);
+    const float r2 = __shfl_xor_sync(0xffffffffu, s2, off);
+    const int q2 = __shfl_xor_sync(0xffffffffu, t2, off);
+    b1[i] = hi ? a1[R / 2 + i] : a1[i];
+    k1[i] = hi ? j1[R / 2 + i] : j1[i];
+    b2[i] = hi ? a2[R / 2 + i] : a2[i];
+    k2[i] = hi ? j2[R / 2 + i] : j2[i];
+    top2_merge(b1[i], k1[i], b2[i], k2[i], r1, q1, r2, q2);
+  }
+}
+
 template <typename T>
 __device__ void run_epilogue_direct(const EpiArgs& e, uint32_t tmem, int n0, int m0, int BN,
                                     float* xbuf, int ep_tid, int ep_threads) {
@@ -431,6 +480,71 @@ __device__ void run_epilogue_direct(const EpiArgs& e, uint32_t tmem, int n0, int
           st_f(base + off + j, lo * cs[i] - hi * sn[i]);
           st_f(base + off + j + 64, hi * cs[i] + lo * sn[i]);
         }
+      }
+      break;
+    }
+    case kEpiVocab: {
+      // lm_head with K = 2 (argmax and margin; no log-sum-exp, no logits):
+      // per token row, the top 2 of the tile's 128 ids (value descending, id
+      // ascending; NaN and -inf never enter), which is what a scan of the ids
+      // in order with strict comparisons keeps.  Per 16-row chunk a warp
+      // reduce-scatters its 32 lanes' lists (five shuffle rounds, each
+      // halving the rows a lane keeps, the last a full exchange): lane l ends
+      // with row l / 2; then a warp of lane quarter 0 merges the four
+      // quarters' lists through the group's buffer.
+      const int nf = min(128, e.N - n0), nvt = (e.N + 127) / 128, vt = n0 / 128;
+      const bool fvalid = f < nf;
+      const int fid = n0 + f;
+      float4* const sc = reinterpret_cast<float4*>(xb);  // [16 rows][4 quarters]
+      for (int c = c0; c < BN; c += cstep) {
+        float v[16];
+        tmem_ld16(taddr + (uint32_t)c, v);
+        float a1[16], a2[16];
+        int j1[16], j2[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const bool ok = fvalid && v[i] > -INFINITY;
+          a1[i] = ok ? v[i] : -INFINITY;
+          j1[i] = ok ? fid : INT_MAX;
+          a2[i] = -INFINITY;
+          j2[i] = INT_MAX;
+        }
+        float b1[8], b2[8], d1[4], d2[4], g1[2], g2[2], h1[1], h2[1];
+        int k1[8], k2[8], e1[4], e2[4], m1[2], m2[2], n1[1], n2[1];
+        top2_halve<16>(a1, j1, a2, j2, b1, k1, b2, k2, lane, 16);
+        top2_halve<8>(b1, k1, b2, k2, d1, e1, d2, e2, lane, 8);
+        top2_halve<4>(d1, e1, d2, e2, g1, m1, g2, m2, lane, 4);
+        top2_halve<2>(g1, m1, g2, m2, h1, n1, h2, n2, lane, 2);
+        {
+          const float r1 = __shfl_xor_sync(0xffffffffu, h1[0], 1);
+          const int q1 = __shfl_xor_sync(0xffffffffu, n1[0], 1);
+          const float r2 = __shfl_xor_sync(0xffffffffu, h2[0], 1);
+          const int q2 = __shfl_xor_sync(0xffffffffu, n2[0], 1);
+          top2_merge(h1[0], n1[0], h2[0], n2[0], r1, q1, r2, q2);
+        }
+        if ((lane & 1) == 0)
+          sc[(lane >> 1) * 4 + quarter] =
+              make_float4(h1[0], __int_as_float(n1[0]), h2[0], __int_as_float(n2[0]));
+        group_bar_sync(grp);
+        if (quarter == 0 && lane < 16) {
+          const int t = m0 + c + lane;
+          float4 q = sc[lane * 4];
+          float x1 = q.x, x2 = q.z;
+          int y1 = __float_as_int(q.y), y2 = __float_as_int(q.w);
+#pragma unroll
+          for (int w = 1; w < 4; ++w) {
+            q = sc[lane * 4 + w];
+            top2_merge(x1, y1, x2, y2, q.x, __float_as_int(q.y), q.z, __float_as_int(q.w));
+          }
+          if (t < M) {
+            const size_t pb = (size_t)t * nvt + vt;
+            e.vr_id[pb * 2] = y1;
+            e.vr_id[pb * 2 + 1] = y2;
+            e.vr_v[pb * 2] = x1;
+            e.vr_v[pb * 2 + 1] = x2;
+          }
+        }
+        group_bar_sync(grp);  // sc is rewritten by the next chunk
       }
       break;
     }

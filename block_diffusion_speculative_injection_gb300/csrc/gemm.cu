@@ -674,6 +674,12 @@ static size_t tc_smem_bytes(int BN, int stages);
 // ring and 8 warps).  Wider tiles hold an SM alone with 12 warps.
 constexpr int kSmallTileRows = 128;
 
+// Planning kind of an lm_head whose epilogue keeps the top 2 per row and
+// 128-id tile and nothing else (no log-sum-exp, no logits): its reduction
+// runs from tensor memory in registers, so it may take the persistent form,
+// where the reduction of one tile overlaps the next tile's main loop.
+constexpr int kPlanVocabTop2 = 7;
+
 static int tc_stages(int BN) {
   const int per = 128 * 64 * 2 + BN * 64 * 2;
   // tiles of up to kSmallTileRows token rows stream weights: 2 CTAs per SM
@@ -735,7 +741,7 @@ static TcPlan plan_tiles(int sm_count, int M, int N, int K, int kind, int max_sp
   if (splits > max_cluster_splits) splits = max_cluster_splits;
   if (splits > max_splits) splits = max_splits;
   if (splits > t.n_kb / 4) splits = t.n_kb / 4;
-  if (splits < 1 || kind == kEpiSlab || kind == kEpiVocab) splits = 1;
+  if (splits < 1 || kind == kEpiSlab || kind == kEpiVocab || kind == kPlanVocabTop2) splits = 1;
   // ... and every cluster of the launch resident at once: clusters that wait
   // for a second wave double the launch time.  A cluster sits inside one GPC,
   // so fewer than slots / size clusters fit; on GB300 (152 SMs, 2 CTAs per
@@ -754,8 +760,9 @@ static TcPlan plan_tiles(int sm_count, int M, int N, int K, int kind, int max_sp
   t.smem_bytes = tc_smem_bytes(t.BN, t.stages);
   // More tiles than SMs, wide token tiles and no K split: the persistent
   // form (one CTA per SM, the epilogue of a tile overlapping the next tile's
-  // main loop).  The lm_head's vocabulary epilogue stages its tile in the
-  // ring's memory, so it keeps one CTA per tile.
+  // main loop).  The lm_head's general vocabulary epilogue stages its tile
+  // in the ring's memory, so it keeps one CTA per tile; the top-2 one does
+  // not (kPlanVocabTop2).
   t.persistent = 0;
   if (t.splits == 1 && t.BN > 64 && kind != kEpiSlab && kind != kEpiVocab &&
       (int64_t)t.n_tiles * t.m_tiles > sm_count) {
@@ -780,7 +787,8 @@ static TcPlan plan_tc(int sm_count, int M, int N, int K, int kind, int max_split
   // main loop and gets a shorter epilogue (QKV at 512 rows: three tiles of
   // 176 rows on 144 SMs instead of two of 256 on 96).
   TcPlan t = plan_tiles(sm_count, M, N, K, kind, max_splits, (M + 255) / 256);
-  if (t.splits == 1 && t.persistent == 0 && t.m_tiles > 1 && kind != kEpiSlab && kind != kEpiVocab) {
+  if (t.splits == 1 && t.persistent == 0 && t.m_tiles > 1 && kind != kEpiSlab && kind != kEpiVocab &&
+      kind != kPlanVocabTop2) {
     int m = t.m_tiles;
     while ((int64_t)t.n_tiles * (m + 1) <= sm_count && (M + m) / (m + 1) > 48) ++m;  // >= 64-row tiles
     if (m > t.m_tiles) t = plan_tiles(sm_count, M, N, K, kind, max_splits, m);
@@ -790,7 +798,7 @@ static TcPlan plan_tc(int sm_count, int M, int N, int K, int kind, int max_split
 
 dflash_status plan_gemm(int sm_count, int M, int N, int K, int kind, int max_splits, int32_t* out) {
   if (!out || sm_count < 1 || M < 1 || N < 1 || K < 64 || K % 64 != 0 || max_splits < 1 ||
-      kind < kEpiSlab || kind > kEpiVocab || (kind == kEpiSwiGLU && N % 128 != 0))
+      kind < kEpiSlab || kind > kPlanVocabTop2 || (kind == kEpiSwiGLU && N % 128 != 0))
     return DFLASH_E_INVALID_ARG;
   const TcPlan t = plan_tc(sm_count, M, N, K, kind, max_splits);
   out[0] = t.BN;
@@ -867,7 +875,10 @@ dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs&
       set_error(ctx, "GEMM segment %d has %d rows (not a multiple of 128)", i, segs.rows[i]);
       return DFLASH_E_UNSUPPORTED;
     }
-  const TcPlan plan = plan_tc(ctx->sm_count, M, N, K, epi_in.kind, max_splits);
+  const bool vocab_top2 = epi_in.kind == kEpiVocab && epi_in.vr_k == 2 && !epi_in.vr_lse &&
+                          !epi_in.vr_logits;
+  const TcPlan plan =
+      plan_tc(ctx->sm_count, M, N, K, vocab_top2 ? kPlanVocabTop2 : epi_in.kind, max_splits);
   const int m_tiles = plan.m_tiles, BN = plan.BN, stages = plan.stages, n_tiles = plan.n_tiles;
   const int n_kb = plan.n_kb;
   const int kb_per = plan.kb_per;
@@ -879,7 +890,8 @@ dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs&
   if (epi_in.kind == kEpiVocab &&
       (epi_in.vr_k < 2 || epi_in.vr_k > 16 || !epi_in.vr_id || !epi_in.vr_v ||
        (epi_in.vr_logits && !epi_in.vr_vec) ||
-       (size_t)128 * (BN + 1) * sizeof(float) > (size_t)stages * (128 * 64 * 2 + BN * 64 * 2))) {
+       (plan.persistent == 0 &&
+        (size_t)128 * (BN + 1) * sizeof(float) > (size_t)stages * (128 * 64 * 2 + BN * 64 * 2)))) {
     set_error(ctx, "lm_head reduction: bad candidate count or buffers");
     return DFLASH_E_INVALID_ARG;
   }

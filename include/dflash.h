@@ -528,7 +528,10 @@ DFLASH_API int64_t dflash_profile_list(dflash_ctx *ctx, int32_t kind, double *ms
  * Tensor-core GEMM of M token rows by an N x K weight (K a multiple of 64)
  * on a GPU with sm_count SMs.  kind: 0 fp32 result, 1 QKV, 2 SwiGLU
  * (N = gate rows + up rows, a multiple of 128), 3 residual add, 4 store,
- * 5 injected K/V, 6 lm_head with the vocabulary reduction in the epilogue.
+ * 5 injected K/V, 6 lm_head with the vocabulary reduction in the epilogue, 7 an
+ * lm_head whose reduction keeps the top 2 per row only (no log-sum-exp, no
+ * logits), which reduces from tensor memory in registers and so may take the
+ * persistent form.
  * max_splits caps the K split.  plan_out[8] receives:
  * token rows per tile, token-row tiles, 128-row weight tiles, pipeline stages,
  * K splits (= thread-block cluster size), threads per CTA, dynamic shared
@@ -536,7 +539,7 @@ DFLASH_API int64_t dflash_profile_list(dflash_ctx *ctx, int32_t kind, double *ms
  * CTA of its own; else one CTA per SM walks the tiles, with the epilogue of a
  * tile overlapping the next tile's main loop: passes of more tiles than SMs
  * with tiles wider than 64 token rows, no K split, and any epilogue but the
- * lm_head's).  DFLASH_E_INVALID_ARG for sizes the GEMM does not take. */
+ * general lm_head's, kind 6).  DFLASH_E_INVALID_ARG for sizes the GEMM does not take. */
 DFLASH_API dflash_status dflash_plan_gemm(int32_t sm_count, int32_t M, int32_t N, int32_t K,
                                           int32_t kind, int32_t max_splits, int32_t *plan_out);
 

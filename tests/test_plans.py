@@ -11,7 +11,7 @@ import pytest
 
 from block_diffusion_speculative_injection_gb300 import capi
 
-QKV, SWIGLU, RESID, SLAB, VOCAB = 1, 2, 3, 0, 6
+QKV, SWIGLU, RESID, SLAB, VOCAB, VOCAB_TOP2 = 1, 2, 3, 0, 6, 7
 GB300_SMS = 152
 
 
@@ -34,6 +34,9 @@ def test_qwen3_8b_one_sequence_grids(lib):
     assert grid(capi.dflash_plan_gemm(GB300_SMS, 16, 4096, 12288, RESID)) == (32, 1, 8)
     assert grid(capi.dflash_plan_gemm(GB300_SMS, 16, 2 * 12288, 4096, SWIGLU)) == (192, 1, 1)
     assert grid(capi.dflash_plan_gemm(GB300_SMS, 16, 151936, 4096, SLAB)) == (1187, 1, 1)
+    # the lm_head with its top-2 reduction in registers: persistent at 512 rows
+    p = capi.dflash_plan_gemm(GB300_SMS, 512, 151936, 4096, VOCAB_TOP2)
+    assert (grid(p), p["persistent"]) == ((1187, 2, 1), GB300_SMS)
     # the lm_head with its vocabulary reduction: one CTA per 128 ids, no K split
     assert grid(capi.dflash_plan_gemm(GB300_SMS, 16, 151936, 4096, VOCAB)) == (1187, 1, 1)
     assert grid(capi.dflash_plan_gemm(GB300_SMS, 512, 151936, 4096, VOCAB)) == (1187, 2, 1)
@@ -59,7 +62,7 @@ def test_qwen3_8b_32_sequences_qkv(lib):
 def test_gemm_plan_rules(lib, sms):
     shapes = [(6144, 4096, QKV), (4096, 4096, RESID), (4096, 12288, RESID),
               (24576, 4096, SWIGLU), (151936, 4096, SLAB), (2048, 8192, 4), (10240, 4096, 5),
-              (151936, 4096, VOCAB)]
+              (151936, 4096, VOCAB), (151936, 4096, VOCAB_TOP2)]
     for M, (N, K, kind) in itertools.product(list(range(1, 80)) + [96, 128, 129, 200, 256, 257,
                                                                   300, 512, 777, 1024, 2048],
                                              shapes):
@@ -71,7 +74,7 @@ def test_gemm_plan_rules(lib, sms):
         mt0 = (M + 255) // 256
         assert BN % 16 == 0 and 16 <= BN <= 256 and BN * mt >= M and mt >= mt0
         if mt > mt0:
-            assert sp == 1 and not p["persistent"] and kind not in (SLAB, VOCAB) and mt0 > 1
+            assert sp == 1 and not p["persistent"] and kind not in (SLAB, VOCAB, VOCAB_TOP2) and mt0 > 1
             assert nt * mt <= sms and BN >= 64
             assert nt * (mt + 1) > sms or -(-M // (mt + 1)) <= 48
         assert nt == (N + 127) // 128
@@ -98,21 +101,21 @@ def test_gemm_plan_rules(lib, sms):
         if sp > 1:
             assert BN * 128 * 4 <= stage_mem
         assert 1 <= sp <= 8 and sp <= K // 64 // 4 or sp == 1
-        if kind in (SWIGLU, SLAB, VOCAB):
+        if kind in (SWIGLU, SLAB, VOCAB, VOCAB_TOP2):
             assert sp == 1
         slots = (2 if BN <= 128 else 1) * sms
         if sp > 1:
             assert nt * mt * sp * 8 <= 7 * slots  # every cluster resident at once
         # a grid that fills under half of the CTA slots is split along K when
         # two splits are allowed (kind, K, partial tile, cluster residency)
-        if (kind not in (SWIGLU, SLAB, VOCAB) and nt * mt * 2 <= slots and K // 64 // 4 >= 2
+        if (kind not in (SWIGLU, SLAB, VOCAB, VOCAB_TOP2) and nt * mt * 2 <= slots and K // 64 // 4 >= 2
                 and BN * 128 * 4 <= stage_mem and nt * mt * 16 <= 7 * slots):
             assert sp >= 2
 
 
 def test_gemm_plan_refuses_bad_sizes(lib):
     for args in [(152, 0, 4096, 4096, 1), (152, 16, 4096, 100, 1), (152, 16, 4096, 0, 1),
-                 (0, 16, 4096, 4096, 1), (152, 16, 4096, 4096, 7), (152, 16, 4160, 4096, SWIGLU)]:
+                 (0, 16, 4096, 4096, 1), (152, 16, 4096, 4096, 8), (152, 16, 4160, 4096, SWIGLU)]:
         with pytest.raises(capi.DFlashError):
             capi.dflash_plan_gemm(*args)
 
