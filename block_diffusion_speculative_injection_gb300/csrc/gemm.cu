@@ -363,14 +363,15 @@ __global__ void __launch_bounds__(384, 1)
 // split): one CTA per SM walks the tiles t = blockIdx.x, + gridDim.x, ...
 // (token tile fastest, as in the grid above).  Warp 0 issues TMA through the
 // stage ring continuously across tiles, warp 1 issues the MMAs into one of
-// two accumulators in tensor memory (columns 0 and 256), and warps 2..9 run
-// the epilogue of tile i from one accumulator while the MMAs of tile i + 1
-// fill the other, so the epilogue no longer idles the tensor pipe.  The
-// epilogue's scratch (two 16 x 128 fp32 exchange buffers, 256 row offsets)
-// has its own shared memory after the ring.
+// two accumulators in tensor memory (columns 0 and 256), and warps 2..13 (three
+// groups of four) run the epilogue of tile i from one accumulator while the
+// MMAs of tile i + 1 fill the other, so the epilogue no longer idles the
+// tensor pipe.  The epilogue's scratch (one 16 x 128 fp32 exchange buffer per
+// group, 256 row offsets) has its own shared memory after the ring.
 // ---------------------------------------------------------------------------
-constexpr int kPersistThreads = 320;
-constexpr uint32_t kPersistScratch = 2 * 16 * 128 * 4 + 256 * 8 + 256 * 4;
+constexpr int kPersistEpiWarps = 12;
+constexpr int kPersistThreads = 64 + 32 * kPersistEpiWarps;
+constexpr uint32_t kPersistScratch = (kPersistEpiWarps / 4) * 16 * 128 * 4 + 256 * 8 + 256 * 4;
 constexpr size_t kPersistSmemMax = 227 * 1024;  // the opt-in limit per CTA
 
 __global__ void __launch_bounds__(kPersistThreads, 1)
@@ -388,7 +389,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(scratch) + kPersistScratch);
   uint64_t* empty = full + S;
   uint64_t* acc_full = empty + S;   // [2] accumulator ready for the epilogue
-  uint64_t* acc_empty = acc_full + 2;  // [2] accumulator read out (8 epilogue warps)
+  uint64_t* acc_empty = acc_full + 2;  // [2] accumulator read out (every epilogue warp)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -413,7 +414,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 8);
+      mbar_init(&acc_empty[b], kPersistEpiWarps);
     }
     mbar_fence_init();
   }
@@ -497,7 +498,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
     }
     __syncwarp();
   } else {
-    // epilogue warps 2..9 (ordered after the preceding kernel before they
+    // epilogue warps 2..13 (ordered after the preceding kernel before they
     // read the residual or write anything)
     pdl_wait();
     const int ep_tid = (int)threadIdx.x - 64;

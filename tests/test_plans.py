@@ -84,9 +84,9 @@ def test_gemm_plan_rules(lib, sms):
         want_pers = sp == 1 and BN > 64 and kind not in (SLAB, VOCAB) and nt * mt > sms
         assert pers == (sms if want_pers else 0)
         if pers:
-            assert th == 320 and smem <= 227 * 1024
-            # ring + the epilogue's own scratch (two 16 x 128 fp32 buffers, 256 x 12 B)
-            assert smem >= st * (128 * 64 * 2 + BN * 64 * 2) + 2 * 16 * 128 * 4 + 256 * 12
+            assert th == 448 and smem <= 227 * 1024
+            # ring + the epilogue's own scratch (three 16 x 128 fp32 buffers, 256 x 12 B)
+            assert smem >= st * (128 * 64 * 2 + BN * 64 * 2) + 3 * 16 * 128 * 4 + 256 * 12
         else:
             assert th == (384 if BN > 128 else 128)
             if BN <= 128:  # two CTAs per SM: dynamic + 3 KB static + 1 KB reserve each
