@@ -418,6 +418,8 @@ dflash_status dflash_create(const dflash_config* cfg, dflash_ctx** out) {
   alloc(&ctx->fb, R * d * es);
   alloc(&ctx->lm_in, R * d * es);
   alloc((void**)&ctx->ws, wsn * sizeof(float));
+  alloc((void**)&ctx->sk_part, (size_t)ctx->sm_count * 128 * 256 * sizeof(float));
+  alloc(&ctx->sk_sync, sk_sync_bytes(ctx->sm_count));
   alloc((void**)&ctx->part_o, ctx->part_rows_cap * c.head_dim * sizeof(float));
   alloc((void**)&ctx->part_ml, ctx->part_rows_cap * 2 * sizeof(float));
   alloc((void**)&ctx->vk_part, ctx->vpart_cap * sizeof(int32_t));
@@ -453,6 +455,7 @@ dflash_status dflash_create(const dflash_config* cfg, dflash_ctx** out) {
              cudaMemset(ctx->seq_len, 0, sizeof(int32_t) * c.max_batch) == cudaSuccess &&
              cudaMemset(ctx->gen_count, 0, sizeof(int32_t) * c.max_batch) == cudaSuccess &&
              cudaMemset(ctx->dev_status, 0, sizeof(int32_t) * 4) == cudaSuccess &&
+             cudaMemset(ctx->sk_sync, 0, sk_sync_bytes(ctx->sm_count)) == cudaSuccess &&
              cudaMemset(ctx->inj_seq, 0xFF, sizeof(int32_t) * R) == cudaSuccess &&
              cudaMemset(ctx->capture, 0, R * c.n_inject * d * es) == cudaSuccess &&
              cudaMemset(ctx->resid, 0, R * d * sizeof(float)) == cudaSuccess;
@@ -484,7 +487,8 @@ void dflash_destroy(dflash_ctx* ctx) {
                   ctx->ao,      ctx->act,        ctx->fb,      ctx->lm_in,   ctx->ws,
                   ctx->part_o,  ctx->part_ml,    ctx->vk_part, ctx->vv_part, ctx->pass_seq,
                   ctx->row_pos, ctx->row_slot,   ctx->row_seq, ctx->lm_rows, ctx->inj_seq,
-                  ctx->inj_pos, ctx->path,       ctx->rope_cos, ctx->rope_sin, ctx->page_tab};
+                  ctx->inj_pos, ctx->path,       ctx->rope_cos, ctx->rope_sin, ctx->page_tab,
+                  ctx->sk_part, ctx->sk_sync};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   pages_destroy(ctx);
@@ -803,6 +807,10 @@ dflash_status dflash_check(dflash_ctx* ctx) {
   if (cudaMemcpy(&s, ctx->dev_status, sizeof(s), cudaMemcpyDeviceToHost) != cudaSuccess)
     return DFLASH_E_CUDA;
   cudaMemset(ctx->dev_status, 0, sizeof(int32_t));
+  // a wait that gave up may have left stream-K arrival counts behind (the
+  // launch ticket stays aligned: every CTA takes its ticket first)
+  if (s == kDevTimeout)
+    cudaMemset(static_cast<uint8_t*>(ctx->sk_sync) + 8, 0, sk_sync_bytes(ctx->sm_count) - 8);
   switch (s) {
     case kDevOk: return DFLASH_OK;
     case kDevCapacity:

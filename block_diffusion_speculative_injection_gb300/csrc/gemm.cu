@@ -38,6 +38,10 @@ struct TcParams {
   int seg_begin[kMaxSeg + 1];
   int BN, stages, kb_per_split, n_kb;
   int m_tiles, n_tiles;  // the persistent form walks m_tiles * n_tiles tiles
+  int sk_tiles;          // ... the last sk_tiles of them split along K (stream-K)
+  float* sk_part;        // [CTA][BN columns][128 lanes] fp32 partial tiles
+  unsigned long long* sk_ticket;
+  int32_t* sk_cnt;       // [sk_tiles] partials arrived
   float* out;
   long long split_stride;
   int32_t* status;
@@ -374,6 +378,9 @@ constexpr int kPersistThreads = 64 + 32 * kPersistEpiWarps;
 constexpr uint32_t kPersistScratch = (kPersistEpiWarps / 4) * 16 * 128 * 4 + 256 * 8 + 256 * 4;
 constexpr size_t kPersistSmemMax = 227 * 1024;  // the opt-in limit per CTA
 
+// kSK: the launch has a stream-K remainder (p.sk_tiles > 0); the instance
+// without one compiles to the plain round-robin walk.
+template <bool kSK>
 __global__ void __launch_bounds__(kPersistThreads, 1)
     gemm_tc_persistent_kernel(const __grid_constant__ TmapSet wmaps,
                               const __grid_constant__ CUtensorMap xmap, const TcParams p) {
@@ -391,6 +398,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
   uint64_t* acc_full = empty + S;   // [2] accumulator ready for the epilogue
   uint64_t* acc_empty = acc_full + 2;  // [2] accumulator read out (every epilogue warp)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  int* vid_slot = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool swiglu = p.epi.kind == kEpiSwiGLU;
@@ -417,6 +425,17 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
       mbar_init(&acc_empty[b], kPersistEpiWarps);
     }
     mbar_fence_init();
+    // With a stream-K remainder a CTA waits only for CTAs of lower work index,
+    // and work indices are handed out in the order CTAs start: those CTAs are
+    // running, so the waits end whatever else shares the GPU.  Every launch
+    // takes exactly gridDim.x tickets, all before it lets the next kernel
+    // launch, so ticket % gridDim.x numbers the CTAs 0 .. gridDim.x - 1.
+    int v = (int)blockIdx.x;
+    if (kSK) {
+      v = (int)(atomicAdd(p.sk_ticket, 1ull) % (unsigned long long)gridDim.x);
+      __threadfence();
+    }
+    *vid_slot = v;
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
@@ -426,7 +445,43 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const int vid = kSK ? *vid_slot : (int)blockIdx.x;
   pdl_trigger();
+
+  // Work of CTA vid: the k-blocks [lo, hi) of the last R tiles, taken in
+  // (tile, k-block) order and cut into G contiguous ranges, then the whole
+  // tiles vid, vid + G, ... below D = tiles - R.  R < G, so a range spans at
+  // most nkb k-blocks and touches at most two tiles.  A piece that ends its
+  // tile is that tile's owner: it adds the partial sums of the lower CTAs'
+  // pieces of the tile and runs the epilogue; the other piece (the head of
+  // the next tile, where the range ends) stores its partial sum to the CTA's
+  // slot and counts itself in.  The pieces run first, the non-owner one
+  // first of all: the partials an owner waits for are then the lower CTAs'
+  // first items, and the owner's epilogue overlaps the first whole tile (a
+  // short piece late in the order would wait for an accumulator still held by
+  // the previous tile's epilogue).
+  const int G = (int)gridDim.x, R = kSK ? p.sk_tiles : 0, D = n_tiles_total - R;
+  const long long U = (long long)R * nkb;
+  auto sk_at = [&](int c) -> int { return (int)(U * c / G); };
+  const int nd = vid < D ? (D - 1 - vid) / G + 1 : 0;
+  const int lo = sk_at(vid), hi = sk_at(vid + 1);
+  const int n_sk = (kSK && hi > lo) ? (hi - 1) / nkb - lo / nkb + 1 : 0;
+  const int n_items = nd + n_sk;
+  auto item = [&](int i, int& tile, int& kb0, int& kb1, bool& owner) {
+    if (i >= n_sk) {
+      tile = vid + (i - n_sk) * G;
+      kb0 = 0;
+      kb1 = nkb;
+      owner = true;
+      return;
+    }
+    const int a = lo / nkb + (n_sk == 2 ? 1 - i : 0);
+    const int s0 = max(lo, a * nkb), e0 = min(hi, (a + 1) * nkb);
+    tile = D + a;
+    kb0 = s0 - a * nkb;
+    kb1 = e0 - a * nkb;
+    owner = e0 == (a + 1) * nkb;
+  };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -435,10 +490,12 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
       const uint64_t wpol = l2_policy_evict_first();
       uint32_t g = 0;
       bool ok = true, waited = false;
-      for (int tile = blockIdx.x; ok && tile < n_tiles_total; tile += gridDim.x) {
-        int n0, m0, seg, wrow0;
+      for (int it = 0; ok && it < n_items; ++it) {
+        int tile, kb0, kb1, n0, m0, seg, wrow0;
+        bool owner;
+        item(it, tile, kb0, kb1, owner);
         tile_geo(tile, n0, m0, seg, wrow0);
-        for (int kb = 0; kb < nkb; ++kb, ++g) {
+        for (int kb = kb0; kb < kb1; ++kb, ++g) {
           const int s = (int)(g % (uint32_t)S);
           const uint32_t ph = (g / (uint32_t)S) & 1u;
           if (g >= (uint32_t)S && !mbar_wait(&empty[s], ph ^ 1u, p.status)) {
@@ -469,17 +526,19 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      // MMA issuer: tile i accumulates into buffer i & 1
+      // MMA issuer: work item i accumulates into buffer i & 1
       const uint32_t idesc = idesc_bf16_f32(128, BN);
       uint32_t g = 0;
-      int i = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < n_tiles_total; tile += gridDim.x, ++i) {
+      for (int i = 0; ok && i < n_items; ++i) {
+        int tile, kb0, kb1;
+        bool owner;
+        item(i, tile, kb0, kb1, owner);
         const int buf = i & 1;
         if (i >= 2 && !mbar_wait(&acc_empty[buf], ((i >> 1) - 1) & 1, p.status)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(buf * 256);
-        for (int kb = 0; kb < nkb; ++kb, ++g) {
+        for (int kb = kb0; kb < kb1; ++kb, ++g) {
           const int s = (int)(g % (uint32_t)S);
           if (!mbar_wait(&full[s], (g / (uint32_t)S) & 1u, p.status)) {
             ok = false;
@@ -490,7 +549,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
           const uint64_t bd = sw128_desc(smem_u32(b_s + s * b_bytes));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            tc_mma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            tc_mma_bf16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
           tc_commit(&empty[s]);
         }
         if (ok) tc_commit(&acc_full[buf]);
@@ -501,9 +560,11 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
     // epilogue warps 2..13 (ordered after the preceding kernel before they
     // read the residual or write anything)
     pdl_wait();
-    const int ep_tid = (int)threadIdx.x - 64;
-    int i = 0;
-    for (int tile = blockIdx.x; tile < n_tiles_total; tile += gridDim.x, ++i) {
+    const int ep_tid = (int)threadIdx.x - 64, ep_threads = kPersistThreads - 64;
+    const int quarter = warp & 3, grp = (ep_tid >> 5) >> 2, ngrp = ep_threads >> 7;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const size_t slot_elems = (size_t)BN * 128;
+    for (int i = 0; i < n_items; ++i) {
       const int buf = i & 1;
       // a wait that gives up has set the status word; the warps go on
       // together regardless (one warp leaving alone would strand the others
@@ -511,10 +572,66 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
       mbar_wait_sleep(&acc_full[buf], (i >> 1) & 1, p.status);
       __syncwarp();
       tc_fence_after();
-      int n0, m0, seg, wrow0;
-      tile_geo(tile, n0, m0, seg, wrow0);
-      run_epilogue_direct<bf16>(p.epi, tmem + (uint32_t)(buf * 256), n0, m0, BN, scratch, ep_tid,
-                                kPersistThreads - 64);
+      int tile, kb0, kb1, n0, m0, seg, wrow0;
+      bool owner;
+      item(i, tile, kb0, kb1, owner);
+      const uint32_t acc = tmem + (uint32_t)(buf * 256);
+      if (kSK && !owner) {
+        // partial sum -> this CTA's slot, [column][lane] so a warp's stores
+        // of one column are 128 contiguous bytes
+        float* slot = p.sk_part + (size_t)vid * slot_elems + quarter * 32 + lane;
+        for (int c = grp * 16; c < BN; c += ngrp * 16) {
+          float v[16];
+          tmem_ld16(acc + lane_off + (uint32_t)c, v);
+#pragma unroll
+          for (int k = 0; k < 16; ++k) __stcg(slot + (size_t)(c + k) * 128, v[k]);
+        }
+        __threadfence();
+        epi_sync_all(ep_threads);
+        if (ep_tid == 0) atomicAdd(p.sk_cnt + (tile - D), 1);
+      } else {
+        if (kSK && i < n_sk && kb0 > 0) {
+          // lower CTAs whose ranges end inside this tile, each with one
+          // partial in its slot: wait for all, then add them in CTA order
+          const int a = tile - D, t0 = a * nkb;
+          int first = vid, expect = 0;
+          for (int c = vid - 1; c >= 0 && sk_at(c + 1) > t0; --c) {
+            first = c;
+            if (sk_at(c + 1) > sk_at(c)) ++expect;
+          }
+          if (ep_tid == 0) {
+            int32_t* cnt = p.sk_cnt + a;
+            bool ok = ld_acquire_gpu(cnt) >= expect;
+            const uint64_t t_start = global_ns();
+            for (uint32_t it = 1; !ok && it < kSpinLimit; ++it) {
+              __nanosleep(256);
+              ok = ld_acquire_gpu(cnt) >= expect;
+              if ((it & 255u) == 0 && global_ns() - t_start > 2000000000ull) break;
+            }
+            if (!ok) set_dev_status(p.status, kDevTimeout);
+            *cnt = 0;  // every partial of this tile has arrived: ready for the next launch
+            __threadfence();
+          }
+          epi_sync_all(ep_threads);
+          for (int c = grp * 16; c < BN; c += ngrp * 16) {
+            float v[16];
+            tmem_ld16(acc + lane_off + (uint32_t)c, v);
+            for (int q = first; q < vid; ++q) {
+              if (sk_at(q + 1) == sk_at(q)) continue;
+              const float* src = p.sk_part + (size_t)q * slot_elems + quarter * 32 + lane;
+#pragma unroll
+              for (int k = 0; k < 16; ++k) v[k] += __ldcg(src + (size_t)(c + k) * 128);
+            }
+            tmem_st16(acc + lane_off + (uint32_t)c, v);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          epi_sync_all(ep_threads);
+          tc_fence_after();
+        }
+        tile_geo(tile, n0, m0, seg, wrow0);
+        run_epilogue_direct<bf16>(p.epi, acc, n0, m0, BN, scratch, ep_tid, ep_threads);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[buf]);
@@ -704,6 +821,7 @@ struct TcPlan {
   int BN, m_tiles, n_tiles, stages, n_kb, splits, kb_per, threads;
   size_t smem_bytes;
   int persistent;  // CTAs of the persistent form (0: one CTA per tile)
+  int sk_tiles;    // tiles of the persistent form's stream-K remainder
 };
 
 static size_t persist_smem_bytes(int BN, int stages) {
@@ -717,7 +835,10 @@ static cudaError_t ensure_tc_smem() {
 }
 static cudaError_t ensure_persist_smem() {
   static std::atomic<bool> done[kMaxDevices];
-  return ensure_smem_attr(done, gemm_tc_persistent_kernel, (int)kPersistSmemMax);
+  static std::atomic<bool> done_sk[kMaxDevices];
+  const cudaError_t e = ensure_smem_attr(done, gemm_tc_persistent_kernel<false>, (int)kPersistSmemMax);
+  if (e != cudaSuccess) return e;
+  return ensure_smem_attr(done_sk, gemm_tc_persistent_kernel<true>, (int)kPersistSmemMax);
 }
 
 // the plan for a given number of token tiles
@@ -765,6 +886,7 @@ static TcPlan plan_tiles(int sm_count, int M, int N, int K, int kind, int max_sp
   // in the ring's memory, so it keeps one CTA per tile; the top-2 one does
   // not (kPlanVocabTop2).
   t.persistent = 0;
+  t.sk_tiles = 0;
   if (t.splits == 1 && t.BN > 64 && kind != kEpiSlab && kind != kEpiVocab &&
       (int64_t)t.n_tiles * t.m_tiles > sm_count) {
     t.persistent = sm_count;
@@ -775,6 +897,15 @@ static TcPlan plan_tiles(int sm_count, int M, int N, int K, int kind, int max_sp
     if (st > 8) st = 8;
     t.stages = st;
     t.smem_bytes = persist_smem_bytes(t.BN, st);
+    // The tiles past the last full round (R = tiles mod CTAs) would run on R
+    // CTAs while the rest idle; split along K over all CTAs instead, when the
+    // idle share is worth the partial-sum exchange (R at most 3/4 of the CTAs)
+    // and every CTA gets at least 8 k-blocks of it.  Not for the top-2
+    // lm_head: its many rounds leave little idle, and its measured time grew.
+    const int R = (int)(((int64_t)t.n_tiles * t.m_tiles) % sm_count);
+    if (kind != kPlanVocabTop2 && R > 0 && R * 4 <= sm_count * 3 &&
+        (int64_t)R * t.n_kb >= 8LL * sm_count)
+      t.sk_tiles = R;
   }
   return t;
 }
@@ -937,11 +1068,16 @@ dflash_status gemm(dflash_ctx* ctx, const void* x, int M, int K, const GemmSegs&
 
   p.m_tiles = m_tiles;
   p.n_tiles = n_tiles;
+  p.sk_tiles = plan.sk_tiles;
+  p.sk_part = ctx->sk_part;
+  p.sk_ticket = static_cast<unsigned long long*>(ctx->sk_sync);
+  p.sk_cnt = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ctx->sk_sync) + 8);
   if (plan.persistent > 0) {
     DF_CUDA_TRY(ctx, ensure_persist_smem());
     const int ctas = (int)std::min<int64_t>((int64_t)m_tiles * n_tiles, plan.persistent);
-    DF_CUDA_TRY(ctx, launch_k(ctx->pdl, gemm_tc_persistent_kernel, dim3(ctas), dim3(kPersistThreads),
-                              plan.smem_bytes, st, maps, *xm, p));
+    auto kern = plan.sk_tiles > 0 ? gemm_tc_persistent_kernel<true> : gemm_tc_persistent_kernel<false>;
+    DF_CUDA_TRY(ctx, launch_k(ctx->pdl, kern, dim3(ctas), dim3(kPersistThreads), plan.smem_bytes, st,
+                              maps, *xm, p));
     DF_LAUNCHED(ctx);
     *splits_used = 1;
     return DFLASH_OK;

@@ -129,6 +129,11 @@ struct dflash_ctx {
   void* lm_in = nullptr;    // [max_rows][d] gathered lm_head input
   float* ws = nullptr;      // GEMM fp32 output / split-K partials
   size_t ws_elems = 0;
+  // stream-K remainder of the persistent GEMM: one fp32 128 x 256 partial
+  // tile per CTA, then the launch ticket (uint64) and one arrival count
+  // per remainder tile
+  float* sk_part = nullptr;
+  void* sk_sync = nullptr;
   float* part_o = nullptr;  // split-KV partial outputs
   float* part_ml = nullptr;
   size_t part_rows_cap = 0;  // capacity in (split*row*head) units
@@ -202,6 +207,9 @@ inline KvPages ctx_pages(const dflash_ctx* ctx) {
 }
 
 struct EpiArgs;
+// bytes of ctx->sk_sync for a GPU of sm_count SMs: the launch ticket, then
+// one arrival count per stream-K tile (fewer than the persistent CTAs)
+inline size_t sk_sync_bytes(int sm_count) { return 8 + 4 * (size_t)std::max(sm_count, 1); }
 // X[M][K] . W^T with W the vertical stack of the segments, then the fused
 // epilogue described by `epi` (see epilogue.cuh).  The fp32 result / K-split
 // slabs live in ctx->ws; *splits_used reports the split count.
@@ -698,6 +706,25 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
       "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
       "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
+}
+// 32 lanes x 16 consecutive 32-bit columns per warp (the store form of tmem_ld16).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+// a 32-bit load with acquire semantics at GPU scope (a flag set by another CTA)
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");

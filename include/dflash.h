@@ -539,7 +539,10 @@ DFLASH_API int64_t dflash_profile_list(dflash_ctx *ctx, int32_t kind, double *ms
  * CTA of its own; else one CTA per SM walks the tiles, with the epilogue of a
  * tile overlapping the next tile's main loop: passes of more tiles than SMs
  * with tiles wider than 64 token rows, no K split, and any epilogue but the
- * general lm_head's, kind 6).  DFLASH_E_INVALID_ARG for sizes the GEMM does not take. */
+ * general lm_head's, kind 6).  In the persistent form the R = tiles mod CTAs
+ * tiles past the last full round are split along K over all CTAs (stream-K)
+ * when R <= 3/4 of the CTAs, R x K / 64 >= 8 x CTAs and the kind is not 7.
+ * DFLASH_E_INVALID_ARG for sizes the GEMM does not take. */
 DFLASH_API dflash_status dflash_plan_gemm(int32_t sm_count, int32_t M, int32_t N, int32_t K,
                                           int32_t kind, int32_t max_splits, int32_t *plan_out);
 
