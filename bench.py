@@ -515,7 +515,7 @@ def run_ours(args, w: wl.Workload) -> None:
     print(json.dumps(line))
 
 
-KERNEL_REV = "gemm-v10"  # vocabulary epilogue, token-tile-first grid, persistent form (12 epilogue warps, top-2 lm_head), batched cluster epilogue, 12 warps above 128 rows, split-chunk pair epilogues
+KERNEL_REV = "gemm-v11"  # vocabulary epilogue, token-tile-first grid, persistent form (12 epilogue warps, top-2 lm_head, stream-K remainder), batched cluster epilogue, 12 warps above 128 rows, split-chunk pair epilogues
 ATTN_KERNELS = "attn_tc_kernel (+ attn_combine_kernel)"
 
 
