@@ -364,8 +364,10 @@ __global__ void __launch_bounds__(384, 1)
 
 // ---------------------------------------------------------------------------
 // Persistent form for passes of more tiles than SMs (wide token tiles, no K
-// split): one CTA per SM walks the tiles t = blockIdx.x, + gridDim.x, ...
-// (token tile fastest, as in the grid above).  Warp 0 issues TMA through the
+// split): one CTA per SM walks the tiles t = v, v + gridDim.x, ... (token
+// tile fastest, as in the grid above; v = blockIdx.x, or the CTA's ticket
+// when the tiles past the last full round are split along K as a stream-K
+// remainder, below).  Warp 0 issues TMA through the
 // stage ring continuously across tiles, warp 1 issues the MMAs into one of
 // two accumulators in tensor memory (columns 0 and 256), and warps 2..13 (three
 // groups of four) run the epilogue of tile i from one accumulator while the
