@@ -476,7 +476,7 @@ def run_ours(args, w: wl.Workload) -> None:
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded random-init weights, uniform random prompt tokens)",
-        "config": {"workload": w.name, "target": w.shape.name, "batch": b, "prompt_len": lens[0],
+        "config": {"workload": w.name, "batch": b, "prompt_len": lens[0],
                    "block": B, "draft_layers": w.shape.n_draft_layers,
                    "inject_layers": list(w.shape.inject_layers), "parallelism": "replicas",
                    "l2": "no flush: every step streams ~19 GB of weights (> 129 MB L2)"},
