@@ -524,11 +524,13 @@ def attn_op_points(steps: int, warmup: int, local: int, only=None):
     lengths x batches: Q [b,16,32,128], K/V [b,8,ctx+16,128] bf16, block
     visible without mask.  Each point: `warmup` calls, then `steps` calls
     timed one by one with CUDA events on the launching stream, a 256 MB
-    buffer written between calls so that every call starts with a cold L2,
-    and the GPU kept busy (a timed sleep) while the host prepares the call,
-    so that the events bracket the GPU's work and not the host's argument
-    marshalling; the median against the measured HBM peak.  Returns
-    (points, clocks)."""
+    buffer written and another 256 MB read between calls so that every call
+    starts with a cold L2 that holds no dirty lines (a write alone leaves the
+    L2 full of the flush buffer's lines, whose write-back then lands inside
+    the timed call), and the GPU kept busy (a timed sleep) while the host
+    prepares the call, so that the events bracket the GPU's work and not the
+    host's argument marshalling; the median against the measured HBM peak.
+    Returns (points, clocks)."""
     import torch
 
     from block_diffusion_speculative_injection_gb300 import capi
@@ -538,6 +540,7 @@ def attn_op_points(steps: int, warmup: int, local: int, only=None):
     BLK = 16
     hbm, _, _ = peaks()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    flush_rd = torch.ones(256 << 20, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
     sampler = ClockSampler(local)
     points = []
@@ -557,6 +560,7 @@ def attn_op_points(steps: int, warmup: int, local: int, only=None):
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             flush.fill_(1)
+            flush_rd.sum(dtype=torch.int32)  # evicts the fill's dirty lines before e0
             torch.cuda._sleep(200000)  # ~0.1 ms: covers the host side of the call
             e0.record(stream)
             capi.dflash_block_attention(b, H, HKV, ctx, BLK, 0, q, k, v, out, ws)
